@@ -1,0 +1,247 @@
+"""Python binding of the fused cascaded GEMM library (``libb2b.so``).
+
+Argument marshalling only: every step of the computation runs in the CUDA
+kernels behind the C ABI declared in ``include/b2b.h``.  PyTorch supplies
+device memory and streams.  There is no fallback: if the library is missing
+this module raises on import, telling how to build it.
+
+Low-level functions carry the C names (``b2b_plan_create``, ``b2b_run``,
+...); :class:`Plan` and :class:`GemmPlan` wrap them for torch tensors.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional, Sequence, Tuple
+
+__all__ = [
+    "B2BError", "DTYPES", "Plan", "GemmPlan", "library_path", "build",
+    "b2b_plan_create", "b2b_gemm_plan_create", "b2b_run", "b2b_plan_destroy",
+    "b2b_plan_device_status", "b2b_plan_set_wait_budget", "b2b_plan_info",
+    "b2b_status_string", "b2b_coordination_matrix", "b2b_probe_operand_image",
+    "b2b_probe_f64_rearrange", "coordination_matrix",
+]
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_HERE, "_lib", "libb2b.so")
+
+# b2b_dtype_t
+DTYPES = {"f16_f32out": 0, "f16": 1, "bf16": 2, "tf32": 3, "f64": 4, "bf16_f32out": 5}
+STATUS = {0: "B2B_OK", 1: "B2B_ERR_INVALID_ARG", 2: "B2B_ERR_UNSUPPORTED", 3: "B2B_ERR_ALIGNMENT",
+          4: "B2B_ERR_ALIAS", 5: "B2B_ERR_DEVICE", 6: "B2B_ERR_CUDA", 7: "B2B_ERR_TIMEOUT"}
+
+
+class B2BError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = int(code)
+        super().__init__(f"{where}: {STATUS.get(self.code, self.code)} ({_lib.b2b_status_string(code).decode()})")
+
+
+def library_path() -> str:
+    return _LIB_PATH
+
+
+def build(force: bool = False) -> str:
+    from . import _build
+    return _build.build(force=force)
+
+
+def _load() -> ctypes.CDLL:
+    if not os.path.exists(_LIB_PATH):
+        raise ImportError(
+            f"{_LIB_PATH} is missing: build the CUDA library first "
+            "(python -c 'import __graft_entry__ as g; g.build()' or "
+            "python fusion_b2b_gemm_gb300/_build.py)")
+    lib = ctypes.CDLL(_LIB_PATH)
+    P = ctypes.c_void_p
+    i64, i32, u64 = ctypes.c_int64, ctypes.c_int, ctypes.c_uint64
+    ip = ctypes.POINTER(ctypes.c_int)
+    sig = {
+        "b2b_plan_create": [ctypes.POINTER(P), i32, i64, i64, i64, i64, i64, i64],
+        "b2b_gemm_plan_create": [ctypes.POINTER(P), i32, i64, i64, i64, i64],
+        "b2b_run": [P, P, P, P, P, P, P],
+        "b2b_plan_destroy": [P],
+        "b2b_plan_device_status": [P, P],
+        "b2b_plan_set_wait_budget": [P, u64],
+        "b2b_plan_info": [P, ip, ip, ip, ip, ip, ip, ip],
+        "b2b_coordination_matrix": [i32, i32, ip, ip, ip, ip, ip],
+        "b2b_probe_operand_image": [i32, i32, P, P, P],
+        "b2b_probe_f64_rearrange": [i32, P, P, P],
+    }
+    for name, args in sig.items():
+        fn = getattr(lib, name)
+        fn.argtypes = args
+        fn.restype = ctypes.c_int
+    lib.b2b_status_string.argtypes = [ctypes.c_int]
+    lib.b2b_status_string.restype = ctypes.c_char_p
+    return lib
+
+
+_lib = _load()
+
+# -- raw C entry points (same names as the C ABI) ---------------------------
+b2b_plan_create = _lib.b2b_plan_create
+b2b_gemm_plan_create = _lib.b2b_gemm_plan_create
+b2b_run = _lib.b2b_run
+b2b_plan_destroy = _lib.b2b_plan_destroy
+b2b_plan_device_status = _lib.b2b_plan_device_status
+b2b_plan_set_wait_budget = _lib.b2b_plan_set_wait_budget
+b2b_plan_info = _lib.b2b_plan_info
+b2b_status_string = _lib.b2b_status_string
+b2b_coordination_matrix = _lib.b2b_coordination_matrix
+b2b_probe_operand_image = _lib.b2b_probe_operand_image
+b2b_probe_f64_rearrange = _lib.b2b_probe_f64_rearrange
+
+
+def _check(code: int, where: str) -> None:
+    if code != 0:
+        raise B2BError(code, where)
+
+
+def _stream_handle(stream) -> Optional[int]:
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream or None
+
+
+def _ptr(t) -> Optional[int]:
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("tensors passed to b2b_run must live on the GPU")
+    if not t.is_contiguous():
+        raise ValueError("tensors passed to b2b_run must be contiguous (row-major)")
+    return t.data_ptr()
+
+
+class Plan:
+    """A fused chain D = (A.B).C, or E = ((A.B).C).F when ``N3 > 0``."""
+
+    _single = False
+
+    def __init__(self, dtype: str, batch: int, M: int, K: int, N1: int, N2: int = 0, N3: int = 0):
+        if dtype not in DTYPES:
+            raise ValueError(f"unknown dtype {dtype!r}; one of {sorted(DTYPES)}")
+        self.dtype = dtype
+        self.batch, self.M, self.K = batch, M, K
+        self.N = (N1,) if self._single else ((N1, N2, N3) if N3 else (N1, N2))
+        h = ctypes.c_void_p()
+        if self._single:
+            code = _lib.b2b_gemm_plan_create(ctypes.byref(h), DTYPES[dtype], batch, M, K, N1)
+        else:
+            code = _lib.b2b_plan_create(ctypes.byref(h), DTYPES[dtype], batch, M, K, N1, N2, N3)
+        _check(code, "b2b_plan_create")
+        self._h = h
+
+    # -- torch helpers ---------------------------------------------------
+    def io_dtypes(self):
+        import torch
+        table = {"f16_f32out": (torch.float16, torch.float32), "f16": (torch.float16, torch.float16),
+                 "bf16": (torch.bfloat16, torch.bfloat16), "bf16_f32out": (torch.bfloat16, torch.float32),
+                 "tf32": (torch.float32, torch.float32), "f64": (torch.float64, torch.float64)}
+        return table[self.dtype]
+
+    def out_shape(self) -> Tuple[int, int, int]:
+        return (self.batch, self.M, self.N[-1])
+
+    def empty_out(self, device="cuda"):
+        import torch
+        return torch.empty(self.out_shape(), dtype=self.io_dtypes()[1], device=device)
+
+    def run(self, A, B, C=None, F=None, D=None, stream=None):
+        """Launch on ``stream`` (default: torch's current stream); returns D."""
+        if D is None:
+            D = self.empty_out(A.device)
+        code = _lib.b2b_run(self._h, _ptr(A), _ptr(B), _ptr(C), _ptr(F), _ptr(D), _stream_handle(stream))
+        _check(code, "b2b_run")
+        return D
+
+    def run_from_host(self, host_inputs: Sequence, host_out, dev_inputs: Sequence, dev_out, stream=None):
+        """One end-to-end call from pinned host buffers.
+
+        Copies the inputs host->device, runs the chain, copies the result
+        device->host, all on ``stream``; returns (h2d_bytes, d2h_bytes).
+        The device buffers are the caller's.
+        """
+        import torch
+        s = stream or torch.cuda.current_stream()
+        h2d = 0
+        with torch.cuda.stream(s):
+            for h, d in zip(host_inputs, dev_inputs):
+                d.copy_(h, non_blocking=True)
+                h2d += h.numel() * h.element_size()
+            args = list(dev_inputs) + [None] * (4 - len(dev_inputs))
+            self.run(args[0], args[1], args[2], args[3], dev_out, stream=s)
+            host_out.copy_(dev_out, non_blocking=True)
+        return h2d, host_out.numel() * host_out.element_size()
+
+    def status(self, stream=None) -> int:
+        """Synchronise and return the device status word (0 = OK)."""
+        return int(_lib.b2b_plan_device_status(self._h, _stream_handle(stream)))
+
+    def set_wait_budget(self, ns: int) -> None:
+        _check(_lib.b2b_plan_set_wait_budget(self._h, int(ns)), "b2b_plan_set_wait_budget")
+
+    def info(self) -> dict:
+        vals = [ctypes.c_int() for _ in range(7)]
+        _check(_lib.b2b_plan_info(self._h, *[ctypes.byref(v) for v in vals]), "b2b_plan_info")
+        keys = ("launches_per_run", "grid", "threads", "smem_bytes", "tmem_cols", "ring_stages", "passes")
+        return {k: v.value for k, v in zip(keys, vals)}
+
+    def close(self) -> None:
+        h = getattr(self, "_h", None)
+        if h is not None and h.value:
+            _lib.b2b_plan_destroy(h)
+            self._h = ctypes.c_void_p()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+class GemmPlan(Plan):
+    """A single GEMM D = A.B (one operator; the unfused chain is built from these)."""
+
+    _single = True
+
+    def __init__(self, dtype: str, batch: int, M: int, K: int, N: int):
+        super().__init__(dtype, batch, M, K, N)
+
+    def run(self, A, B, C=None, F=None, D=None, stream=None):
+        return super().run(A, B, None, None, D, stream)
+
+
+def coordination_matrix(src_thread: Sequence[Sequence[int]], src_reg: Sequence[Sequence[int]]):
+    """H as a list of rows [(p, q, r), ...] (one triple per round)."""
+    n, m = len(src_thread), len(src_thread[0])
+    flat_t = (ctypes.c_int * (n * m))(*[x for row in src_thread for x in row])
+    flat_r = (ctypes.c_int * (n * m))(*[x for row in src_reg for x in row])
+    P, Q, R = [(ctypes.c_int * (n * m))() for _ in range(3)]
+    _check(_lib.b2b_coordination_matrix(n, m, flat_t, flat_r, P, Q, R), "b2b_coordination_matrix")
+    return [[(P[i * m + j], Q[i * m + j], R[i * m + j]) for j in range(m)] for i in range(n)]
+
+
+def probe_operand_image(dtype: str, acc):
+    """Run the converter routine on acc (torch fp32 [128, width] on the GPU)."""
+    import torch
+    width = acc.shape[1]
+    if dtype == "tf32":
+        out = torch.empty((128, width), dtype=torch.int32, device=acc.device)
+    else:
+        out = torch.empty((width * 256 // 4,), dtype=torch.int32, device=acc.device)
+    _check(_lib.b2b_probe_operand_image(DTYPES[dtype], width, _ptr(acc.contiguous()), _ptr(out),
+                                        _stream_handle(None)), "b2b_probe_operand_image")
+    return out
+
+
+def probe_f64_rearrange(cfrag):
+    """cfrag: torch fp64 [32, tiles*2] on the GPU -> afrag of the same shape."""
+    import torch
+    tiles = cfrag.shape[1] // 2
+    out = torch.empty_like(cfrag)
+    _check(_lib.b2b_probe_f64_rearrange(tiles, _ptr(cfrag.contiguous()), _ptr(out), _stream_handle(None)),
+           "b2b_probe_f64_rearrange")
+    return out

@@ -1,0 +1,650 @@
+// C ABI of the fused cascaded GEMM library (include/b2b.h).
+//
+// b2b_plan_create is the operator-determination and relation-determination
+// step (patent "数据处理方法、装置、设备及介质", Alibaba 2023, Detailed
+// description para. 46-53, apparatus modules 51 and 52, para. 140-142): the
+// caller names the chain, the data type fixes the accumulator layout (rule 1)
+// and the operand layout (rule 2), and the plan picks the compiled
+// rearrangement and tiling.  b2b_run is the rearrangement module 53
+// (para. 143): one kernel launch that computes, rearranges and consumes every
+// intermediate on chip.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+#include <new>
+#include <vector>
+
+#include "b2b.h"
+#include "chain_f64.cuh"
+#include "registry.h"
+
+using namespace b2b;
+
+namespace {
+
+constexpr uint64_t kDefaultBudgetNs = 2000000000ull;
+constexpr int kSmemOptin = 232448;         // 227 KB per CTA on sm_100 / sm_103
+constexpr int kSmemBudget = kSmemOptin - 1024;  // minus the 1024-byte alignment slack
+
+enum PlanKind : int {
+  kPlanChainTC = 0,
+  kPlanGemmTC = 1,
+  kPlanChainF64 = 2,
+  kPlanGemmF64 = 3,
+  kPlanEmpty = 4
+};
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+int64_t pad64(int64_t n) { return (n + 63) / 64 * 64; }
+
+uint32_t pow2_cols(uint32_t n) {
+  uint32_t c = 32;
+  while (c < n) c <<= 1;
+  return c;
+}
+
+const ChainKernelEntry* find_chain_kernel(int in, int out, int S, int n1p, int n2p, int nf,
+                                          bool res) {
+  const ChainTable tables[] = {chain_table_f16(), chain_table_bf16(), chain_table_tf32()};
+  for (const ChainTable& t : tables)
+    for (int i = 0; i < t.count; ++i) {
+      const ChainKernelEntry& e = t.entries[i];
+      if (e.in == in && e.out == out && e.S == S && e.nf == nf && e.res == res &&
+          (S < 2 || e.n1p == n1p) && (S < 3 || e.n2p == n2p))
+        return &e;
+    }
+  return nullptr;
+}
+
+// Rearrangement relation of the fp64 path and its coordination matrix
+// (patent para. 61-102).  Rule 1, the m8n8k4 fp64 accumulator: lane 4g+t
+// holds row g, columns 2t and 2t+1.  Rule 2, the m8n8k4 A operand: lane
+// 4g+t holds row g, column t.  One 8-column accumulator tile feeds two k4
+// slices: receiver t of a group needs column 4h + t for its slot h, which
+// sender (4h + t) / 2 holds as its value (4h + t) % 2.
+struct F64Tables {
+  uint32_t fsrc[2], qsend[2], hslot[2];
+  bool ok;
+};
+
+F64Tables f64_tables() {
+  static F64Tables tab{};
+  static std::once_flag once;
+  std::call_once(once, [] {
+    int st[8], sr[8], P[8], Q[8], R[8];
+    for (int t = 0; t < 4; ++t)
+      for (int h = 0; h < 2; ++h) {
+        const int col = 4 * h + t;
+        st[t * 2 + h] = col / 2;
+        sr[t * 2 + h] = col % 2;
+      }
+    tab.ok = b2b_coordination_matrix(4, 2, st, sr, P, Q, R) == B2B_OK;
+    if (!tab.ok) return;
+    for (int j = 0; j < 2; ++j) {
+      tab.fsrc[j] = tab.qsend[j] = tab.hslot[j] = 0;
+      for (int i = 0; i < 4; ++i) {
+        const int p = P[i * 2 + j], q = Q[i * 2 + j], r = R[i * 2 + j];
+        tab.fsrc[j] |= static_cast<uint32_t>(p) << (2 * i);
+        tab.hslot[j] |= static_cast<uint32_t>(r) << (2 * i);
+        tab.qsend[j] |= static_cast<uint32_t>(q) << (2 * p);  // sender p offers its value q
+      }
+    }
+  });
+  return tab;
+}
+
+b2b_status_t check_device(int* dev_out, int* sms_out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return B2B_ERR_DEVICE;
+  }
+  int major = 0, minor = 0, sms = 0;
+  if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+    cudaGetLastError();
+    return B2B_ERR_CUDA;
+  }
+  if (major != 10 || minor != 3) return B2B_ERR_DEVICE;
+  if (dev_out) *dev_out = dev;
+  if (sms_out) *sms_out = sms;
+  return B2B_OK;
+}
+
+}  // namespace
+
+struct b2b_plan_s {
+  int kind;
+  b2b_dtype_t dtype;
+  int device;
+  int sms;
+  int stages;
+  int64_t batch, M, K, N[3];
+  int in_kind, out_kind, esz, osz;
+  int n1p, n2p, nf;
+  bool res;
+  ChainParams prm;
+  int smem_bytes, grid, threads;
+  const void* fn;
+  F64Params f64;
+  int* d_status;
+  uint64_t budget_ns;
+};
+
+namespace {
+
+// Tiling of a tcgen05 chain: padded widths, final-pass width, tensor-memory
+// regions, shared-memory carve-up, and whether the weights stay resident.
+b2b_status_t setup_chain_tc(b2b_plan_s* p) {
+  const int S = p->stages;
+  const int CK = 128 / p->esz;
+  p->n1p = S >= 2 ? static_cast<int>(pad64(p->N[0])) : 64;
+  p->n2p = S >= 3 ? static_cast<int>(pad64(p->N[1])) : 64;
+  const int64_t nlast = p->N[S - 1];
+  const int nl = static_cast<int>(std::max<int64_t>(64, pad64(nlast)));
+  const int base_z = (S >= 2 ? p->n1p : 0) + (S >= 3 ? p->n2p : 0);
+
+  int nf = 0, nz = -1;
+  const int cands[3] = {256, 128, 64};
+  for (int c : cands)
+    if (c <= nl && base_z + 2 * c <= 512) { nf = c; nz = 2; break; }
+  if (nz < 0)
+    for (int c : cands)
+      if (c <= nl && base_z + c <= 512) { nf = c; nz = 1; break; }
+  if (nz < 0 && S == 3)
+    for (int c : cands)
+      if (c <= nl && c <= p->n1p && c <= p->n2p) { nf = c; nz = 0; break; }
+  if (nz < 0) return B2B_ERR_UNSUPPORTED;
+  if (nf == 0) return B2B_ERR_UNSUPPORTED;
+  p->nf = nf;
+
+  ChainParams& c = p->prm;
+  std::memset(&c, 0, sizeof(c));
+  c.batch = static_cast<int>(p->batch);
+  c.M = static_cast<int>(p->M);
+  c.K = static_cast<int>(p->K);
+  c.m_tiles = static_cast<int>((p->M + 127) / 128);
+  const int64_t tiles = p->batch * c.m_tiles;
+  if (tiles > (1ll << 30)) return B2B_ERR_UNSUPPORTED;
+  c.total_tiles = static_cast<int>(tiles);
+  c.npass = static_cast<int>((nlast + nf - 1) / nf);
+  c.kpan0 = static_cast<int>((p->K + CK - 1) / CK);
+  c.nz = nz;
+  c.region_col[0] = 0;
+  c.region_col[1] = S >= 3 ? p->n1p : 0;
+  c.region_col[2] = base_z;
+  c.region_col[3] = base_z + nf;
+  if (nz == 0) {  // the final passes reuse X and Y in turn
+    c.region_col[2] = c.region_col[0];
+    c.region_col[3] = c.region_col[1];
+  }
+  const uint32_t cols_used = nz > 0 ? static_cast<uint32_t>(base_z + nz * nf) : static_cast<uint32_t>(base_z);
+  c.tmem_cols = pow2_cols(cols_used);
+  if (c.tmem_cols > 512) return B2B_ERR_UNSUPPORTED;
+
+  const bool p_smem = (S >= 2) && p->in_kind != kInTF32;
+  const uint32_t p_bytes =
+      p_smem ? static_cast<uint32_t>(std::max(p->n1p, S >= 3 ? p->n2p : 0)) * 128u * p->esz : 0u;
+  const int maxw = std::max({S >= 2 ? p->n1p : 0, S >= 3 ? p->n2p : 0, nf});
+
+  // Two layouts: weights resident for the whole batch, or streamed per tile.
+  struct Layout { bool res; uint32_t stage, wres0, wres1; int nst, nstg; };
+  auto fit = [&](bool res) -> Layout {
+    Layout L{res, 0, 0, 0, 0, 0};
+    L.stage = res ? kPanelBytes : kPanelBytes + 128u * maxw;
+    if (res) {
+      L.wres0 = static_cast<uint32_t>(c.kpan0) * 128u * p->n1p;
+      L.wres1 = static_cast<uint32_t>(p->n1p / CK) * 128u * nf;
+    }
+    const int64_t fixed = int64_t(L.wres0) + L.wres1 + p_bytes + kBarBytes;
+    for (int nstg = 2; nstg >= 1; --nstg) {
+      const int64_t room = kSmemBudget - fixed - int64_t(nstg) * kPanelBytes;
+      const int nst = room > 0 ? static_cast<int>(std::min<int64_t>(8, room / L.stage)) : 0;
+      L.nst = nst;
+      L.nstg = nstg;
+      if (nst >= 3) break;
+    }
+    return L;
+  };
+  Layout L = fit(false);
+  if (S == 2 && c.npass == 1 &&
+      find_chain_kernel(p->in_kind, p->out_kind, S, p->n1p, p->n2p, nf, true)) {
+    Layout R = fit(true);
+    if (R.nst >= 3) L = R;
+  }
+  if (L.nst < 2) return B2B_ERR_UNSUPPORTED;
+  p->res = L.res;
+  c.nst = L.nst;
+  c.nstg = L.nstg;
+  c.stage_bytes = L.stage;
+  c.off_ring = 0;
+  c.off_wres0 = static_cast<uint32_t>(L.nst) * L.stage;
+  c.off_wres1 = c.off_wres0 + L.wres0;
+  c.off_p = c.off_wres1 + L.wres1;
+  c.off_stg = c.off_p + p_bytes;
+  c.off_bar = c.off_stg + static_cast<uint32_t>(L.nstg) * kPanelBytes;
+  p->smem_bytes = static_cast<int>(c.off_bar + kBarBytes + 1024);
+  if (p->smem_bytes > kSmemOptin) return B2B_ERR_UNSUPPORTED;
+
+  const ChainKernelEntry* e =
+      find_chain_kernel(p->in_kind, p->out_kind, S, p->n1p, p->n2p, nf, p->res);
+  if (!e) return B2B_ERR_UNSUPPORTED;
+  p->fn = e->fn;
+  p->threads = kChainThreads;
+  p->grid = static_cast<int>(std::min<int64_t>(c.total_tiles, p->sms));
+  return B2B_OK;
+}
+
+b2b_status_t setup_f64(b2b_plan_s* p) {
+  const F64Tables tab = f64_tables();
+  if (!tab.ok) return B2B_ERR_UNSUPPORTED;
+  F64Params& f = p->f64;
+  std::memset(&f, 0, sizeof(f));
+  f.batch = static_cast<int>(p->batch);
+  f.M = static_cast<int>(p->M);
+  f.K = static_cast<int>(p->K);
+  f.m8_tiles = static_cast<int>((p->M + 7) / 8);
+  f.total = p->batch * f.m8_tiles;
+  for (int j = 0; j < 2; ++j) {
+    f.fsrc[j] = tab.fsrc[j];
+    f.qsend[j] = tab.qsend[j];
+    f.hslot[j] = tab.hslot[j];
+  }
+  const int n1 = static_cast<int>(p->N[0]);
+  const int n2 = p->stages >= 2 ? static_cast<int>(p->N[1]) : 0;
+  const void* fn = nullptr;
+#define B2B_F64_CASE(A, B)                                                              \
+  if (p->stages == 2 && n1 == A && n2 == B)                                             \
+    fn = reinterpret_cast<const void*>(&chain_f64_kernel<A, B, 2>);
+  B2B_F64_CASE(16, 16) B2B_F64_CASE(16, 32) B2B_F64_CASE(16, 64)
+  B2B_F64_CASE(32, 16) B2B_F64_CASE(32, 32) B2B_F64_CASE(32, 64)
+  B2B_F64_CASE(64, 16) B2B_F64_CASE(64, 32) B2B_F64_CASE(64, 64)
+#undef B2B_F64_CASE
+  if (p->stages == 1) {
+    if (n1 == 16) fn = reinterpret_cast<const void*>(&chain_f64_kernel<16, 8, 1>);
+    if (n1 == 32) fn = reinterpret_cast<const void*>(&chain_f64_kernel<32, 8, 1>);
+    if (n1 == 64) fn = reinterpret_cast<const void*>(&chain_f64_kernel<64, 8, 1>);
+  }
+  if (!fn) return B2B_ERR_UNSUPPORTED;
+  p->fn = fn;
+  p->threads = 128;
+  int per_sm = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, 128, 0) != cudaSuccess || per_sm < 1) {
+    cudaGetLastError();
+    per_sm = 4;
+  }
+  const int64_t need = (f.total + 3) / 4;
+  p->grid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(need, int64_t(p->sms) * per_sm)));
+  p->smem_bytes = 0;
+  return B2B_OK;
+}
+
+b2b_status_t validate_sizes(b2b_dtype_t dt, int stages, int64_t batch, int64_t M, int64_t K,
+                            const int64_t* N) {
+  if (batch < 0 || M < 0 || K < 1) return B2B_ERR_INVALID_ARG;
+  for (int s = 0; s < stages; ++s)
+    if (N[s] < 1) return B2B_ERR_INVALID_ARG;
+  if (batch > (1 << 24) || M > (1ll << 30) || K > (1 << 20)) return B2B_ERR_UNSUPPORTED;
+  switch (dt) {
+    case B2B_F16_F32OUT:
+    case B2B_F16:
+    case B2B_BF16:
+    case B2B_BF16_F32OUT:
+      if (K % 8) return B2B_ERR_UNSUPPORTED;
+      for (int s = 0; s < stages; ++s) {
+        if (N[s] % 8) return B2B_ERR_UNSUPPORTED;
+        if (s < stages - 1 && N[s] > 256) return B2B_ERR_UNSUPPORTED;
+        if (N[s] > 4096) return B2B_ERR_UNSUPPORTED;
+      }
+      return B2B_OK;
+    case B2B_TF32:
+      if (stages > 2) return B2B_ERR_UNSUPPORTED;
+      if (K % 4) return B2B_ERR_UNSUPPORTED;
+      for (int s = 0; s < stages; ++s) {
+        if (N[s] % 4) return B2B_ERR_UNSUPPORTED;
+        if (s < stages - 1 && N[s] > 256) return B2B_ERR_UNSUPPORTED;
+        if (N[s] > 4096) return B2B_ERR_UNSUPPORTED;
+      }
+      return B2B_OK;
+    case B2B_F64:
+      if (stages > 2) return B2B_ERR_UNSUPPORTED;
+      if (K % 4) return B2B_ERR_UNSUPPORTED;
+      for (int s = 0; s < stages; ++s)
+        if (N[s] != 16 && N[s] != 32 && N[s] != 64) return B2B_ERR_UNSUPPORTED;
+      return B2B_OK;
+    default:
+      return B2B_ERR_INVALID_ARG;
+  }
+}
+
+void type_info(b2b_dtype_t dt, int* in_kind, int* out_kind, int* esz, int* osz) {
+  switch (dt) {
+    case B2B_F16_F32OUT: *in_kind = kInF16; *out_kind = kOutF32; *esz = 2; *osz = 4; break;
+    case B2B_F16: *in_kind = kInF16; *out_kind = kOutF16; *esz = 2; *osz = 2; break;
+    case B2B_BF16: *in_kind = kInBF16; *out_kind = kOutBF16; *esz = 2; *osz = 2; break;
+    case B2B_BF16_F32OUT: *in_kind = kInBF16; *out_kind = kOutF32; *esz = 2; *osz = 4; break;
+    case B2B_TF32: *in_kind = kInTF32; *out_kind = kOutF32; *esz = 4; *osz = 4; break;
+    default: *in_kind = -1; *out_kind = -1; *esz = 8; *osz = 8; break;
+  }
+}
+
+b2b_status_t create_common(b2b_plan_t* out, b2b_dtype_t dt, int stages, bool single,
+                           int64_t batch, int64_t M, int64_t K, const int64_t* N) {
+  if (!out) return B2B_ERR_INVALID_ARG;
+  *out = nullptr;
+  if (dt < B2B_F16_F32OUT || dt > B2B_BF16_F32OUT) return B2B_ERR_INVALID_ARG;
+  b2b_status_t st = validate_sizes(dt, stages, batch, M, K, N);
+  if (st != B2B_OK) return st;
+  int dev = 0, sms = 0;
+  st = check_device(&dev, &sms);
+  if (st != B2B_OK) return st;
+
+  b2b_plan_s* p = new (std::nothrow) b2b_plan_s();
+  if (!p) return B2B_ERR_CUDA;
+  p->dtype = dt;
+  p->device = dev;
+  p->sms = sms;
+  p->stages = stages;
+  p->batch = batch;
+  p->M = M;
+  p->K = K;
+  for (int s = 0; s < 3; ++s) p->N[s] = s < stages ? N[s] : 0;
+  p->budget_ns = kDefaultBudgetNs;
+  type_info(dt, &p->in_kind, &p->out_kind, &p->esz, &p->osz);
+  if (batch == 0 || M == 0) {
+    // An empty chain: valid, and every run is a no-op.
+    p->kind = kPlanEmpty;
+    p->grid = 0;
+    p->threads = 0;
+  } else if (dt == B2B_F64) {
+    p->kind = single ? kPlanGemmF64 : kPlanChainF64;
+    st = setup_f64(p);
+  } else {
+    p->kind = single ? kPlanGemmTC : kPlanChainTC;
+    st = setup_chain_tc(p);
+    if (st == B2B_OK &&
+        cudaFuncSetAttribute(p->fn, cudaFuncAttributeMaxDynamicSharedMemorySize, p->smem_bytes) !=
+            cudaSuccess) {
+      cudaGetLastError();
+      st = B2B_ERR_CUDA;
+    }
+  }
+  if (st == B2B_OK) {
+    p->d_status = nullptr;
+    if (cudaMalloc(&p->d_status, sizeof(int)) != cudaSuccess ||
+        cudaMemset(p->d_status, 0, sizeof(int)) != cudaSuccess) {
+      cudaGetLastError();
+      st = B2B_ERR_CUDA;
+    }
+  }
+  if (st != B2B_OK) {
+    if (p->d_status) cudaFree(p->d_status);
+    delete p;
+    return st;
+  }
+  *out = p;
+  return B2B_OK;
+}
+
+b2b_status_t encode_3d(CUtensorMap* map, CUtensorMapDataType dt, int esz, const void* ptr,
+                       int64_t inner, int64_t rows, int64_t batch, uint32_t box_inner,
+                       uint32_t box_rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return B2B_ERR_CUDA;
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(rows),
+                              static_cast<cuuint64_t>(batch)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(inner * esz),
+                                 static_cast<cuuint64_t>(inner * rows * esz)};
+  const cuuint32_t box[3] = {box_inner, box_rows, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  const CUresult r = fn(map, dt, 3, const_cast<void*>(ptr), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? B2B_OK : B2B_ERR_CUDA;
+}
+
+bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
+  if (!a || !b || na == 0 || nb == 0) return false;
+  const uintptr_t a0 = reinterpret_cast<uintptr_t>(a), b0 = reinterpret_cast<uintptr_t>(b);
+  return a0 < b0 + nb && b0 < a0 + na;
+}
+
+b2b_status_t run_chain_tc(b2b_plan_s* p, const void* const* W, const void* A, void* D,
+                          cudaStream_t stream) {
+  const int S = p->stages;
+  const CUtensorMapDataType in_dt = p->in_kind == kInF16    ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                                    : p->in_kind == kInBF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                                            : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+  const CUtensorMapDataType out_dt = p->out_kind == kOutF16    ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                                     : p->out_kind == kOutBF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                                               : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+  const uint32_t CK = 128 / p->esz;
+  alignas(64) CUtensorMap maps[5];
+  std::memset(maps, 0, sizeof(maps));
+  b2b_status_t st = encode_3d(&maps[0], in_dt, p->esz, A, p->K, p->M, p->batch, CK, 128);
+  int64_t kin = p->K;
+  for (int s = 0; s < S && st == B2B_OK; ++s) {
+    st = encode_3d(&maps[1 + s], in_dt, p->esz, W[s], p->N[s], kin, p->batch, CK, CK);
+    kin = p->N[s];
+  }
+  for (int s = S; s < 3; ++s) maps[1 + s] = maps[1];
+  if (st == B2B_OK)
+    st = encode_3d(&maps[4], out_dt, p->osz, D, p->N[S - 1], p->M, p->batch, 128 / p->osz, 128);
+  if (st != B2B_OK) return st;
+
+  ChainParams prm = p->prm;
+  prm.status = p->d_status;
+  prm.budget_ns = p->budget_ns;
+  void* args[6] = {&maps[0], &maps[1], &maps[2], &maps[3], &maps[4], &prm};
+  const cudaError_t e = cudaLaunchKernel(p->fn, dim3(p->grid), dim3(p->threads), args,
+                                         static_cast<size_t>(p->smem_bytes), stream);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return B2B_ERR_CUDA;
+  }
+  return B2B_OK;
+}
+
+b2b_status_t run_f64(b2b_plan_s* p, const void* A, const void* B, const void* C, void* D,
+                     cudaStream_t stream) {
+  F64Params prm = p->f64;
+  const double* a = static_cast<const double*>(A);
+  const double* b = static_cast<const double*>(B);
+  const double* c = static_cast<const double*>(C);
+  double* d = static_cast<double*>(D);
+  void* args[5] = {&a, &b, &c, &d, &prm};
+  const cudaError_t e =
+      cudaLaunchKernel(p->fn, dim3(p->grid), dim3(p->threads), args, 0, stream);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return B2B_ERR_CUDA;
+  }
+  return B2B_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+b2b_status_t b2b_plan_create(b2b_plan_t* out, b2b_dtype_t dtype, int64_t batch, int64_t M,
+                             int64_t K, int64_t N1, int64_t N2, int64_t N3) {
+  if (N3 < 0) return B2B_ERR_INVALID_ARG;
+  const int64_t N[3] = {N1, N2, N3};
+  return create_common(out, dtype, N3 > 0 ? 3 : 2, false, batch, M, K, N);
+}
+
+b2b_status_t b2b_gemm_plan_create(b2b_plan_t* out, b2b_dtype_t dtype, int64_t batch, int64_t M,
+                                  int64_t K, int64_t N) {
+  const int64_t Ns[3] = {N, 0, 0};
+  return create_common(out, dtype, 1, true, batch, M, K, Ns);
+}
+
+b2b_status_t b2b_run(b2b_plan_t p, const void* A, const void* B, const void* C, const void* F,
+                     void* D, b2b_stream_t stream) {
+  if (!p) return B2B_ERR_INVALID_ARG;
+  if (p->kind == kPlanEmpty) return B2B_OK;
+  const int S = p->stages;
+  if (!A || !B || !D) return B2B_ERR_INVALID_ARG;
+  if ((S >= 2) != (C != nullptr)) return B2B_ERR_INVALID_ARG;
+  if ((S >= 3) != (F != nullptr)) return B2B_ERR_INVALID_ARG;
+  const void* ins[4] = {A, B, C, F};
+  for (const void* q : ins)
+    if (q && (reinterpret_cast<uintptr_t>(q) & 15u)) return B2B_ERR_ALIGNMENT;
+  if (reinterpret_cast<uintptr_t>(D) & 15u) return B2B_ERR_ALIGNMENT;
+  const size_t e = static_cast<size_t>(p->esz);
+  size_t sizes[4];
+  sizes[0] = static_cast<size_t>(p->batch * p->M * p->K) * e;
+  int64_t kin = p->K;
+  for (int s = 0; s < 3; ++s) {
+    sizes[1 + s] = s < S ? static_cast<size_t>(p->batch * kin * p->N[s]) * e : 0;
+    if (s < S) kin = p->N[s];
+  }
+  const size_t dbytes = static_cast<size_t>(p->batch * p->M * p->N[S - 1]) * p->osz;
+  for (int i = 0; i < 4; ++i)
+    if (overlaps(D, dbytes, ins[i], sizes[i])) return B2B_ERR_ALIAS;
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return B2B_ERR_CUDA;
+  }
+  if (dev != p->device) return B2B_ERR_DEVICE;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (p->kind == kPlanChainF64 || p->kind == kPlanGemmF64) return run_f64(p, A, B, C, D, s);
+  const void* W[3] = {B, C, F};
+  return run_chain_tc(p, W, A, D, s);
+}
+
+b2b_status_t b2b_plan_destroy(b2b_plan_t p) {
+  if (!p) return B2B_OK;
+  if (p->d_status) cudaFree(p->d_status);
+  delete p;
+  return B2B_OK;
+}
+
+b2b_status_t b2b_plan_device_status(b2b_plan_t p, b2b_stream_t stream) {
+  if (!p) return B2B_ERR_INVALID_ARG;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(s) != cudaSuccess) {
+    cudaGetLastError();
+    return B2B_ERR_CUDA;
+  }
+  int v = 0;
+  if (cudaMemcpy(&v, p->d_status, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess ||
+      cudaMemset(p->d_status, 0, sizeof(int)) != cudaSuccess) {
+    cudaGetLastError();
+    return B2B_ERR_CUDA;
+  }
+  return v == 0 ? B2B_OK : static_cast<b2b_status_t>(v);
+}
+
+b2b_status_t b2b_plan_set_wait_budget(b2b_plan_t p, uint64_t budget_ns) {
+  if (!p) return B2B_ERR_INVALID_ARG;
+  p->budget_ns = budget_ns ? budget_ns : kDefaultBudgetNs;
+  return B2B_OK;
+}
+
+b2b_status_t b2b_plan_info(b2b_plan_t p, int* launches, int* grid, int* threads, int* smem,
+                           int* tmem_cols, int* ring_stages, int* passes) {
+  if (!p) return B2B_ERR_INVALID_ARG;
+  const bool tc = p->kind == kPlanChainTC || p->kind == kPlanGemmTC;
+  if (launches) *launches = p->kind == kPlanEmpty ? 0 : 1;
+  if (grid) *grid = p->grid;
+  if (threads) *threads = p->threads;
+  if (smem) *smem = p->smem_bytes;
+  if (tmem_cols) *tmem_cols = tc ? static_cast<int>(p->prm.tmem_cols) : 0;
+  if (ring_stages) *ring_stages = tc ? p->prm.nst : 0;
+  if (passes) *passes = tc ? p->prm.npass : 1;
+  return B2B_OK;
+}
+
+const char* b2b_status_string(b2b_status_t s) {
+  switch (s) {
+    case B2B_OK: return "ok";
+    case B2B_ERR_INVALID_ARG: return "invalid argument";
+    case B2B_ERR_UNSUPPORTED: return "unsupported size or type";
+    case B2B_ERR_ALIGNMENT: return "pointer not 16-byte aligned";
+    case B2B_ERR_ALIAS: return "output overlaps an input";
+    case B2B_ERR_DEVICE: return "current device is not an sm_103 GPU";
+    case B2B_ERR_CUDA: return "CUDA call failed";
+    case B2B_ERR_TIMEOUT: return "a bounded wait inside a kernel timed out";
+    default: return "unknown status";
+  }
+}
+
+b2b_status_t b2b_probe_operand_image(b2b_dtype_t dtype, int width, const void* acc, void* image,
+                                     b2b_stream_t stream) {
+  if (!acc || !image) return B2B_ERR_INVALID_ARG;
+  if (width != 64 && width != 128 && width != 256) return B2B_ERR_INVALID_ARG;
+  int in_kind, out_kind, esz, osz;
+  type_info(dtype, &in_kind, &out_kind, &esz, &osz);
+  if (in_kind < 0) return B2B_ERR_UNSUPPORTED;
+  b2b_status_t st = check_device(nullptr, nullptr);
+  if (st != B2B_OK) return st;
+  const void* fn = in_kind == kInF16    ? reinterpret_cast<const void*>(&probe_operand_kernel<kInF16>)
+                   : in_kind == kInBF16 ? reinterpret_cast<const void*>(&probe_operand_kernel<kInBF16>)
+                                        : reinterpret_cast<const void*>(&probe_operand_kernel<kInTF32>);
+  const int smem = in_kind == kInTF32 ? 1024 : width * 256 + 1024;
+  if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess) {
+    cudaGetLastError();
+    return B2B_ERR_CUDA;
+  }
+  const uint32_t* a = static_cast<const uint32_t*>(acc);
+  uint32_t* o = static_cast<uint32_t*>(image);
+  uint32_t cols = pow2_cols(static_cast<uint32_t>(width));
+  void* args[4] = {&a, &o, &width, &cols};
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (cudaLaunchKernel(fn, dim3(1), dim3(128), args, static_cast<size_t>(smem), s) != cudaSuccess ||
+      cudaStreamSynchronize(s) != cudaSuccess) {
+    cudaGetLastError();
+    return B2B_ERR_CUDA;
+  }
+  return B2B_OK;
+}
+
+b2b_status_t b2b_probe_f64_rearrange(int tiles, const double* cfrag, double* afrag,
+                                     b2b_stream_t stream) {
+  if (!cfrag || !afrag || tiles < 1 || tiles > 8) return B2B_ERR_INVALID_ARG;
+  b2b_status_t st = check_device(nullptr, nullptr);
+  if (st != B2B_OK) return st;
+  const F64Tables tab = f64_tables();
+  if (!tab.ok) return B2B_ERR_UNSUPPORTED;
+  F64Params prm;
+  std::memset(&prm, 0, sizeof(prm));
+  for (int j = 0; j < 2; ++j) {
+    prm.fsrc[j] = tab.fsrc[j];
+    prm.qsend[j] = tab.qsend[j];
+    prm.hslot[j] = tab.hslot[j];
+  }
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  probe_f64_rearrange_kernel<<<1, 32, 0, s>>>(cfrag, afrag, tiles, prm);
+  if (cudaGetLastError() != cudaSuccess || cudaStreamSynchronize(s) != cudaSuccess) {
+    cudaGetLastError();
+    return B2B_ERR_CUDA;
+  }
+  return B2B_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,659 @@
+// Fused cascaded GEMM on the 5th-generation tensor cores (tcgen05), sm_103a.
+//
+//   P1 = A.W0  ->  rearrange/round  ->  P2 = P1.W1  [->  rearrange  ->  E = P2.W2]
+//
+// Source of the method: patent "数据处理方法、装置、设备及介质" (Alibaba, 2023),
+// Detailed description para. 35-37 (steps 101-103), para. 54-60 (the result
+// of operator 1 is held by rule 1, rearranged, and handed to operator 2 by
+// rule 2 without going through memory), para. 103-110 (rearrangement through
+// shared memory) and para. 41 (three cascaded operators).
+//
+// On this hardware rule 1 is the tcgen05 accumulator layout in tensor memory
+// (row m of the 128-row tile in TMEM lane m, column n in TMEM column n, fp32)
+// and rule 2 is the K-major 128-byte-swizzled shared-memory operand image that
+// a tcgen05.mma A-descriptor reads.  Because a row stays in one lane, the
+// rearrangement needs no cross-thread exchange: each converter thread loads
+// its row with tcgen05.ld, rounds it to the operand type and writes it into
+// the swizzled image with 16-byte st.shared.  For tf32 the rounded operand is
+// written back into the accumulator's own columns (tcgen05.st), because the
+// tf32 MMA can take its A operand from tensor memory, where the layout of
+// rule 2 equals rule 1.
+//
+// CTA roles (320 threads, one CTA per SM, persistent over 128-row tiles):
+//   warp 0     TMA producer: A panels and weight panels into a ring of stages
+//   warp 1     TMEM allocator and the single MMA-issuing thread
+//   warps 2-5  converters: accumulator -> operand (the rearrangement)
+//   warps 6-9  epilogue: accumulator -> output type -> swizzled staging -> TMA store
+// Every wait is bounded (ptx::BoundedWait); on a timeout the CTA raises an
+// abort flag, every role leaves its loop, in-flight copies and MMAs are
+// drained, tensor memory is freed and the status word reports the timeout.
+#pragma once
+
+#include <cuda.h>
+#include <cstdint>
+
+#include "ptx.cuh"
+
+namespace b2b {
+
+enum : int { kInF16 = 0, kInBF16 = 1, kInTF32 = 2 };
+enum : int { kOutF32 = 0, kOutF16 = 1, kOutBF16 = 2 };
+
+constexpr int kChainThreads = 320;
+constexpr int kPanelBytes = 128 * 128;  // one 128-row x 128-byte swizzled panel
+constexpr int kBarBytes = 512;
+constexpr int kTimeoutCode = 7;         // B2B_ERR_TIMEOUT
+
+// Barrier slots (8 bytes each) at ChainParams::off_bar.
+enum : int {
+  kBarFull = 0,     // [8] ring stage filled by TMA
+  kBarEmpty = 8,    // [8] ring stage consumed by the MMAs
+  kBarWFull = 16,   // resident weights landed
+  kBarWEmpty = 17,  // resident weights no longer read
+  kBarRFull = 18,   // [4] region holds a final product for the epilogue
+  kBarREmpty = 22,  // [4] tensor-memory region drained by a warpgroup
+  kBarPFull = 26,   // operand image of the intermediate written
+  kBarPEmpty = 27,  // operand image of the intermediate no longer read
+  kBarEpiSync = 28,
+  kBarDrain = 29,
+  kBarCFull = 30,   // [2] region X / Y holds an intermediate for the converters
+  kSlotTmem = 32,   // uint32 TMEM base address, then the int abort flag
+};
+// Each consumer warpgroup has its own "full" barrier per region, so that it
+// sees every completion of that barrier in order: when the last GEMM reuses
+// X and Y, the converters and the epilogue take turns on the same region,
+// and a parity wait could not tell a waiter's own phase from the other's.
+
+struct ChainParams {
+  int batch, M, K;
+  int m_tiles, total_tiles;
+  int npass;          // passes of the final GEMM (NF columns each)
+  int kpan0;          // 128-byte K panels of A (ceil(K / panel width))
+  int nst;            // ring depth
+  int nstg;           // output staging buffers (1 or 2)
+  uint32_t off_ring, stage_bytes, off_wres0, off_wres1, off_p, off_stg, off_bar;
+  uint32_t tmem_cols;
+  int region_col[4];  // X, Y, Z0, Z1 (TMEM column offsets)
+  int nz;             // Z buffers for the final accumulator; 0 = reuse X/Y in turn
+  int* status;
+  unsigned long long budget_ns;
+};
+
+// Which tensor-memory region phase `ph` of local tile `it` writes, and how
+// many times that region has been written before (its use index, which the
+// MMA thread waits on through the region's "empty" barrier).
+// Phases 0..S-2 are the intermediate GEMMs (X, then Y); the rest are the
+// passes of the final GEMM (Z buffers in turn, or X/Y in turn when nz == 0).
+__host__ __device__ __forceinline__ void region_use(const ChainParams& p, int S, int it, int ph,
+                                                    int& r, uint32_t& u) {
+  const int ux = 1 + (p.npass + 1) / 2, uy = 1 + p.npass / 2;
+  if (ph < S - 1) {
+    r = ph;
+    u = (p.nz > 0) ? static_cast<uint32_t>(it)
+                   : static_cast<uint32_t>(it) * static_cast<uint32_t>(ph == 0 ? ux : uy);
+    return;
+  }
+  const int pass = ph - (S - 1);
+  if (p.nz > 0) {
+    const uint32_t g = static_cast<uint32_t>(it) * p.npass + pass;
+    r = 2 + static_cast<int>(g % p.nz);
+    u = g / p.nz;
+  } else {
+    r = pass & 1;
+    u = static_cast<uint32_t>(it) * static_cast<uint32_t>(r == 0 ? ux : uy) + 1 + pass / 2;
+  }
+}
+
+// ------------------------------------------------------------ rearrangement
+// One converter thread holds 32 consecutive fp32 accumulator columns
+// [c0, c0 + 32) of its row.  Round them to the operand type and store them
+// into the K-major 128B-swizzled operand image at `img` (panels of 128 rows x
+// 128 bytes): 16-byte unit u of row r lands at unit u ^ (r % 8).
+template <int IN>
+__device__ __forceinline__ void store_operand_row(uint32_t img, int row, int c0,
+                                                  const uint32_t (&v)[32]) {
+  using namespace ptx;
+  const uint32_t sw = static_cast<uint32_t>(row & 7);
+  if constexpr (IN == kInTF32) {
+    const uint32_t rbase = img + static_cast<uint32_t>(c0 / 32) * kPanelBytes + row * 128u;
+#pragma unroll
+    for (uint32_t u = 0; u < 8; ++u)
+      st_shared_v4(rbase + ((u ^ sw) << 4), to_tf32_rna(v[4 * u]), to_tf32_rna(v[4 * u + 1]),
+                   to_tf32_rna(v[4 * u + 2]), to_tf32_rna(v[4 * u + 3]));
+  } else {
+    const uint32_t rbase = img + static_cast<uint32_t>(c0 / 64) * kPanelBytes + row * 128u;
+    const uint32_t unit0 = static_cast<uint32_t>((c0 % 64) / 8);
+#pragma unroll
+    for (uint32_t u = 0; u < 4; ++u) {
+      uint32_t w[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+        w[i] = (IN == kInF16) ? pack_f16x2(v[8 * u + 2 * i], v[8 * u + 2 * i + 1])
+                              : pack_bf16x2(v[8 * u + 2 * i], v[8 * u + 2 * i + 1]);
+      st_shared_v4(rbase + (((unit0 + u) ^ sw) << 4), w[0], w[1], w[2], w[3]);
+    }
+  }
+}
+
+// Output staging: 32 fp32 accumulator columns [c, c + 32) of a store box
+// (128 bytes wide) -> output type -> 128B-swizzled box image.
+template <int OUT>
+__device__ __forceinline__ void store_output_row(uint32_t img, int row, int c,
+                                                 const uint32_t (&v)[32]) {
+  using namespace ptx;
+  const uint32_t sw = static_cast<uint32_t>(row & 7);
+  const uint32_t rbase = img + row * 128u;
+  if constexpr (OUT == kOutF32) {
+#pragma unroll
+    for (uint32_t u = 0; u < 8; ++u)
+      st_shared_v4(rbase + ((u ^ sw) << 4), v[4 * u], v[4 * u + 1], v[4 * u + 2], v[4 * u + 3]);
+  } else {
+    const uint32_t unit0 = static_cast<uint32_t>(c / 8);
+#pragma unroll
+    for (uint32_t u = 0; u < 4; ++u) {
+      uint32_t w[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+        w[i] = (OUT == kOutF16) ? pack_f16x2(v[8 * u + 2 * i], v[8 * u + 2 * i + 1])
+                                : pack_bf16x2(v[8 * u + 2 * i], v[8 * u + 2 * i + 1]);
+      st_shared_v4(rbase + (((unit0 + u) ^ sw) << 4), w[0], w[1], w[2], w[3]);
+    }
+  }
+}
+
+// The rearrangement of one accumulator row (step 103 on this hardware).
+// `tsrc` is the TMEM address of this warp's lane quadrant at the first
+// accumulator column; the thread owns row `row` of the tile.  16-bit types:
+// round and store into the swizzled shared-memory operand image `p_img`.
+// tf32: round in place; the MMA then reads the operand from tensor memory.
+template <int IN>
+__device__ __forceinline__ void rearrange_accumulator(uint32_t tsrc, int width, int row,
+                                                      uint32_t p_img) {
+  using namespace ptx;
+#pragma unroll 1
+  for (int c0 = 0; c0 < width; c0 += 32) {
+    uint32_t v[32];
+    tmem_ld32(tsrc + static_cast<uint32_t>(c0), v);
+    tmem_wait_ld();
+    if constexpr (IN == kInTF32) {
+#pragma unroll
+      for (int i = 0; i < 32; ++i) v[i] = to_tf32_rna(v[i]);
+      tmem_st32(tsrc + static_cast<uint32_t>(c0), v);
+    } else {
+      store_operand_row<IN>(p_img, row, c0, v);
+    }
+  }
+  if constexpr (IN == kInTF32) {
+    tmem_wait_st();
+  } else {
+    fence_proxy_async_smem();
+  }
+}
+
+// Warp-uniform bounded wait: the warp goes on only if every lane saw the phase.
+__device__ __forceinline__ bool warp_wait(const ptx::BoundedWait& bw, uint32_t bar,
+                                          uint32_t parity) {
+  const bool ok = bw.wait(bar, parity);
+  return __all_sync(0xffffffffu, ok) != 0;
+}
+
+// Barrier among the 128 threads of one warpgroup, built on an mbarrier so
+// that it is bounded like every other wait.
+__device__ __forceinline__ bool group_sync(const ptx::BoundedWait& bw, uint32_t bar,
+                                           uint32_t& uses) {
+  ptx::mbar_arrive(bar);
+  const bool ok = warp_wait(bw, bar, uses & 1u);
+  ++uses;
+  return ok;
+}
+
+// Wait used while draining after an abort: ignores the abort flag (the copy
+// or MMA being waited for completes on its own) but still has a budget.
+__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, uint64_t budget_ns) {
+  if (ptx::mbar_try_wait(bar, parity)) return;
+  const uint64_t t0 = ptx::globaltimer_ns();
+  while (!ptx::mbar_try_wait(bar, parity)) {
+    if (ptx::globaltimer_ns() - t0 > budget_ns) return;
+  }
+}
+
+template <int IN, int OUT, int S, int N1P, int N2P, int NF, bool RES>
+__global__ void __launch_bounds__(kChainThreads, 1)
+    chain_tc_kernel(const __grid_constant__ CUtensorMap tmA,
+                    const __grid_constant__ CUtensorMap tmW0,
+                    const __grid_constant__ CUtensorMap tmW1,
+                    const __grid_constant__ CUtensorMap tmW2,
+                    const __grid_constant__ CUtensorMap tmOut,
+                    const __grid_constant__ ChainParams p) {
+  using namespace ptx;
+  constexpr bool TF32 = (IN == kInTF32);
+  constexpr int ESZ = TF32 ? 4 : 2;
+  constexpr int OSZ = (OUT == kOutF32) ? 4 : 2;
+  constexpr int CK = 128 / ESZ;       // K elements per 128-byte panel
+  constexpr int KSTEP = 32 / ESZ;     // K of one tcgen05.mma
+  constexpr int WBOX_N = 128 / ESZ;   // weight columns per TMA box
+  constexpr int WBOX_BYTES = CK * 128;
+  constexpr int OBOX_N = 128 / OSZ;   // output columns per TMA store box
+  constexpr bool P_TMEM = TF32;
+  constexpr uint32_t FMT = (IN == kInF16) ? 0u : (IN == kInBF16 ? 1u : 2u);
+  constexpr int NPH_FIXED = S - 1;    // intermediate phases per tile
+  static_assert(S >= 1 && S <= 3, "one to three cascaded GEMMs");
+  static_assert(!(TF32 && S == 3), "tf32 chains have two stages");
+  static_assert(!RES || S == 2, "resident weights only for two-stage chains");
+  static_assert(N1P % 64 == 0 && N2P % 64 == 0 && NF % 64 == 0, "panel widths");
+  static_assert(N1P <= 256 && N2P <= 256 && NF <= 256, "one MMA covers at most 256 columns");
+
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* gbase = smem_raw + (base - raw);
+  const uint32_t bar0 = base + p.off_bar;
+  auto bar = [&](int i) -> uint32_t { return bar0 + 8u * static_cast<uint32_t>(i); };
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + p.off_bar + 8 * kSlotTmem);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < 8; ++i) {
+      mbar_init(bar(kBarFull + i), 1);
+      mbar_init(bar(kBarEmpty + i), 1);
+    }
+    mbar_init(bar(kBarWFull), 1);
+    mbar_init(bar(kBarWEmpty), 1);
+    for (int i = 0; i < 4; ++i) {
+      mbar_init(bar(kBarRFull + i), 1);
+      mbar_init(bar(kBarREmpty + i), 128);
+    }
+    mbar_init(bar(kBarCFull), 1);
+    mbar_init(bar(kBarCFull + 1), 1);
+    mbar_init(bar(kBarPFull), 128);
+    mbar_init(bar(kBarPEmpty), 1);
+    mbar_init(bar(kBarEpiSync), 128);
+    mbar_init(bar(kBarDrain), 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), p.tmem_cols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  BoundedWait bw{abort_flag, p.status, p.budget_ns, kTimeoutCode};
+
+  // Tiles of this CTA: a contiguous range when the weights stay resident
+  // (few batch changes), otherwise strided so that concurrent CTAs share the
+  // same weights in L2.
+  int t_begin, t_step, t_count;
+  if constexpr (RES) {
+    const long long T = p.total_tiles, G = gridDim.x;
+    const int b0 = static_cast<int>((blockIdx.x * T) / G);
+    const int b1 = static_cast<int>(((blockIdx.x + 1) * T) / G);
+    t_begin = b0;
+    t_step = 1;
+    t_count = b1 - b0;
+  } else {
+    t_begin = blockIdx.x;
+    t_step = gridDim.x;
+    t_count = (static_cast<int>(blockIdx.x) < p.total_tiles)
+                  ? (p.total_tiles - static_cast<int>(blockIdx.x) + gridDim.x - 1) / gridDim.x
+                  : 0;
+  }
+  const int nph = NPH_FIXED + p.npass;
+
+  auto stage_width = [](int s) -> int { return s < S - 1 ? (s == 0 ? N1P : N2P) : NF; };
+  auto stage_kpan = [&](int s) -> int { return s == 0 ? p.kpan0 : (s == 1 ? N1P / CK : N2P / CK); };
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      prefetch_tmap(&tmA);
+      prefetch_tmap(&tmW0);
+      if (S >= 2) prefetch_tmap(&tmW1);
+      if (S >= 3) prefetch_tmap(&tmW2);
+      prefetch_tmap(&tmOut);
+      uint32_t stage = 0, phase = 0, wl = 0;
+      uint64_t issued = 0;
+      int cur_b = -1;
+      bool ok = true;
+      for (int it = 0; it < t_count && ok; ++it) {
+        const int tile = t_begin + it * t_step;
+        const int b = tile / p.m_tiles;
+        const int m0 = (tile % p.m_tiles) * 128;
+        if constexpr (RES) {
+          if (b != cur_b) {
+            if (wl > 0 && !bw.wait(bar(kBarWEmpty), (wl - 1) & 1u)) {
+              ok = false;
+              break;
+            }
+            const uint32_t bytes = static_cast<uint32_t>(p.kpan0) * 128u * N1P +
+                                   static_cast<uint32_t>(N1P / CK) * 128u * NF;
+            mbar_arrive_expect_tx(bar(kBarWFull), bytes);
+            for (int kb = 0; kb < p.kpan0; ++kb)
+              for (int j = 0; j < N1P / WBOX_N; ++j)
+                tma_load_3d(base + p.off_wres0 + kb * 128u * N1P + j * WBOX_BYTES, &tmW0,
+                            bar(kBarWFull), j * WBOX_N, kb * CK, b);
+            for (int kb = 0; kb < N1P / CK; ++kb)
+              for (int j = 0; j < NF / WBOX_N; ++j)
+                tma_load_3d(base + p.off_wres1 + kb * 128u * NF + j * WBOX_BYTES, &tmW1,
+                            bar(kBarWFull), j * WBOX_N, kb * CK, b);
+            cur_b = b;
+            ++wl;
+          }
+        }
+        for (int ph = 0; ph < nph && ok; ++ph) {
+          const int s = ph < S - 1 ? ph : S - 1;
+          if (RES && s != 0) continue;
+          const int width = stage_width(s);
+          const int n0 = ph < S - 1 ? 0 : (ph - (S - 1)) * NF;
+          const int kpan = stage_kpan(s);
+          const CUtensorMap* wm = s == 0 ? &tmW0 : (s == 1 ? &tmW1 : &tmW2);
+          for (int kb = 0; kb < kpan; ++kb) {
+            if (!bw.wait(bar(kBarEmpty + stage), phase ^ 1u)) {
+              ok = false;
+              break;
+            }
+            const uint32_t dst = base + p.off_ring + stage * p.stage_bytes;
+            const uint32_t bytes =
+                (s == 0 ? kPanelBytes : 0u) + (RES ? 0u : 128u * static_cast<uint32_t>(width));
+            mbar_arrive_expect_tx(bar(kBarFull + stage), bytes);
+            if (s == 0) tma_load_3d(dst, &tmA, bar(kBarFull + stage), kb * CK, m0, b);
+            if constexpr (!RES) {
+              for (int j = 0; j < width / WBOX_N; ++j)
+                tma_load_3d(dst + kPanelBytes + j * WBOX_BYTES, wm, bar(kBarFull + stage),
+                            n0 + j * WBOX_N, kb * CK, b);
+            }
+            ++issued;
+            if (++stage == static_cast<uint32_t>(p.nst)) {
+              stage = 0;
+              phase ^= 1u;
+            }
+          }
+        }
+      }
+      // Wait for every copy still in flight before the CTA may exit.
+      const uint64_t nst = static_cast<uint64_t>(p.nst);
+      const uint64_t tail = issued < nst ? issued : nst;
+      for (uint64_t j = 0; j < tail; ++j) {
+        const uint64_t idx = issued - 1 - j;
+        drain_wait(bar(kBarFull + static_cast<int>(idx % nst)),
+                   static_cast<uint32_t>((idx / nst) & 1u), p.budget_ns);
+      }
+      if (RES && wl > 0) drain_wait(bar(kBarWFull), (wl - 1) & 1u, p.budget_ns);
+    }
+  } else if (warp == 1) {
+    // ----------------------------------------------------------------- MMA
+    if (lane == 0) {
+      uint32_t stage = 0, phase = 0, pf = 0, wl = 0;
+      int cur_b = -1;
+      bool ok = true;
+      for (int it = 0; it < t_count && ok; ++it) {
+        const int tile = t_begin + it * t_step;
+        const int b = tile / p.m_tiles;
+        if constexpr (RES) {
+          if (b != cur_b) {
+            if (!bw.wait(bar(kBarWFull), wl & 1u)) {
+              ok = false;
+              break;
+            }
+            ++wl;
+            cur_b = b;
+            tc_fence_after();
+          }
+        }
+        if constexpr (P_TMEM) {
+          // The intermediate of the previous tile (in region X) must be fully
+          // read before GEMM1 of this tile overwrites X.
+          if (it > 0 && !bw.wait(bar(kBarPEmpty), (it - 1) & 1u)) {
+            ok = false;
+            break;
+          }
+        }
+        for (int ph = 0; ph < nph && ok; ++ph) {
+          const int s = ph < S - 1 ? ph : S - 1;
+          const int width = stage_width(s);
+          const int kpan = stage_kpan(s);
+          // The first phase that reads an intermediate waits for its operand
+          // (the later passes of the last GEMM read the same operand).
+          if (s >= 1 && ph == s) {
+            if (!bw.wait(bar(kBarPFull), pf & 1u)) {
+              ok = false;
+              break;
+            }
+            ++pf;
+            tc_fence_after();
+          }
+          int r;
+          uint32_t u;
+          region_use(p, S, it, ph, r, u);
+          if (!bw.wait(bar(kBarREmpty + r), (u & 1u) ^ 1u)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(p.region_col[r]);
+          const uint32_t idesc = make_idesc(FMT, static_cast<uint32_t>(width), 128u, true);
+          const uint32_t wres = (s == 0) ? p.off_wres0 : p.off_wres1;
+          for (int kb = 0; kb < kpan; ++kb) {
+            const bool ring = (s == 0) || !RES;
+            const uint32_t sa = base + p.off_ring + stage * p.stage_bytes;
+            if (ring) {
+              if (!bw.wait(bar(kBarFull + stage), phase)) {
+                ok = false;
+                break;
+              }
+              tc_fence_after();
+            }
+            const uint32_t b_base =
+                RES ? base + wres + static_cast<uint32_t>(kb) * 128u * width : sa + kPanelBytes;
+#pragma unroll
+            for (int kk = 0; kk < CK / KSTEP; ++kk) {
+              const uint64_t bdesc = desc_sw128(b_base + kk * KSTEP * 128u, WBOX_BYTES, 1024u);
+              const uint32_t acc = (kb | kk) != 0 ? 1u : 0u;
+              if (s == 0) {
+                mma_ss<TF32>(d_tmem, desc_sw128(sa + kk * 32u, 16u, 1024u), bdesc, idesc, acc);
+              } else if constexpr (P_TMEM) {
+                mma_ts<TF32>(d_tmem,
+                             tmem_base + static_cast<uint32_t>(p.region_col[0] + kb * CK + kk * KSTEP),
+                             bdesc, idesc, acc);
+              } else {
+                mma_ss<TF32>(d_tmem,
+                             desc_sw128(base + p.off_p + kb * kPanelBytes + kk * 32u, 16u, 1024u),
+                             bdesc, idesc, acc);
+              }
+            }
+            if (ring) {
+              tc_commit(bar(kBarEmpty + stage));
+              if (++stage == static_cast<uint32_t>(p.nst)) {
+                stage = 0;
+                phase ^= 1u;
+              }
+            }
+          }
+          if (!ok) break;
+          tc_commit(bar(ph < S - 1 ? kBarCFull + r : kBarRFull + r));
+          if (S >= 2 && ph == nph - 1) tc_commit(bar(kBarPEmpty));
+        }
+        if constexpr (RES) {
+          if (ok && it + 1 < t_count) {
+            const int nb = (t_begin + (it + 1) * t_step) / p.m_tiles;
+            if (nb != b) tc_commit(bar(kBarWEmpty));
+          }
+        }
+      }
+      // Every MMA issued so far must be complete before tensor memory is freed.
+      tc_commit(bar(kBarDrain));
+      drain_wait(bar(kBarDrain), 0, p.budget_ns);
+    }
+  } else if (warp < 6) {
+    // ---------------------------------------------------------- converters
+    if constexpr (S >= 2) {
+      const int q = warp & 3;
+      const int row = q * 32 + lane;
+      const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
+      bool ok = true;
+      for (int it = 0; it < t_count && ok; ++it) {
+        for (int s = 0; s < S - 1 && ok; ++s) {
+          int r;
+          uint32_t u;
+          region_use(p, S, it, s, r, u);
+          if (!P_TMEM && s == 0 && !warp_wait(bw, bar(kBarPEmpty), (static_cast<uint32_t>(it) & 1u) ^ 1u)) {
+            ok = false;
+            break;
+          }
+          // region r (X or Y) receives one intermediate per tile
+          if (!warp_wait(bw, bar(kBarCFull + r), static_cast<uint32_t>(it) & 1u)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const int width = (s == 0) ? N1P : N2P;
+          const uint32_t tsrc = tmem_base + lane_off + static_cast<uint32_t>(p.region_col[r]);
+          rearrange_accumulator<IN>(tsrc, width, row, base + p.off_p);
+          tc_fence_before();
+          mbar_arrive(bar(kBarPFull));
+          mbar_arrive(bar(kBarREmpty + r));
+        }
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int q = warp & 3;
+    const int row = q * 32 + lane;
+    const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
+    const bool elected = (warp == 6 && lane == 0);
+    constexpr int NBOX = NF / OBOX_N;
+    uint32_t nbox = 0, gs = 0;
+    bool ok = true;
+    for (int it = 0; it < t_count && ok; ++it) {
+      const int tile = t_begin + it * t_step;
+      const int b = tile / p.m_tiles;
+      const int m0 = (tile % p.m_tiles) * 128;
+      for (int pass = 0; pass < p.npass && ok; ++pass) {
+        int r;
+        uint32_t u;
+        region_use(p, S, it, NPH_FIXED + pass, r, u);
+        // how many final products this region held before (epilogue's own count)
+        const uint32_t eu =
+            p.nz > 0 ? u
+                     : static_cast<uint32_t>(it) * static_cast<uint32_t>(r == 0 ? (p.npass + 1) / 2 : p.npass / 2) +
+                           static_cast<uint32_t>(pass / 2);
+        if (!warp_wait(bw, bar(kBarRFull + r), eu & 1u)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t tsrc = tmem_base + lane_off + static_cast<uint32_t>(p.region_col[r]);
+        const int n0 = pass * NF;
+#pragma unroll 1
+        for (int j = 0; j < NBOX; ++j) {
+          const uint32_t buf = (p.nstg == 2) ? (nbox & 1u) : 0u;
+          const uint32_t stg = base + p.off_stg + buf * kPanelBytes;
+          if (elected && nbox >= static_cast<uint32_t>(p.nstg)) {
+            if (p.nstg == 2)
+              bulk_wait_read<1>();
+            else
+              bulk_wait_read<0>();
+          }
+          if (!group_sync(bw, bar(kBarEpiSync), gs)) {
+            ok = false;
+            break;
+          }
+#pragma unroll
+          for (int c = 0; c < OBOX_N; c += 32) {
+            uint32_t v[32];
+            tmem_ld32(tsrc + static_cast<uint32_t>(j * OBOX_N + c), v);
+            tmem_wait_ld();
+            store_output_row<OUT>(stg, row, c, v);
+          }
+          if (j == NBOX - 1) {
+            tc_fence_before();
+            mbar_arrive(bar(kBarREmpty + r));
+          }
+          fence_proxy_async_smem();
+          if (!group_sync(bw, bar(kBarEpiSync), gs)) {
+            ok = false;
+            break;
+          }
+          if (elected) {
+            tma_store_3d(&tmOut, stg, n0 + j * OBOX_N, m0, b);
+            bulk_commit();
+          }
+          ++nbox;
+        }
+      }
+    }
+    if (elected) bulk_wait_all();
+  }
+
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, p.tmem_cols);
+  }
+}
+
+}  // namespace b2b
+
+namespace b2b {
+
+// Test support: run the converter routine of the fused kernel on one 128-row
+// tile.  `acc` holds the tile's fp32 bit patterns [128][width]; they are put
+// into tensor memory in the accumulator layout, rearranged by
+// rearrange_accumulator<IN>, and the resulting operand (the swizzled
+// shared-memory image, or for tf32 the tensor-memory operand) is copied out.
+template <int IN>
+__global__ void __launch_bounds__(128, 1)
+    probe_operand_kernel(const uint32_t* __restrict__ acc, uint32_t* __restrict__ out, int width,
+                         uint32_t tmem_cols) {
+  using namespace ptx;
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ uint32_t tslot;
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t img = (raw + 1023u) & ~1023u;
+  const uint8_t* gimg = smem_raw + (img - raw);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int row = warp * 32 + lane;
+  if (warp == 0) {
+    tmem_alloc(smem_u32(&tslot), tmem_cols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = tslot;
+  const uint32_t tsrc = tbase + (static_cast<uint32_t>(warp * 32) << 16);
+  for (int c0 = 0; c0 < width; c0 += 32) {
+    uint32_t v[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = acc[row * width + c0 + i];
+    tmem_st32(tsrc + static_cast<uint32_t>(c0), v);
+  }
+  tmem_wait_st();
+  rearrange_accumulator<IN>(tsrc, width, row, img);
+  if constexpr (IN == kInTF32) {
+    for (int c0 = 0; c0 < width; c0 += 32) {
+      uint32_t v[32];
+      tmem_ld32(tsrc + static_cast<uint32_t>(c0), v);
+      tmem_wait_ld();
+#pragma unroll
+      for (int i = 0; i < 32; ++i) out[row * width + c0 + i] = v[i];
+    }
+  } else {
+    __syncthreads();
+    const int words = width * 256 / 4;
+    const uint32_t* src = reinterpret_cast<const uint32_t*>(gimg);
+    for (int i = threadIdx.x; i < words; i += blockDim.x) out[i] = src[i];
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 0) tmem_dealloc(tbase, tmem_cols);
+}
+
+}  // namespace b2b

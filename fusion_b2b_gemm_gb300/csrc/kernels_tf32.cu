@@ -1,0 +1,12 @@
+// tf32 tcgen05 chain kernels (fp32 storage and output).
+#include "registry.h"
+
+namespace b2b {
+namespace {
+const ChainKernelEntry kEntries[] = {
+    B2B_CHAIN_ENTRY(kInTF32, kOutF32, 2, 256, 64, 128, false),
+    B2B_CHAIN_ENTRY(kInTF32, kOutF32, 1, 64, 64, 256, false),
+};
+}  // namespace
+ChainTable chain_table_tf32() { return {kEntries, static_cast<int>(sizeof(kEntries) / sizeof(kEntries[0]))}; }
+}  // namespace b2b

@@ -1,0 +1,192 @@
+/*
+ * b2b.h -- fused cascaded (back-to-back) GEMM for GB300 (sm_103a).
+ *
+ *   D = (A.B).C              (two cascaded GEMMs)
+ *   E = ((A.B).C).F          (three cascaded GEMMs)
+ *
+ * The method is the one of patent "数据处理方法、装置、设备及介质"
+ * (Alibaba, 2023): two (or three) cascaded operators are fused so that the
+ * result of operator 1 is never written to memory.  Operator 1's result,
+ * held in the layout of the accumulator ("first data processing rule"), is
+ * rearranged on chip into the operand layout operator 2 reads ("second data
+ * processing rule") and handed straight to operator 2 (Detailed description
+ * para. 35-37, steps 101-103; para. 54-60; three operators: para. 41).
+ * The apparatus splits this into an operator-determination module, a
+ * relation-determination module and a rearrangement module (para. 140-143,
+ * Fig. 5); here b2b_plan_create plays the first two (the caller names the
+ * chain; the relation is fixed from the data types at plan time) and b2b_run
+ * the third.
+ *
+ * Conventions for every entry point
+ *   - Matrices are dense, row-major, batched: A[batch][M][K],
+ *     B[batch][K][N1], C[batch][N1][N2], F[batch][N2][N3], and the output
+ *     D[batch][M][N2] (two stages) or E[batch][M][N3] (three stages).  Each
+ *     batch has its own weights; the batch stride is the matrix size.
+ *   - Device pointers are CUDA device addresses on the device that was
+ *     current when the plan was created.  The caller owns every buffer and
+ *     stream and keeps them alive until the work on the stream has finished.
+ *   - Status codes are returned; nothing is thrown across this interface.
+ *   - Computation: inputs are read in their storage type, products are
+ *     accumulated in fp32 (fp64 for B2B_F64), every intermediate is rounded
+ *     to the operand type of the next GEMM (fp16 / bf16: round to nearest
+ *     even; tf32: round to nearest, ties away from zero; fp64: kept), and the
+ *     last product is rounded to the output type.
+ */
+#ifndef B2B_H_
+#define B2B_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct b2b_plan_s* b2b_plan_t;
+/* A cudaStream_t (NULL = the legacy default stream). */
+typedef struct CUstream_st* b2b_stream_t;
+
+typedef enum {
+  B2B_OK = 0,
+  B2B_ERR_INVALID_ARG = 1, /* null plan/pointer, bad size                   */
+  B2B_ERR_UNSUPPORTED = 2, /* valid request this build has no kernel for    */
+  B2B_ERR_ALIGNMENT = 3,   /* pointer not 16-byte aligned                   */
+  B2B_ERR_ALIAS = 4,       /* output overlaps an input                      */
+  B2B_ERR_DEVICE = 5,      /* current device is not sm_103 (GB300)          */
+  B2B_ERR_CUDA = 6,        /* a CUDA runtime/driver call failed             */
+  B2B_ERR_TIMEOUT = 7      /* a bounded wait inside a kernel gave up        */
+} b2b_status_t;
+
+/* Storage and compute types of a chain (inputs / intermediate / output). */
+typedef enum {
+  B2B_F16_F32OUT = 0,  /* fp16 in, fp16 intermediates, fp32 out            */
+  B2B_F16 = 1,         /* fp16 in, fp16 intermediates, fp16 out            */
+  B2B_BF16 = 2,        /* bf16 in, bf16 intermediates, bf16 out            */
+  B2B_TF32 = 3,        /* fp32 storage, tf32 operands and intermediate, fp32 out */
+  B2B_F64 = 4,         /* fp64 throughout                                   */
+  B2B_BF16_F32OUT = 5  /* bf16 in, bf16 intermediates, fp32 out            */
+} b2b_dtype_t;
+
+/*
+ * Create a plan for a fused chain (operator determination and relation
+ * determination, patent para. 46-53, 140-142).
+ *   out      receives the plan handle (set to NULL on failure).
+ *   dtype    see b2b_dtype_t.
+ *   batch, M >= 0 (any M: the last row tile is partial; batch == 0 or
+ *            M == 0 gives an empty chain whose runs do nothing).
+ *   K        contraction length of GEMM1, >= 1.
+ *   N1, N2   output widths of GEMM1 and GEMM2.
+ *   N3       output width of GEMM3, or 0 for a two-stage chain.
+ * Sizes this build supports (otherwise B2B_ERR_UNSUPPORTED):
+ *   16-bit types: K % 8 == 0; N1, N2 (and N3) % 8 == 0; N1, N2 <= 256;
+ *                 N3 <= 4096 (the last GEMM runs in passes of up to 256).
+ *   B2B_TF32:     two stages; K % 4 == 0; N1 <= 256; N1, N2 % 4 == 0.
+ *   B2B_F64:      two stages; K % 4 == 0; N1, N2 in {16, 32, 64}.
+ * Binds to the current CUDA device, which must be an sm_103 GPU
+ * (B2B_ERR_DEVICE otherwise).  Allocates one 4-byte device status word.
+ * No kernel is launched.
+ */
+b2b_status_t b2b_plan_create(b2b_plan_t* out, b2b_dtype_t dtype, int64_t batch, int64_t M,
+                             int64_t K, int64_t N1, int64_t N2, int64_t N3);
+
+/*
+ * A single GEMM D = A.B (one operator, no fusion), used to build the unfused
+ * reference chain.  dtype gives the input and output types as above (the
+ * output of B2B_F16 / B2B_BF16 is 16-bit, of B2B_TF32 fp32).  Run it with
+ * b2b_run(plan, A, B, NULL, NULL, D, stream).
+ */
+b2b_status_t b2b_gemm_plan_create(b2b_plan_t* out, b2b_dtype_t dtype, int64_t batch, int64_t M,
+                                  int64_t K, int64_t N);
+
+/*
+ * Run the fused chain asynchronously on `stream` (rearrangement and
+ * execution, patent para. 54-60, 143).
+ *   A, B, C  device inputs as described above; F is the third weight for a
+ *            three-stage plan and must be NULL for a two-stage plan.
+ *            For a single-GEMM plan C and F must be NULL.
+ *   D        device output [batch][M][N_last]; must not overlap any input.
+ * Every pointer must be 16-byte aligned (B2B_ERR_ALIGNMENT).
+ * Returns B2B_ERR_CUDA if the launch fails.  A kernel that gives up a
+ * bounded wait records B2B_ERR_TIMEOUT in the plan's status word, which
+ * b2b_plan_device_status reports.  Runs on one plan from several streams
+ * may overlap: the plan is not modified by b2b_run.
+ */
+b2b_status_t b2b_run(b2b_plan_t plan, const void* A, const void* B, const void* C, const void* F,
+                     void* D, b2b_stream_t stream);
+
+/* Destroy a plan (NULL is accepted).  No run on it may still be in flight. */
+b2b_status_t b2b_plan_destroy(b2b_plan_t plan);
+
+/*
+ * Synchronise `stream`, then read and clear the plan's device status word:
+ * B2B_OK, or B2B_ERR_TIMEOUT if a kernel gave up a bounded wait since the
+ * last query.  Returns B2B_ERR_CUDA if the synchronisation itself fails.
+ */
+b2b_status_t b2b_plan_device_status(b2b_plan_t plan, b2b_stream_t stream);
+
+/* Time budget of every bounded wait inside the kernels of this plan, in
+ * nanoseconds (default 2e9).  0 restores the default. */
+b2b_status_t b2b_plan_set_wait_budget(b2b_plan_t plan, uint64_t budget_ns);
+
+/*
+ * Describe a plan: kernel launches per b2b_run, grid size, threads per CTA,
+ * dynamic shared memory per CTA, tensor-memory columns, ring depth and the
+ * number of passes of the last GEMM.  Any pointer may be NULL.
+ */
+b2b_status_t b2b_plan_info(b2b_plan_t plan, int* launches_per_run, int* grid, int* threads,
+                           int* smem_bytes, int* tmem_cols, int* ring_stages, int* passes);
+
+/* Human-readable name of a status code (static storage). */
+const char* b2b_status_string(b2b_status_t status);
+
+/*
+ * Coordination matrix of a register rearrangement (patent para. 75-102,
+ * Fig. 4; host only, no GPU needed).
+ * n threads each hold m values; receiver i's value r must come from thread
+ * src_thread[i*m + r], register src_reg[i*m + r].  The result is an n x m
+ * matrix H of triples (p, q, r) in P, Q, R (row-major, index i*m + j): in
+ * exchange round j, thread i takes value q of thread p and keeps it as its
+ * value r.  In every column the p's are distinct, so no thread is asked for
+ * two values in one round (para. 90).  Receivers are scheduled in order and
+ * each takes, round by round, its first remaining source that is still free
+ * in that round; if that greedy order gets stuck a depth-first search
+ * finishes the matrix.
+ * Returns B2B_OK, B2B_ERR_INVALID_ARG (bad sizes, a source used twice, or a
+ * thread asked for a number of values other than m), or B2B_ERR_UNSUPPORTED
+ * (no conflict-free schedule exists).
+ */
+b2b_status_t b2b_coordination_matrix(int n, int m, const int* src_thread, const int* src_reg,
+                                     int* P, int* Q, int* R);
+
+/*
+ * Layout probe of the accumulator -> operand rearrangement (test support).
+ * Runs the converter device code of the tcgen05 kernels on one 128-row tile:
+ * acc[128][width] (device, fp32 bit patterns) is written to tensor memory in
+ * the accumulator layout, read back by the same converter routine the fused
+ * kernel uses, rounded to the operand type of `dtype`, and the operand image
+ * is copied to `image` (device):
+ *   16-bit types: the K-major 128-byte-swizzled shared-memory image,
+ *                 width*256 bytes;
+ *   B2B_TF32:     the tensor-memory operand, 128 x width 32-bit words, row m
+ *                 then column k.
+ * width is 64, 128 or 256.  Synchronous.
+ */
+b2b_status_t b2b_probe_operand_image(b2b_dtype_t dtype, int width, const void* acc, void* image,
+                                     b2b_stream_t stream);
+
+/*
+ * Register probe of the fp64 rearrangement (test support).  One warp loads
+ * cfrag[lane][tiles*2] (device, the m8n8k4 accumulator fragments of `tiles`
+ * 8-column tiles, lane-major) into registers, performs the shuffle rounds
+ * the fp64 kernel derives from its coordination matrix, and writes the
+ * operand fragments afrag[lane][tiles*2] (device, lane-major).  tiles is 1..8.
+ * Synchronous.
+ */
+b2b_status_t b2b_probe_f64_rearrange(int tiles, const double* cfrag, double* afrag,
+                                     b2b_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* B2B_H_ */

@@ -1,0 +1,212 @@
+"""Parity of the CUDA path with the CPU oracle (needs a GB300).
+
+Every call goes through the C ABI (via the thin binding).  Bars:
+  - integer-valued inputs: bit-exact (every product and partial sum is an
+    integer below 2^24, so fp32 accumulation is exact and both sides round
+    the same exact values);
+  - random inputs: max|gpu - oracle| / max|oracle| <= 1e-2 (fp16, bf16),
+    5e-3 (tf32), 1e-12 (fp64);
+  - full-size workloads: the same bound on sampled rows, which the oracle
+    computes one by one.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads as wl
+
+pytestmark = pytest.mark.gpu
+
+b2b = pytest.importorskip("fusion_b2b_gemm_gb300")
+
+KINDS = {
+    "f16_f32out": (oracle.F32, oracle.F16, oracle.F32),
+    "f16": (oracle.F32, oracle.F16, oracle.F16),
+    "bf16": (oracle.F32, oracle.BF16, oracle.BF16),
+    "bf16_f32out": (oracle.F32, oracle.BF16, oracle.F32),
+    "tf32": (oracle.F32, oracle.TF32, oracle.F32),
+    "f64": (oracle.NONE, oracle.NONE, oracle.NONE),
+}
+TOL = {"f16_f32out": 1e-2, "f16": 1e-2, "bf16": 1e-2, "bf16_f32out": 1e-2, "tf32": 5e-3, "f64": 1e-12}
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda():
+    if not torch.cuda.is_available():
+        pytest.skip("no GPU")
+    torch.cuda.set_device(0)
+
+
+def run_gpu(w, host):
+    plan = b2b.Plan(w.dtype, w.batch, w.M, w.K, *w.N)
+    dev = [t.cuda() for t in host]
+    out = plan.run(*dev)
+    torch.cuda.synchronize()
+    assert plan.status() == 0
+    return out.cpu()
+
+
+def run_oracle(w, host, rows=None, batches=None):
+    A = oracle.widen(host[0])
+    Ws = [oracle.widen(t) for t in host[1:]]
+    if batches is not None:
+        A = A[batches]
+        Ws = [x[batches] for x in Ws]
+    if rows is not None:
+        A = A[:, rows]
+    acc, mid, fin = KINDS[w.dtype]
+    return oracle.chain(A, Ws, acc, mid, fin)
+
+
+def rel_err(got, want):
+    got = got.double().numpy() if isinstance(got, torch.Tensor) else got
+    return float(np.max(np.abs(got - want)) / max(np.max(np.abs(want)), 1e-300))
+
+
+def bits_equal(got: torch.Tensor, want: np.ndarray, dtype: str) -> bool:
+    """Exact equality of every output value (the oracle's values are already
+    rounded to the output type; +0 and -0 compare equal)."""
+    _, out_dt = wl.io_dtypes(dtype)
+    want_t = torch.from_numpy(want).to(out_dt)
+    return bool(torch.equal(got.double(), want_t.double()))
+
+
+# ------------------------------------------------------------ bit-exact --
+
+EXACT = [
+    wl.Workload("x_f16_f32out", "f16_f32out", 2, 300, 64, (64, 64), "int", 2, 11),
+    wl.Workload("x_f16", "f16", 3, 257, 128, (128, 128), "int", 2, 12),
+    wl.Workload("x_bf16_3", "bf16", 1, 300, 512, (256, 256, 512), "int", 1, 13),
+    wl.Workload("x_tf32", "tf32", 1, 333, 256, (256, 256), "int", 2, 14),
+    wl.Workload("x_f64", "f64", 2, 77, 64, (64, 64), "int", 2, 15),
+]
+
+
+@pytest.mark.parametrize("w", EXACT, ids=lambda w: w.name)
+def test_integer_inputs_bit_exact(w):
+    host = wl.make_inputs(w)
+    got = run_gpu(w, host)
+    want = run_oracle(w, host)
+    assert np.max(np.abs(want)) < 2 ** 24
+    assert bits_equal(got, want, w.dtype), f"max abs diff {np.max(np.abs(got.double().numpy() - want))}"
+
+
+# ------------------------------------------------------ random, reduced --
+
+REDUCED = [
+    wl.small(wl.WORKLOADS["tiny_f16"], M=256),
+    wl.small(wl.WORKLOADS["batched_f16"], M=500, batch=3),
+    wl.small(wl.WORKLOADS["tf32"], M=640),
+    wl.small(wl.WORKLOADS["f64"], M=200, batch=3),
+    wl.small(wl.WORKLOADS["three_stage_bf16"], M=520),
+]
+
+
+@pytest.mark.parametrize("w", REDUCED, ids=lambda w: w.name)
+def test_random_inputs_within_tolerance(w):
+    host = wl.make_inputs(w)
+    got = run_gpu(w, host)
+    want = run_oracle(w, host)
+    err = rel_err(got, want)
+    assert err <= TOL[w.dtype], err
+
+
+# ---------------------------------------------------------- edge cases --
+
+EDGES = [
+    wl.Workload("m1_f16", "f16_f32out", 1, 1, 64, (64, 64), "uniform", 1.0, 21),
+    wl.Workload("m5_batch3_f16", "f16", 3, 5, 128, (128, 128), "normal_fanin", 1.0, 22),
+    wl.Workload("narrow_n_f16", "f16_f32out", 2, 130, 64, (40, 56), "uniform", 1.0, 23),
+    wl.Workload("ragged_n_f16", "f16", 1, 129, 128, (96, 120), "normal_fanin", 1.0, 24),
+    wl.Workload("k_tail_f16", "f16", 2, 140, 72, (128, 128), "normal_fanin", 1.0, 25),
+    wl.Workload("n3_partial_bf16", "bf16", 1, 150, 512, (256, 256, 320), "normal_fanin", 1.0, 26),
+    wl.Workload("ragged_tf32", "tf32", 1, 190, 256, (200, 136), "normal", 1.0 / 16, 27),
+    wl.Workload("m13_f64", "f64", 3, 13, 64, (64, 64), "uniform", 1.0, 28),
+    wl.Workload("small_f64", "f64", 2, 40, 32, (32, 16), "uniform", 1.0, 29),
+]
+
+
+@pytest.mark.parametrize("w", EDGES, ids=lambda w: w.name)
+def test_edge_shapes(w):
+    host = wl.make_inputs(w)
+    got = run_gpu(w, host)
+    want = run_oracle(w, host)
+    assert rel_err(got, want) <= TOL[w.dtype]
+
+
+def test_empty_chain_is_a_no_op():
+    plan = b2b.Plan("f16", 1, 0, 64, 64, 64)
+    assert plan.info()["launches_per_run"] == 0
+    a = torch.zeros(16, dtype=torch.float16, device="cuda")
+    d = torch.full((16,), 7.0, dtype=torch.float16, device="cuda")
+    plan.run(a, a, a, None, d)
+    torch.cuda.synchronize()
+    assert torch.all(d == 7.0)
+
+
+def test_runs_are_deterministic():
+    w = wl.small(wl.WORKLOADS["batched_f16"], M=384, batch=2)
+    host = wl.make_inputs(w)
+    dev = [t.cuda() for t in host]
+    plan = b2b.Plan(w.dtype, w.batch, w.M, w.K, *w.N)
+    a = plan.run(*dev).clone()
+    b = plan.run(*dev).clone()
+    torch.cuda.synchronize()
+    assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+
+
+def test_argument_errors_on_device():
+    plan = b2b.Plan("f16", 1, 128, 64, 64, 64)
+    A = torch.zeros((1, 128, 64), dtype=torch.float16, device="cuda")
+    B = torch.zeros((1, 64, 64), dtype=torch.float16, device="cuda")
+    D = torch.zeros((1, 128, 64), dtype=torch.float16, device="cuda")
+    with pytest.raises(b2b.B2BError) as e:       # C missing
+        plan.run(A, B, None, None, D)
+    assert e.value.code == 1
+    with pytest.raises(b2b.B2BError) as e:       # F given to a two-stage plan
+        plan.run(A, B, B, B, D)
+    assert e.value.code == 1
+    with pytest.raises(b2b.B2BError) as e:       # output on top of an input
+        plan.run(A, B, B, None, A)
+    assert e.value.code == 4
+    raw = torch.zeros(128 * 64 + 8, dtype=torch.float16, device="cuda")
+    with pytest.raises(b2b.B2BError) as e:       # 2-byte offset: not 16-byte aligned
+        plan.run(raw[1:1 + 128 * 64], B, B, None, D)
+    assert e.value.code == 3
+
+
+# ------------------------------------------ unfused reference building block --
+
+@pytest.mark.parametrize("dtype,K,N", [("f16", 128, 128), ("f16_f32out", 64, 64), ("bf16", 256, 512),
+                                       ("tf32", 256, 256), ("f64", 64, 64)])
+def test_single_gemm_plan(dtype, K, N):
+    w = wl.Workload("gemm", dtype, 2, 300, K, (N,), "normal", 0.2, 31)
+    host = wl.make_inputs(w)
+    plan = b2b.GemmPlan(dtype, w.batch, w.M, K, N)
+    dev = [t.cuda() for t in host]
+    out = plan.run(*dev)
+    torch.cuda.synchronize()
+    assert plan.status() == 0
+    acc, _, fin = KINDS[dtype]
+    if dtype == "tf32":
+        fin = oracle.F32
+    want = oracle.chain(oracle.widen(host[0]), [oracle.widen(host[1])], acc, oracle.NONE, fin)
+    tol = 5e-3 if dtype == "tf32" else TOL[dtype]
+    assert rel_err(out.cpu(), want) <= tol
+
+
+# ------------------------------------------------ full-size, sampled rows --
+
+@pytest.mark.parametrize("name", list(wl.WORKLOADS))
+def test_full_size_sampled_rows(name):
+    w = wl.WORKLOADS[name]
+    host = wl.make_inputs(w)
+    got = run_gpu(w, host)
+    rng = np.random.default_rng(99)
+    batches = sorted(set([0, w.batch - 1] + list(rng.integers(0, w.batch, size=min(4, w.batch)))))
+    rows = sorted(set([0, 1, 127, 128, w.M - 1] + list(rng.integers(0, w.M, size=60))))
+    want = run_oracle(w, host, rows=rows, batches=batches)
+    sub = got[batches][:, rows]
+    assert rel_err(sub, want) <= TOL[w.dtype]
+    assert torch.isfinite(got.float()).all()

@@ -15,7 +15,7 @@ import os
 from typing import Optional, Sequence, Tuple
 
 __all__ = [
-    "B2BError", "DTYPES", "Plan", "GemmPlan", "library_path", "build",
+    "B2BError", "DTYPES", "Plan", "GemmPlan", "library_path",
     "b2b_plan_create", "b2b_gemm_plan_create", "b2b_run", "b2b_plan_destroy",
     "b2b_plan_device_status", "b2b_plan_set_wait_budget", "b2b_plan_info",
     "b2b_status_string", "b2b_coordination_matrix", "b2b_probe_operand_image",
@@ -39,11 +39,6 @@ class B2BError(RuntimeError):
 
 def library_path() -> str:
     return _LIB_PATH
-
-
-def build(force: bool = False) -> str:
-    from . import _build
-    return _build.build(force=force)
 
 
 def _load() -> ctypes.CDLL:

@@ -21,6 +21,7 @@
 #include "b2b.h"
 #include "chain_f64.cuh"
 #include "registry.h"
+#include "transpose.cuh"
 
 using namespace b2b;
 
@@ -67,7 +68,7 @@ uint32_t pow2_cols(uint32_t n) {
 
 const ChainKernelEntry* find_chain_kernel(int in, int out, int S, int n1p, int n2p, int nf,
                                           bool res) {
-  const ChainTable tables[] = {chain_table_f16(), chain_table_bf16(), chain_table_tf32()};
+  const ChainTable tables[] = {chain_table_f16(), chain_table_bf16(), chain_table_s3_f16(), chain_table_s3_bf16(), chain_table_tf32()};
   for (const ChainTable& t : tables)
     for (int i = 0; i < t.count; ++i) {
       const ChainKernelEntry& e = t.entries[i];
@@ -152,6 +153,9 @@ struct b2b_plan_s {
   F64Params f64;
   int* d_status;
   uint64_t budget_ns;
+  // tf32 only: the weights transposed to [N][K] before every run
+  void* d_wt;
+  size_t wt_bytes;
 };
 
 namespace {
@@ -321,7 +325,7 @@ b2b_status_t validate_sizes(b2b_dtype_t dt, int stages, int64_t batch, int64_t M
       }
       return B2B_OK;
     case B2B_TF32:
-      if (stages > 2) return B2B_ERR_UNSUPPORTED;
+      if (stages > 2 || batch > 32767) return B2B_ERR_UNSUPPORTED;
       if (K % 4) return B2B_ERR_UNSUPPORTED;
       for (int s = 0; s < stages; ++s) {
         if (N[s] % 4) return B2B_ERR_UNSUPPORTED;
@@ -400,8 +404,21 @@ b2b_status_t create_common(b2b_plan_t* out, b2b_dtype_t dt, int stages, bool sin
       st = B2B_ERR_CUDA;
     }
   }
+  if (st == B2B_OK && dt == B2B_TF32 && p->kind != kPlanEmpty) {
+    int64_t words = 0, kin = K;
+    for (int s = 0; s < stages; ++s) {
+      words += batch * kin * N[s];
+      kin = N[s];
+    }
+    p->wt_bytes = static_cast<size_t>(words) * 4;
+    if (cudaMalloc(&p->d_wt, p->wt_bytes) != cudaSuccess) {
+      cudaGetLastError();
+      st = B2B_ERR_CUDA;
+    }
+  }
   if (st != B2B_OK) {
     if (p->d_status) cudaFree(p->d_status);
+    if (p->d_wt) cudaFree(p->d_wt);
     delete p;
     return st;
   }
@@ -445,10 +462,41 @@ b2b_status_t run_chain_tc(b2b_plan_s* p, const void* const* W, const void* A, vo
   alignas(64) CUtensorMap maps[5];
   std::memset(maps, 0, sizeof(maps));
   b2b_status_t st = encode_3d(&maps[0], in_dt, p->esz, A, p->K, p->M, p->batch, CK, 128);
-  int64_t kin = p->K;
-  for (int s = 0; s < S && st == B2B_OK; ++s) {
-    st = encode_3d(&maps[1 + s], in_dt, p->esz, W[s], p->N[s], kin, p->batch, CK, CK);
-    kin = p->N[s];
+  if (p->in_kind == kInTF32) {
+    // The tf32 MMA reads B K-major: transpose every weight to [N][K] first.
+    TransposeJob job;
+    std::memset(&job, 0, sizeof(job));
+    job.batch = static_cast<int>(p->batch);
+    job.count = S;
+    uint32_t* dst = static_cast<uint32_t*>(p->d_wt);
+    int64_t kin = p->K;
+    int max_r = 0, max_c = 0;
+    for (int s = 0; s < S; ++s) {
+      job.in[s] = static_cast<const uint32_t*>(W[s]);
+      job.out[s] = dst;
+      job.rows[s] = static_cast<int>(kin);
+      job.cols[s] = static_cast<int>(p->N[s]);
+      max_r = std::max(max_r, job.rows[s]);
+      max_c = std::max(max_c, job.cols[s]);
+      dst += p->batch * kin * p->N[s];
+      kin = p->N[s];
+    }
+    const dim3 grid((max_c + 31) / 32, (max_r + 31) / 32, static_cast<unsigned>(S * p->batch));
+    transpose32_kernel<<<grid, 256, 0, stream>>>(job);
+    if (cudaGetLastError() != cudaSuccess) return B2B_ERR_CUDA;
+    kin = p->K;
+    for (int s = 0; s < S && st == B2B_OK; ++s) {
+      const uint32_t rows = s < S - 1 ? static_cast<uint32_t>(s == 0 ? p->n1p : p->n2p)
+                                      : static_cast<uint32_t>(p->nf);
+      st = encode_3d(&maps[1 + s], in_dt, p->esz, job.out[s], kin, p->N[s], p->batch, CK, rows);
+      kin = p->N[s];
+    }
+  } else {
+    int64_t kin = p->K;
+    for (int s = 0; s < S && st == B2B_OK; ++s) {
+      st = encode_3d(&maps[1 + s], in_dt, p->esz, W[s], p->N[s], kin, p->batch, CK, CK);
+      kin = p->N[s];
+    }
   }
   for (int s = S; s < 3; ++s) maps[1 + s] = maps[1];
   if (st == B2B_OK)
@@ -540,6 +588,7 @@ b2b_status_t b2b_run(b2b_plan_t p, const void* A, const void* B, const void* C, 
 b2b_status_t b2b_plan_destroy(b2b_plan_t p) {
   if (!p) return B2B_OK;
   if (p->d_status) cudaFree(p->d_status);
+  if (p->d_wt) cudaFree(p->d_wt);
   delete p;
   return B2B_OK;
 }
@@ -570,7 +619,7 @@ b2b_status_t b2b_plan_info(b2b_plan_t p, int* launches, int* grid, int* threads,
                            int* tmem_cols, int* ring_stages, int* passes) {
   if (!p) return B2B_ERR_INVALID_ARG;
   const bool tc = p->kind == kPlanChainTC || p->kind == kPlanGemmTC;
-  if (launches) *launches = p->kind == kPlanEmpty ? 0 : 1;
+  if (launches) *launches = p->kind == kPlanEmpty ? 0 : (p->d_wt ? 2 : 1);
   if (grid) *grid = p->grid;
   if (threads) *threads = p->threads;
   if (smem) *smem = p->smem_bytes;

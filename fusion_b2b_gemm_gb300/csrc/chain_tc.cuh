@@ -235,6 +235,10 @@ __global__ void __launch_bounds__(kChainThreads, 1)
   constexpr int WBOX_BYTES = CK * 128;
   constexpr int OBOX_N = 128 / OSZ;   // output columns per TMA store box
   constexpr bool P_TMEM = TF32;
+  // tf32 weights arrive transposed ([N][K], K-major): the tf32 MMA takes its
+  // B operand K-major only.  16-bit weights are read as stored ([K][N],
+  // MN-major B operand).
+  constexpr bool W_KMAJOR = TF32;
   constexpr uint32_t FMT = (IN == kInF16) ? 0u : (IN == kInBF16 ? 1u : 2u);
   constexpr int NPH_FIXED = S - 1;    // intermediate phases per tile
   static_assert(S >= 1 && S <= 3, "one to three cascaded GEMMs");
@@ -334,14 +338,24 @@ __global__ void __launch_bounds__(kChainThreads, 1)
             const uint32_t bytes = static_cast<uint32_t>(p.kpan0) * 128u * N1P +
                                    static_cast<uint32_t>(N1P / CK) * 128u * NF;
             mbar_arrive_expect_tx(bar(kBarWFull), bytes);
-            for (int kb = 0; kb < p.kpan0; ++kb)
-              for (int j = 0; j < N1P / WBOX_N; ++j)
-                tma_load_3d(base + p.off_wres0 + kb * 128u * N1P + j * WBOX_BYTES, &tmW0,
-                            bar(kBarWFull), j * WBOX_N, kb * CK, b);
-            for (int kb = 0; kb < N1P / CK; ++kb)
-              for (int j = 0; j < NF / WBOX_N; ++j)
-                tma_load_3d(base + p.off_wres1 + kb * 128u * NF + j * WBOX_BYTES, &tmW1,
-                            bar(kBarWFull), j * WBOX_N, kb * CK, b);
+            for (int kb = 0; kb < p.kpan0; ++kb) {
+              const uint32_t dst = base + p.off_wres0 + kb * 128u * N1P;
+              if constexpr (W_KMAJOR) {
+                tma_load_3d(dst, &tmW0, bar(kBarWFull), kb * CK, 0, b);
+              } else {
+                for (int j = 0; j < N1P / WBOX_N; ++j)
+                  tma_load_3d(dst + j * WBOX_BYTES, &tmW0, bar(kBarWFull), j * WBOX_N, kb * CK, b);
+              }
+            }
+            for (int kb = 0; kb < N1P / CK; ++kb) {
+              const uint32_t dst = base + p.off_wres1 + kb * 128u * NF;
+              if constexpr (W_KMAJOR) {
+                tma_load_3d(dst, &tmW1, bar(kBarWFull), kb * CK, 0, b);
+              } else {
+                for (int j = 0; j < NF / WBOX_N; ++j)
+                  tma_load_3d(dst + j * WBOX_BYTES, &tmW1, bar(kBarWFull), j * WBOX_N, kb * CK, b);
+              }
+            }
             cur_b = b;
             ++wl;
           }
@@ -364,9 +378,14 @@ __global__ void __launch_bounds__(kChainThreads, 1)
             mbar_arrive_expect_tx(bar(kBarFull + stage), bytes);
             if (s == 0) tma_load_3d(dst, &tmA, bar(kBarFull + stage), kb * CK, m0, b);
             if constexpr (!RES) {
-              for (int j = 0; j < width / WBOX_N; ++j)
-                tma_load_3d(dst + kPanelBytes + j * WBOX_BYTES, wm, bar(kBarFull + stage),
-                            n0 + j * WBOX_N, kb * CK, b);
+              if constexpr (W_KMAJOR) {
+                // one box: `width` rows of the transposed weight, 128 bytes of K
+                tma_load_3d(dst + kPanelBytes, wm, bar(kBarFull + stage), kb * CK, n0, b);
+              } else {
+                for (int j = 0; j < width / WBOX_N; ++j)
+                  tma_load_3d(dst + kPanelBytes + j * WBOX_BYTES, wm, bar(kBarFull + stage),
+                              n0 + j * WBOX_N, kb * CK, b);
+              }
             }
             ++issued;
             if (++stage == static_cast<uint32_t>(p.nst)) {
@@ -437,7 +456,7 @@ __global__ void __launch_bounds__(kChainThreads, 1)
           }
           tc_fence_after();
           const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(p.region_col[r]);
-          const uint32_t idesc = make_idesc(FMT, static_cast<uint32_t>(width), 128u, true);
+          const uint32_t idesc = make_idesc(FMT, static_cast<uint32_t>(width), 128u, !W_KMAJOR);
           const uint32_t wres = (s == 0) ? p.off_wres0 : p.off_wres1;
           for (int kb = 0; kb < kpan; ++kb) {
             const bool ring = (s == 0) || !RES;
@@ -453,7 +472,9 @@ __global__ void __launch_bounds__(kChainThreads, 1)
                 RES ? base + wres + static_cast<uint32_t>(kb) * 128u * width : sa + kPanelBytes;
 #pragma unroll
             for (int kk = 0; kk < CK / KSTEP; ++kk) {
-              const uint64_t bdesc = desc_sw128(b_base + kk * KSTEP * 128u, WBOX_BYTES, 1024u);
+              const uint64_t bdesc =
+                  W_KMAJOR ? desc_sw128(b_base + kk * 32u, 16u, 1024u)
+                           : desc_sw128(b_base + kk * KSTEP * 128u, WBOX_BYTES, 1024u);
               const uint32_t acc = (kb | kk) != 0 ? 1u : 0u;
               if (s == 0) {
                 mma_ss<TF32>(d_tmem, desc_sw128(sa + kk * 32u, 16u, 1024u), bdesc, idesc, acc);

@@ -4,8 +4,22 @@
 namespace b2b {
 namespace {
 const ChainKernelEntry kEntries[] = {
-    B2B_CHAIN_ENTRY(kInTF32, kOutF32, 2, 256, 64, 128, false),
+    B2B_CHAIN_ENTRY(kInTF32, kOutF32, 1, 64, 64, 64, false),
+    B2B_CHAIN_ENTRY(kInTF32, kOutF32, 1, 64, 64, 128, false),
     B2B_CHAIN_ENTRY(kInTF32, kOutF32, 1, 64, 64, 256, false),
+    B2B_CHAIN_ENTRY(kInTF32, kOutF32, 2, 64, 64, 64, false),
+    B2B_CHAIN_ENTRY(kInTF32, kOutF32, 2, 64, 64, 128, false),
+    B2B_CHAIN_ENTRY(kInTF32, kOutF32, 2, 64, 64, 256, false),
+    B2B_CHAIN_ENTRY(kInTF32, kOutF32, 2, 128, 64, 64, false),
+    B2B_CHAIN_ENTRY(kInTF32, kOutF32, 2, 128, 64, 128, false),
+    B2B_CHAIN_ENTRY(kInTF32, kOutF32, 2, 128, 64, 256, false),
+    B2B_CHAIN_ENTRY(kInTF32, kOutF32, 2, 256, 64, 64, false),
+    B2B_CHAIN_ENTRY(kInTF32, kOutF32, 2, 256, 64, 128, false),
+    B2B_CHAIN_ENTRY(kInTF32, kOutF32, 2, 256, 64, 256, false),
+    B2B_CHAIN_ENTRY(kInTF32, kOutF32, 2, 64, 64, 64, true),
+    B2B_CHAIN_ENTRY(kInTF32, kOutF32, 2, 64, 64, 128, true),
+    B2B_CHAIN_ENTRY(kInTF32, kOutF32, 2, 128, 64, 64, true),
+    B2B_CHAIN_ENTRY(kInTF32, kOutF32, 2, 128, 64, 128, true),
 };
 }  // namespace
 ChainTable chain_table_tf32() { return {kEntries, static_cast<int>(sizeof(kEntries) / sizeof(kEntries[0]))}; }

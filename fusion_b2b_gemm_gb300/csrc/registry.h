@@ -21,6 +21,8 @@ struct ChainTable {
 ChainTable chain_table_f16();
 ChainTable chain_table_bf16();
 ChainTable chain_table_tf32();
+ChainTable chain_table_s3_f16();
+ChainTable chain_table_s3_bf16();
 
 }  // namespace b2b
 

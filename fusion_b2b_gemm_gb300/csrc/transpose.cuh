@@ -1,0 +1,48 @@
+// Batched 2-D transpose of 32-bit words: out[b][c][r] = in[b][r][c].
+//
+// The tf32 tensor-core MMA reads its B operand K-major only (an MN-major
+// tf32 B descriptor yields zeros on sm_103a), while the weights of a chain
+// are stored row-major [K][N].  Before a tf32 chain runs, its weights are
+// turned into [N][K] in a plan-owned workspace by this kernel.  Two matrices
+// per launch (blockIdx.z = matrix * batch + b); 32x32 tiles through shared
+// memory so that reads and writes are both coalesced.
+#pragma once
+
+#include <cstdint>
+
+namespace b2b {
+
+struct TransposeJob {
+  const uint32_t* in[2];
+  uint32_t* out[2];
+  int rows[2], cols[2];  // of the input matrix
+  int batch;
+  int count;             // matrices in this launch (1 or 2)
+};
+
+__global__ void __launch_bounds__(256) transpose32_kernel(const __grid_constant__ TransposeJob job) {
+  __shared__ uint32_t tile[32][33];
+  const int z = blockIdx.z;
+  const int mat = z / job.batch;
+  const int b = z % job.batch;
+  if (mat >= job.count) return;
+  const int R = job.rows[mat], C = job.cols[mat];
+  const int r0 = blockIdx.y * 32, c0 = blockIdx.x * 32;
+  if (r0 >= R || c0 >= C) return;
+  const uint32_t* in = job.in[mat] + static_cast<size_t>(b) * R * C;
+  uint32_t* out = job.out[mat] + static_cast<size_t>(b) * R * C;
+  const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;  // 32 x 8
+#pragma unroll
+  for (int i = 0; i < 32; i += 8) {
+    const int r = r0 + ty + i, c = c0 + tx;
+    if (r < R && c < C) tile[ty + i][tx] = in[static_cast<size_t>(r) * C + c];
+  }
+  __syncthreads();
+#pragma unroll
+  for (int i = 0; i < 32; i += 8) {
+    const int c = c0 + ty + i, r = r0 + tx;
+    if (r < R && c < C) out[static_cast<size_t>(c) * R + r] = tile[tx][ty + i];
+  }
+}
+
+}  // namespace b2b

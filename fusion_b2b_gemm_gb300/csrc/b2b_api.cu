@@ -171,10 +171,19 @@ b2b_status_t setup_chain_tc(b2b_plan_s* p) {
   const int nl = static_cast<int>(std::max<int64_t>(64, pad64(nlast)));
   const int base_z = (S >= 2 ? p->n1p : 0) + (S >= 3 ? p->n2p : 0);
 
-  int nf = 0, nz = -1;
+  int nf = 0, nz = -1, lookahead = 0;
   const int cands[3] = {256, 128, 64};
-  for (int c : cands)
-    if (c <= nl && base_z + 2 * c <= 512) { nf = c; nz = 2; break; }
+  // Two-stage chains: prefer a double-buffered GEMM1 accumulator (GEMM1 of
+  // the next tile then runs while the current tile is rearranged).
+  if (S == 2) {
+    const int base_la = 2 * p->n1p;
+    for (int k = 2; k >= 1 && nz < 0; --k)
+      for (int c : cands)
+        if (c <= nl && base_la + k * c <= 512) { nf = c; nz = k; lookahead = 1; break; }
+  }
+  if (nz < 0)
+    for (int c : cands)
+      if (c <= nl && base_z + 2 * c <= 512) { nf = c; nz = 2; break; }
   if (nz < 0)
     for (int c : cands)
       if (c <= nl && base_z + c <= 512) { nf = c; nz = 1; break; }
@@ -197,15 +206,18 @@ b2b_status_t setup_chain_tc(b2b_plan_s* p) {
   c.npass = static_cast<int>((nlast + nf - 1) / nf);
   c.kpan0 = static_cast<int>((p->K + CK - 1) / CK);
   c.nz = nz;
+  c.lookahead = lookahead;
+  const int zbase = lookahead ? 2 * p->n1p : base_z;
   c.region_col[0] = 0;
-  c.region_col[1] = S >= 3 ? p->n1p : 0;
-  c.region_col[2] = base_z;
-  c.region_col[3] = base_z + nf;
+  c.region_col[1] = (S >= 3 || lookahead) ? p->n1p : 0;
+  c.region_col[2] = zbase;
+  c.region_col[3] = zbase + nf;
   if (nz == 0) {  // the final passes reuse X and Y in turn
     c.region_col[2] = c.region_col[0];
     c.region_col[3] = c.region_col[1];
   }
-  const uint32_t cols_used = nz > 0 ? static_cast<uint32_t>(base_z + nz * nf) : static_cast<uint32_t>(base_z);
+  const uint32_t cols_used =
+      nz > 0 ? static_cast<uint32_t>(zbase + nz * nf) : static_cast<uint32_t>(base_z);
   c.tmem_cols = pow2_cols(cols_used);
   if (c.tmem_cols > 512) return B2B_ERR_UNSUPPORTED;
 

@@ -75,6 +75,7 @@ struct ChainParams {
   uint32_t tmem_cols;
   int region_col[4];  // X, Y, Z0, Z1 (TMEM column offsets)
   int nz;             // Z buffers for the final accumulator; 0 = reuse X/Y in turn
+  int lookahead;      // two-stage only: GEMM1 double-buffered (X, Y) and issued a tile ahead
   int* status;
   unsigned long long budget_ns;
 };
@@ -87,6 +88,11 @@ struct ChainParams {
 __host__ __device__ __forceinline__ void region_use(const ChainParams& p, int S, int it, int ph,
                                                     int& r, uint32_t& u) {
   const int ux = 1 + (p.npass + 1) / 2, uy = 1 + p.npass / 2;
+  if (p.lookahead && ph == 0) {  // GEMM1 alternates between two buffers
+    r = it & 1;
+    u = static_cast<uint32_t>(it) >> 1;
+    return;
+  }
   if (ph < S - 1) {
     r = ph;
     u = (p.nz > 0) ? static_cast<uint32_t>(it)
@@ -313,6 +319,32 @@ __global__ void __launch_bounds__(kChainThreads, 1)
   auto stage_width = [](int s) -> int { return s < S - 1 ? (s == 0 ? N1P : N2P) : NF; };
   auto stage_kpan = [&](int s) -> int { return s == 0 ? p.kpan0 : (s == 1 ? N1P / CK : N2P / CK); };
 
+  // Order in which the producer loads and the MMA thread computes the phases.
+  // Plain order: every phase of tile 0, then of tile 1, ...  With lookahead
+  // (two-stage chains whose first accumulator is double-buffered in tensor
+  // memory), GEMM1 of tile it+1 is issued before GEMM2 of tile it, so the
+  // tensor cores work on GEMM1(it+1) while the converters rearrange tile it.
+  // Across a change of batch with resident weights there is no lookahead:
+  // the new weights may only land after GEMM2 of the old batch.
+  const bool lookahead = p.lookahead != 0;
+  auto batch_of = [&](int it) -> int { return (t_begin + it * t_step) / p.m_tiles; };
+  auto for_each_phase = [&](auto&& fn) {
+    if (!lookahead) {
+      for (int it = 0; it < t_count; ++it)
+        for (int ph = 0; ph < nph; ++ph)
+          if (!fn(it, ph)) return;
+      return;
+    }
+    if (t_count > 0 && !fn(0, 0)) return;
+    for (int it = 0; it < t_count; ++it) {
+      const bool ahead = it + 1 < t_count && (!RES || batch_of(it + 1) == batch_of(it));
+      if (ahead && !fn(it + 1, 0)) return;
+      for (int ph = 1; ph < nph; ++ph)
+        if (!fn(it, ph)) return;
+      if (!ahead && it + 1 < t_count && !fn(it + 1, 0)) return;
+    }
+  };
+
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
@@ -324,17 +356,13 @@ __global__ void __launch_bounds__(kChainThreads, 1)
       uint32_t stage = 0, phase = 0, wl = 0;
       uint64_t issued = 0;
       int cur_b = -1;
-      bool ok = true;
-      for (int it = 0; it < t_count && ok; ++it) {
+      for_each_phase([&](int it, int ph) -> bool {
         const int tile = t_begin + it * t_step;
         const int b = tile / p.m_tiles;
         const int m0 = (tile % p.m_tiles) * 128;
         if constexpr (RES) {
-          if (b != cur_b) {
-            if (wl > 0 && !bw.wait(bar(kBarWEmpty), (wl - 1) & 1u)) {
-              ok = false;
-              break;
-            }
+          if (ph == 0 && b != cur_b) {
+            if (wl > 0 && !bw.wait(bar(kBarWEmpty), (wl - 1) & 1u)) return false;
             const uint32_t bytes = static_cast<uint32_t>(p.kpan0) * 128u * N1P +
                                    static_cast<uint32_t>(N1P / CK) * 128u * NF;
             mbar_arrive_expect_tx(bar(kBarWFull), bytes);
@@ -360,41 +388,37 @@ __global__ void __launch_bounds__(kChainThreads, 1)
             ++wl;
           }
         }
-        for (int ph = 0; ph < nph && ok; ++ph) {
-          const int s = ph < S - 1 ? ph : S - 1;
-          if (RES && s != 0) continue;
-          const int width = stage_width(s);
-          const int n0 = ph < S - 1 ? 0 : (ph - (S - 1)) * NF;
-          const int kpan = stage_kpan(s);
-          const CUtensorMap* wm = s == 0 ? &tmW0 : (s == 1 ? &tmW1 : &tmW2);
-          for (int kb = 0; kb < kpan; ++kb) {
-            if (!bw.wait(bar(kBarEmpty + stage), phase ^ 1u)) {
-              ok = false;
-              break;
-            }
-            const uint32_t dst = base + p.off_ring + stage * p.stage_bytes;
-            const uint32_t bytes =
-                (s == 0 ? kPanelBytes : 0u) + (RES ? 0u : 128u * static_cast<uint32_t>(width));
-            mbar_arrive_expect_tx(bar(kBarFull + stage), bytes);
-            if (s == 0) tma_load_3d(dst, &tmA, bar(kBarFull + stage), kb * CK, m0, b);
-            if constexpr (!RES) {
-              if constexpr (W_KMAJOR) {
-                // one box: `width` rows of the transposed weight, 128 bytes of K
-                tma_load_3d(dst + kPanelBytes, wm, bar(kBarFull + stage), kb * CK, n0, b);
-              } else {
-                for (int j = 0; j < width / WBOX_N; ++j)
-                  tma_load_3d(dst + kPanelBytes + j * WBOX_BYTES, wm, bar(kBarFull + stage),
-                              n0 + j * WBOX_N, kb * CK, b);
-              }
-            }
-            ++issued;
-            if (++stage == static_cast<uint32_t>(p.nst)) {
-              stage = 0;
-              phase ^= 1u;
+        const int s = ph < S - 1 ? ph : S - 1;
+        if (RES && s != 0) return true;
+        const int width = stage_width(s);
+        const int n0 = ph < S - 1 ? 0 : (ph - (S - 1)) * NF;
+        const int kpan = stage_kpan(s);
+        const CUtensorMap* wm = s == 0 ? &tmW0 : (s == 1 ? &tmW1 : &tmW2);
+        for (int kb = 0; kb < kpan; ++kb) {
+          if (!bw.wait(bar(kBarEmpty + stage), phase ^ 1u)) return false;
+          const uint32_t dst = base + p.off_ring + stage * p.stage_bytes;
+          const uint32_t bytes =
+              (s == 0 ? kPanelBytes : 0u) + (RES ? 0u : 128u * static_cast<uint32_t>(width));
+          mbar_arrive_expect_tx(bar(kBarFull + stage), bytes);
+          if (s == 0) tma_load_3d(dst, &tmA, bar(kBarFull + stage), kb * CK, m0, b);
+          if constexpr (!RES) {
+            if constexpr (W_KMAJOR) {
+              // one box: `width` rows of the transposed weight, 128 bytes of K
+              tma_load_3d(dst + kPanelBytes, wm, bar(kBarFull + stage), kb * CK, n0, b);
+            } else {
+              for (int j = 0; j < width / WBOX_N; ++j)
+                tma_load_3d(dst + kPanelBytes + j * WBOX_BYTES, wm, bar(kBarFull + stage),
+                            n0 + j * WBOX_N, kb * CK, b);
             }
           }
+          ++issued;
+          if (++stage == static_cast<uint32_t>(p.nst)) {
+            stage = 0;
+            phase ^= 1u;
+          }
         }
-      }
+        return true;
+      });
       // Wait for every copy still in flight before the CTA may exit.
       const uint64_t nst = static_cast<uint64_t>(p.nst);
       const uint64_t tail = issued < nst ? issued : nst;
@@ -410,103 +434,91 @@ __global__ void __launch_bounds__(kChainThreads, 1)
     if (lane == 0) {
       uint32_t stage = 0, phase = 0, pf = 0, wl = 0;
       int cur_b = -1;
-      bool ok = true;
-      for (int it = 0; it < t_count && ok; ++it) {
+      for_each_phase([&](int it, int ph) -> bool {
         const int tile = t_begin + it * t_step;
         const int b = tile / p.m_tiles;
-        if constexpr (RES) {
-          if (b != cur_b) {
-            if (!bw.wait(bar(kBarWFull), wl & 1u)) {
-              ok = false;
-              break;
-            }
-            ++wl;
-            cur_b = b;
-            tc_fence_after();
-          }
-        }
-        if constexpr (P_TMEM) {
-          // The intermediate of the previous tile (in region X) must be fully
-          // read before GEMM1 of this tile overwrites X.
-          if (it > 0 && !bw.wait(bar(kBarPEmpty), (it - 1) & 1u)) {
-            ok = false;
-            break;
-          }
-        }
-        for (int ph = 0; ph < nph && ok; ++ph) {
-          const int s = ph < S - 1 ? ph : S - 1;
-          const int width = stage_width(s);
-          const int kpan = stage_kpan(s);
-          // The first phase that reads an intermediate waits for its operand
-          // (the later passes of the last GEMM read the same operand).
-          if (s >= 1 && ph == s) {
-            if (!bw.wait(bar(kBarPFull), pf & 1u)) {
-              ok = false;
-              break;
-            }
-            ++pf;
-            tc_fence_after();
-          }
-          int r;
-          uint32_t u;
-          region_use(p, S, it, ph, r, u);
-          if (!bw.wait(bar(kBarREmpty + r), (u & 1u) ^ 1u)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(p.region_col[r]);
-          const uint32_t idesc = make_idesc(FMT, static_cast<uint32_t>(width), 128u, !W_KMAJOR);
-          const uint32_t wres = (s == 0) ? p.off_wres0 : p.off_wres1;
-          for (int kb = 0; kb < kpan; ++kb) {
-            const bool ring = (s == 0) || !RES;
-            const uint32_t sa = base + p.off_ring + stage * p.stage_bytes;
-            if (ring) {
-              if (!bw.wait(bar(kBarFull + stage), phase)) {
-                ok = false;
-                break;
-              }
+        if (ph == 0) {
+          if constexpr (RES) {
+            if (b != cur_b) {
+              if (!bw.wait(bar(kBarWFull), wl & 1u)) return false;
+              ++wl;
+              cur_b = b;
               tc_fence_after();
             }
-            const uint32_t b_base =
-                RES ? base + wres + static_cast<uint32_t>(kb) * 128u * width : sa + kPanelBytes;
+          }
+          if constexpr (P_TMEM) {
+            // The intermediate that last lived in this GEMM1 region (tile
+            // it-1, or it-2 with two alternating regions) must be fully read
+            // by GEMM2 before GEMM1 of this tile overwrites it.
+            const int prev = it - (lookahead ? 2 : 1);
+            if (prev >= 0 && !bw.wait(bar(kBarPEmpty), static_cast<uint32_t>(prev) & 1u)) return false;
+          }
+        }
+        const int s = ph < S - 1 ? ph : S - 1;
+        const int width = stage_width(s);
+        const int kpan = stage_kpan(s);
+        // The first phase that reads an intermediate waits for its operand
+        // (the later passes of the last GEMM read the same operand).
+        if (s >= 1 && ph == s) {
+          if (!bw.wait(bar(kBarPFull), pf & 1u)) return false;
+          ++pf;
+          tc_fence_after();
+        }
+        int r;
+        uint32_t u;
+        region_use(p, S, it, ph, r, u);
+        if (!bw.wait(bar(kBarREmpty + r), (u & 1u) ^ 1u)) return false;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(p.region_col[r]);
+        const uint32_t idesc = make_idesc(FMT, static_cast<uint32_t>(width), 128u, !W_KMAJOR);
+        const uint32_t wres = (s == 0) ? p.off_wres0 : p.off_wres1;
+        // the operand of a later stage: which region holds the intermediate
+        const uint32_t a_tmem =
+            tmem_base + static_cast<uint32_t>(p.region_col[(lookahead && s >= 1) ? (it & 1) : 0]);
+        for (int kb = 0; kb < kpan; ++kb) {
+          const bool ring = (s == 0) || !RES;
+          const uint32_t sa = base + p.off_ring + stage * p.stage_bytes;
+          if (ring) {
+            if (!bw.wait(bar(kBarFull + stage), phase)) return false;
+            tc_fence_after();
+          }
+          const uint32_t b_base =
+              RES ? base + wres + static_cast<uint32_t>(kb) * 128u * width : sa + kPanelBytes;
 #pragma unroll
-            for (int kk = 0; kk < CK / KSTEP; ++kk) {
-              const uint64_t bdesc =
-                  W_KMAJOR ? desc_sw128(b_base + kk * 32u, 16u, 1024u)
-                           : desc_sw128(b_base + kk * KSTEP * 128u, WBOX_BYTES, 1024u);
-              const uint32_t acc = (kb | kk) != 0 ? 1u : 0u;
-              if (s == 0) {
-                mma_ss<TF32>(d_tmem, desc_sw128(sa + kk * 32u, 16u, 1024u), bdesc, idesc, acc);
-              } else if constexpr (P_TMEM) {
-                mma_ts<TF32>(d_tmem,
-                             tmem_base + static_cast<uint32_t>(p.region_col[0] + kb * CK + kk * KSTEP),
-                             bdesc, idesc, acc);
-              } else {
-                mma_ss<TF32>(d_tmem,
-                             desc_sw128(base + p.off_p + kb * kPanelBytes + kk * 32u, 16u, 1024u),
-                             bdesc, idesc, acc);
-              }
-            }
-            if (ring) {
-              tc_commit(bar(kBarEmpty + stage));
-              if (++stage == static_cast<uint32_t>(p.nst)) {
-                stage = 0;
-                phase ^= 1u;
-              }
+          for (int kk = 0; kk < CK / KSTEP; ++kk) {
+            const uint64_t bdesc =
+                W_KMAJOR ? desc_sw128(b_base + kk * 32u, 16u, 1024u)
+                         : desc_sw128(b_base + kk * KSTEP * 128u, WBOX_BYTES, 1024u);
+            const uint32_t acc = (kb | kk) != 0 ? 1u : 0u;
+            if (s == 0) {
+              mma_ss<TF32>(d_tmem, desc_sw128(sa + kk * 32u, 16u, 1024u), bdesc, idesc, acc);
+            } else if constexpr (P_TMEM) {
+              mma_ts<TF32>(d_tmem, a_tmem + static_cast<uint32_t>(kb * CK + kk * KSTEP), bdesc, idesc,
+                           acc);
+            } else {
+              mma_ss<TF32>(d_tmem,
+                           desc_sw128(base + p.off_p + kb * kPanelBytes + kk * 32u, 16u, 1024u),
+                           bdesc, idesc, acc);
             }
           }
-          if (!ok) break;
-          tc_commit(bar(ph < S - 1 ? kBarCFull + r : kBarRFull + r));
-          if (S >= 2 && ph == nph - 1) tc_commit(bar(kBarPEmpty));
-        }
-        if constexpr (RES) {
-          if (ok && it + 1 < t_count) {
-            const int nb = (t_begin + (it + 1) * t_step) / p.m_tiles;
-            if (nb != b) tc_commit(bar(kBarWEmpty));
+          if (ring) {
+            tc_commit(bar(kBarEmpty + stage));
+            if (++stage == static_cast<uint32_t>(p.nst)) {
+              stage = 0;
+              phase ^= 1u;
+            }
           }
         }
-      }
+        tc_commit(bar(ph < S - 1 ? kBarCFull + r : kBarRFull + r));
+        if (S >= 2 && ph == nph - 1) {
+          tc_commit(bar(kBarPEmpty));
+          // release the resident weights at the end of a batch segment
+          if (RES && it + 1 < t_count && batch_of(it + 1) != b) tc_commit(bar(kBarWEmpty));
+        }
+        if (S == 1 && RES && ph == nph - 1 && it + 1 < t_count && batch_of(it + 1) != b)
+          tc_commit(bar(kBarWEmpty));
+        return true;
+      });
       // Every MMA issued so far must be complete before tensor memory is freed.
       tc_commit(bar(kBarDrain));
       drain_wait(bar(kBarDrain), 0, p.budget_ns);
@@ -527,8 +539,10 @@ __global__ void __launch_bounds__(kChainThreads, 1)
             ok = false;
             break;
           }
-          // region r (X or Y) receives one intermediate per tile
-          if (!warp_wait(bw, bar(kBarCFull + r), static_cast<uint32_t>(it) & 1u)) {
+          // region r receives one intermediate per tile (per two tiles for
+          // each of the two buffers of a lookahead chain)
+          const uint32_t cu = lookahead ? static_cast<uint32_t>(it) >> 1 : static_cast<uint32_t>(it);
+          if (!warp_wait(bw, bar(kBarCFull + r), cu & 1u)) {
             ok = false;
             break;
           }

@@ -175,7 +175,7 @@ b2b_status_t setup_chain_tc(b2b_plan_s* p) {
   const int cands[3] = {256, 128, 64};
   // Two-stage chains: prefer a double-buffered GEMM1 accumulator (GEMM1 of
   // the next tile then runs while the current tile is rearranged).
-  if (S == 2) {
+  if (S == 2 && p->in_kind != kInTF32) {
     const int base_la = 2 * p->n1p;
     for (int k = 2; k >= 1 && nz < 0; --k)
       for (int c : cands)
@@ -230,7 +230,8 @@ b2b_status_t setup_chain_tc(b2b_plan_s* p) {
   struct Layout { bool res; uint32_t stage, wres0, wres1; int nst, nstg; };
   auto fit = [&](bool res) -> Layout {
     Layout L{res, 0, 0, 0, 0, 0};
-    L.stage = res ? kPanelBytes : kPanelBytes + 128u * maxw;
+    // resident weights: a ring stage holds a whole A tile (all K panels)
+    L.stage = res ? static_cast<uint32_t>(c.kpan0) * kPanelBytes : kPanelBytes + 128u * maxw;
     if (res) {
       L.wres0 = static_cast<uint32_t>(c.kpan0) * 128u * p->n1p;
       L.wres1 = static_cast<uint32_t>(p->n1p / CK) * 128u * nf;
@@ -246,7 +247,7 @@ b2b_status_t setup_chain_tc(b2b_plan_s* p) {
     return L;
   };
   Layout L = fit(false);
-  if (S == 2 && c.npass == 1 &&
+  if (S == 2 && c.npass == 1 && c.kpan0 <= 4 &&
       find_chain_kernel(p->in_kind, p->out_kind, S, p->n1p, p->n2p, nf, true)) {
     Layout R = fit(true);
     if (R.nst >= 3) L = R;

@@ -19,11 +19,13 @@
 // tf32 MMA can take its A operand from tensor memory, where the layout of
 // rule 2 equals rule 1.
 //
-// CTA roles (320 threads, one CTA per SM, persistent over 128-row tiles):
+// CTA roles (352 threads, one CTA per SM, persistent over 128-row tiles):
 //   warp 0     TMA producer: A panels and weight panels into a ring of stages
-//   warp 1     TMEM allocator and the single MMA-issuing thread
+//   warp 1     TMEM allocator and the MMA-issuing thread (GEMM1 only when the
+//              weights are resident; then warp 10 issues GEMM2)
 //   warps 2-5  converters: accumulator -> operand (the rearrangement)
 //   warps 6-9  epilogue: accumulator -> output type -> swizzled staging -> TMA store
+//   warp 10    second MMA-issuing thread (resident-weight chains)
 // Every wait is bounded (ptx::BoundedWait); on a timeout the CTA raises an
 // abort flag, every role leaves its loop, in-flight copies and MMAs are
 // drained, tensor memory is freed and the status word reports the timeout.
@@ -39,7 +41,7 @@ namespace b2b {
 enum : int { kInF16 = 0, kInBF16 = 1, kInTF32 = 2 };
 enum : int { kOutF32 = 0, kOutF16 = 1, kOutBF16 = 2 };
 
-constexpr int kChainThreads = 320;
+constexpr int kChainThreads = 352;
 constexpr int kPanelBytes = 128 * 128;  // one 128-row x 128-byte swizzled panel
 constexpr int kBarBytes = 512;
 constexpr int kTimeoutCode = 7;         // B2B_ERR_TIMEOUT
@@ -57,7 +59,8 @@ enum : int {
   kBarEpiSync = 28,
   kBarDrain = 29,
   kBarCFull = 30,   // [2] region X / Y holds an intermediate for the converters
-  kSlotTmem = 32,   // uint32 TMEM base address, then the int abort flag
+  kBarDrain2 = 32,
+  kSlotTmem = 33,   // uint32 TMEM base address, then the int abort flag
 };
 // Each consumer warpgroup has its own "full" barrier per region, so that it
 // sees every completion of that barrier in order: when the last GEMM reuses
@@ -223,6 +226,26 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, uint64
   }
 }
 
+// Tiles of one CTA, walked without divisions: batch b and 128-row tile mt.
+struct TileCursor {
+  int b, mt, db, dmt, m_tiles;
+  __device__ __forceinline__ void init(int tile, int step, int mtiles) {
+    m_tiles = mtiles;
+    b = tile / mtiles;
+    mt = tile - b * mtiles;
+    db = step / mtiles;
+    dmt = step - db * mtiles;
+  }
+  __device__ __forceinline__ void next() {
+    mt += dmt;
+    b += db;
+    if (mt >= m_tiles) {
+      mt -= m_tiles;
+      ++b;
+    }
+  }
+};
+
 template <int IN, int OUT, int S, int N1P, int N2P, int NF, bool RES>
 __global__ void __launch_bounds__(kChainThreads, 1)
     chain_tc_kernel(const __grid_constant__ CUtensorMap tmA,
@@ -245,6 +268,11 @@ __global__ void __launch_bounds__(kChainThreads, 1)
   // B operand K-major only.  16-bit weights are read as stored ([K][N],
   // MN-major B operand).
   constexpr bool W_KMAJOR = TF32;
+  // With resident weights (16-bit), GEMM1 and GEMM2 are issued by two
+  // threads (warps 1 and 10): the tensor pipe holds little more than the MMA
+  // being executed, so every wait of a single issuing thread would leave it
+  // idle; with two issuers one waits while the other issues.
+  constexpr bool SPLIT = RES && !TF32;
   constexpr uint32_t FMT = (IN == kInF16) ? 0u : (IN == kInBF16 ? 1u : 2u);
   constexpr int NPH_FIXED = S - 1;    // intermediate phases per tile
   static_assert(S >= 1 && S <= 3, "one to three cascaded GEMMs");
@@ -271,7 +299,7 @@ __global__ void __launch_bounds__(kChainThreads, 1)
       mbar_init(bar(kBarEmpty + i), 1);
     }
     mbar_init(bar(kBarWFull), 1);
-    mbar_init(bar(kBarWEmpty), 1);
+    mbar_init(bar(kBarWEmpty), SPLIT ? 2 : 1);
     for (int i = 0; i < 4; ++i) {
       mbar_init(bar(kBarRFull + i), 1);
       mbar_init(bar(kBarREmpty + i), 128);
@@ -282,6 +310,7 @@ __global__ void __launch_bounds__(kChainThreads, 1)
     mbar_init(bar(kBarPEmpty), 1);
     mbar_init(bar(kBarEpiSync), 128);
     mbar_init(bar(kBarDrain), 1);
+    mbar_init(bar(kBarDrain2), 1);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -314,35 +343,99 @@ __global__ void __launch_bounds__(kChainThreads, 1)
                   ? (p.total_tiles - static_cast<int>(blockIdx.x) + gridDim.x - 1) / gridDim.x
                   : 0;
   }
+  TileCursor first;
+  first.init(t_begin, t_step, p.m_tiles);
   const int nph = NPH_FIXED + p.npass;
+  const bool lookahead = p.lookahead != 0;
 
   auto stage_width = [](int s) -> int { return s < S - 1 ? (s == 0 ? N1P : N2P) : NF; };
   auto stage_kpan = [&](int s) -> int { return s == 0 ? p.kpan0 : (s == 1 ? N1P / CK : N2P / CK); };
+  // With resident weights the ring carries whole A tiles (kpan0 panels per
+  // stage); otherwise one panel (A and/or weight) per stage.
+  auto panels_per_stage = [&](int s) -> int { return (RES && s == 0) ? p.kpan0 : 1; };
+  // Final-pass region index without divisions (nz is 1 or 2).
+  auto zregion = [&](int it, int pass, int& r, uint32_t& u) {
+    const uint32_t g = static_cast<uint32_t>(it) * static_cast<uint32_t>(p.npass) + pass;
+    r = 2 + ((p.nz == 2) ? static_cast<int>(g & 1u) : 0);
+    u = (p.nz == 2) ? (g >> 1) : g;
+  };
 
-  // Order in which the producer loads and the MMA thread computes the phases.
-  // Plain order: every phase of tile 0, then of tile 1, ...  With lookahead
-  // (two-stage chains whose first accumulator is double-buffered in tensor
-  // memory), GEMM1 of tile it+1 is issued before GEMM2 of tile it, so the
-  // tensor cores work on GEMM1(it+1) while the converters rearrange tile it.
-  // Across a change of batch with resident weights there is no lookahead:
-  // the new weights may only land after GEMM2 of the old batch.
-  const bool lookahead = p.lookahead != 0;
-  auto batch_of = [&](int it) -> int { return (t_begin + it * t_step) / p.m_tiles; };
+  // Order in which the producer loads and a single MMA thread computes the
+  // phases.  Plain order: every phase of tile 0, then of tile 1, ...  With
+  // lookahead (two-stage chains whose first accumulator is double-buffered in
+  // tensor memory), GEMM1 of tile it+1 comes before GEMM2 of tile it.  Across a
+  // change of batch with resident weights there is no lookahead: the new
+  // weights may only land after GEMM2 of the old batch.
   auto for_each_phase = [&](auto&& fn) {
+    TileCursor cur = first;
     if (!lookahead) {
-      for (int it = 0; it < t_count; ++it)
+      for (int it = 0; it < t_count; ++it, cur.next())
         for (int ph = 0; ph < nph; ++ph)
-          if (!fn(it, ph)) return;
+          if (!fn(it, ph, cur)) return;
       return;
     }
-    if (t_count > 0 && !fn(0, 0)) return;
-    for (int it = 0; it < t_count; ++it) {
-      const bool ahead = it + 1 < t_count && (!RES || batch_of(it + 1) == batch_of(it));
-      if (ahead && !fn(it + 1, 0)) return;
+    TileCursor nxt = first;
+    if (t_count > 0 && !fn(0, 0, cur)) return;
+    nxt.next();
+    for (int it = 0; it < t_count; ++it, cur.next(), nxt.next()) {
+      const bool more = it + 1 < t_count;
+      const bool ahead = more && (!RES || nxt.b == cur.b);
+      if (ahead && !fn(it + 1, 0, nxt)) return;
       for (int ph = 1; ph < nph; ++ph)
-        if (!fn(it, ph)) return;
-      if (!ahead && it + 1 < t_count && !fn(it + 1, 0)) return;
+        if (!fn(it, ph, cur)) return;
+      if (!ahead && more && !fn(it + 1, 0, nxt)) return;
     }
+  };
+
+  // One GEMM phase issued by the calling thread: operands from the ring
+  // and/or resident weights and/or the intermediate, accumulator in region r.
+  // `stage`/`phase` track the ring; returns false on abort.
+  auto issue_phase = [&](int it, int ph, int r, uint32_t& stage, uint32_t& phase) -> bool {
+    const int s = ph < S - 1 ? ph : S - 1;
+    const int width = stage_width(s);
+    const int kpan = stage_kpan(s);
+    const int ppst = panels_per_stage(s);
+    const bool ring = (s == 0) || !RES;
+    const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(p.region_col[r]);
+    const uint32_t idesc = make_idesc(FMT, static_cast<uint32_t>(width), 128u, !W_KMAJOR);
+    const uint32_t wres = (s == 0) ? p.off_wres0 : p.off_wres1;
+    // the operand of a later stage: which region holds the intermediate
+    const uint32_t a_tmem =
+        tmem_base + static_cast<uint32_t>(p.region_col[(lookahead && s >= 1) ? (it & 1) : 0]);
+    int kin = 0;
+    for (int kb = 0; kb < kpan; ++kb) {
+      const uint32_t sbase = base + p.off_ring + stage * p.stage_bytes;
+      if (ring && kin == 0) {
+        if (!bw.wait(bar(kBarFull + stage), phase)) return false;
+        tc_fence_after();
+      }
+      const uint32_t sa = sbase + static_cast<uint32_t>(kin) * kPanelBytes;
+      const uint32_t b_base =
+          RES ? base + wres + static_cast<uint32_t>(kb) * 128u * width : sbase + kPanelBytes;
+#pragma unroll
+      for (int kk = 0; kk < CK / KSTEP; ++kk) {
+        const uint64_t bdesc = W_KMAJOR ? desc_sw128(b_base + kk * 32u, 16u, 1024u)
+                                        : desc_sw128(b_base + kk * KSTEP * 128u, WBOX_BYTES, 1024u);
+        const uint32_t acc = (kb | kk) != 0 ? 1u : 0u;
+        if (s == 0) {
+          mma_ss<TF32>(d_tmem, desc_sw128(sa + kk * 32u, 16u, 1024u), bdesc, idesc, acc);
+        } else if constexpr (P_TMEM) {
+          mma_ts<TF32>(d_tmem, a_tmem + static_cast<uint32_t>(kb * CK + kk * KSTEP), bdesc, idesc, acc);
+        } else {
+          mma_ss<TF32>(d_tmem, desc_sw128(base + p.off_p + kb * kPanelBytes + kk * 32u, 16u, 1024u),
+                       bdesc, idesc, acc);
+        }
+      }
+      if (ring && ++kin == ppst) {
+        kin = 0;
+        tc_commit(bar(kBarEmpty + stage));
+        if (++stage == static_cast<uint32_t>(p.nst)) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+    }
+    return true;
   };
 
   if (warp == 0) {
@@ -356,10 +449,9 @@ __global__ void __launch_bounds__(kChainThreads, 1)
       uint32_t stage = 0, phase = 0, wl = 0;
       uint64_t issued = 0;
       int cur_b = -1;
-      for_each_phase([&](int it, int ph) -> bool {
-        const int tile = t_begin + it * t_step;
-        const int b = tile / p.m_tiles;
-        const int m0 = (tile % p.m_tiles) * 128;
+      for_each_phase([&](int it, int ph, const TileCursor& c) -> bool {
+        const int b = c.b;
+        const int m0 = c.mt * 128;
         if constexpr (RES) {
           if (ph == 0 && b != cur_b) {
             if (wl > 0 && !bw.wait(bar(kBarWEmpty), (wl - 1) & 1u)) return false;
@@ -393,22 +485,26 @@ __global__ void __launch_bounds__(kChainThreads, 1)
         const int width = stage_width(s);
         const int n0 = ph < S - 1 ? 0 : (ph - (S - 1)) * NF;
         const int kpan = stage_kpan(s);
+        const int ppst = panels_per_stage(s);
         const CUtensorMap* wm = s == 0 ? &tmW0 : (s == 1 ? &tmW1 : &tmW2);
-        for (int kb = 0; kb < kpan; ++kb) {
+        for (int kb0 = 0; kb0 < kpan; kb0 += ppst) {
           if (!bw.wait(bar(kBarEmpty + stage), phase ^ 1u)) return false;
           const uint32_t dst = base + p.off_ring + stage * p.stage_bytes;
-          const uint32_t bytes =
-              (s == 0 ? kPanelBytes : 0u) + (RES ? 0u : 128u * static_cast<uint32_t>(width));
+          const uint32_t bytes = (s == 0 ? kPanelBytes * static_cast<uint32_t>(ppst) : 0u) +
+                                 (RES ? 0u : 128u * static_cast<uint32_t>(width));
           mbar_arrive_expect_tx(bar(kBarFull + stage), bytes);
-          if (s == 0) tma_load_3d(dst, &tmA, bar(kBarFull + stage), kb * CK, m0, b);
-          if constexpr (!RES) {
-            if constexpr (W_KMAJOR) {
-              // one box: `width` rows of the transposed weight, 128 bytes of K
-              tma_load_3d(dst + kPanelBytes, wm, bar(kBarFull + stage), kb * CK, n0, b);
-            } else {
-              for (int j = 0; j < width / WBOX_N; ++j)
-                tma_load_3d(dst + kPanelBytes + j * WBOX_BYTES, wm, bar(kBarFull + stage),
-                            n0 + j * WBOX_N, kb * CK, b);
+          for (int q = 0; q < ppst; ++q) {
+            const int kb = kb0 + q;
+            if (s == 0) tma_load_3d(dst + q * kPanelBytes, &tmA, bar(kBarFull + stage), kb * CK, m0, b);
+            if constexpr (!RES) {
+              if constexpr (W_KMAJOR) {
+                // one box: `width` rows of the transposed weight, 128 bytes of K
+                tma_load_3d(dst + kPanelBytes, wm, bar(kBarFull + stage), kb * CK, n0, b);
+              } else {
+                for (int j = 0; j < width / WBOX_N; ++j)
+                  tma_load_3d(dst + kPanelBytes + j * WBOX_BYTES, wm, bar(kBarFull + stage),
+                              n0 + j * WBOX_N, kb * CK, b);
+              }
             }
           }
           ++issued;
@@ -429,34 +525,28 @@ __global__ void __launch_bounds__(kChainThreads, 1)
       }
       if (RES && wl > 0) drain_wait(bar(kBarWFull), (wl - 1) & 1u, p.budget_ns);
     }
-  } else if (warp == 1) {
-    // ----------------------------------------------------------------- MMA
+  } else if (warp == 1 && !SPLIT) {
+    // ---------------------------------------------- MMA (single issuer)
     if (lane == 0) {
       uint32_t stage = 0, phase = 0, pf = 0, wl = 0;
       int cur_b = -1;
-      for_each_phase([&](int it, int ph) -> bool {
-        const int tile = t_begin + it * t_step;
-        const int b = tile / p.m_tiles;
+      for_each_phase([&](int it, int ph, const TileCursor& c) -> bool {
         if (ph == 0) {
           if constexpr (RES) {
-            if (b != cur_b) {
+            if (c.b != cur_b) {
               if (!bw.wait(bar(kBarWFull), wl & 1u)) return false;
               ++wl;
-              cur_b = b;
+              cur_b = c.b;
               tc_fence_after();
             }
           }
           if constexpr (P_TMEM) {
-            // The intermediate that last lived in this GEMM1 region (tile
-            // it-1, or it-2 with two alternating regions) must be fully read
-            // by GEMM2 before GEMM1 of this tile overwrites it.
-            const int prev = it - (lookahead ? 2 : 1);
-            if (prev >= 0 && !bw.wait(bar(kBarPEmpty), static_cast<uint32_t>(prev) & 1u)) return false;
+            // The intermediate of the previous tile (in region X) must be fully
+            // read by GEMM2 before GEMM1 of this tile overwrites X.
+            if (it > 0 && !bw.wait(bar(kBarPEmpty), static_cast<uint32_t>(it - 1) & 1u)) return false;
           }
         }
         const int s = ph < S - 1 ? ph : S - 1;
-        const int width = stage_width(s);
-        const int kpan = stage_kpan(s);
         // The first phase that reads an intermediate waits for its operand
         // (the later passes of the last GEMM read the same operand).
         if (s >= 1 && ph == s) {
@@ -469,61 +559,80 @@ __global__ void __launch_bounds__(kChainThreads, 1)
         region_use(p, S, it, ph, r, u);
         if (!bw.wait(bar(kBarREmpty + r), (u & 1u) ^ 1u)) return false;
         tc_fence_after();
-        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(p.region_col[r]);
-        const uint32_t idesc = make_idesc(FMT, static_cast<uint32_t>(width), 128u, !W_KMAJOR);
-        const uint32_t wres = (s == 0) ? p.off_wres0 : p.off_wres1;
-        // the operand of a later stage: which region holds the intermediate
-        const uint32_t a_tmem =
-            tmem_base + static_cast<uint32_t>(p.region_col[(lookahead && s >= 1) ? (it & 1) : 0]);
-        for (int kb = 0; kb < kpan; ++kb) {
-          const bool ring = (s == 0) || !RES;
-          const uint32_t sa = base + p.off_ring + stage * p.stage_bytes;
-          if (ring) {
-            if (!bw.wait(bar(kBarFull + stage), phase)) return false;
-            tc_fence_after();
-          }
-          const uint32_t b_base =
-              RES ? base + wres + static_cast<uint32_t>(kb) * 128u * width : sa + kPanelBytes;
-#pragma unroll
-          for (int kk = 0; kk < CK / KSTEP; ++kk) {
-            const uint64_t bdesc =
-                W_KMAJOR ? desc_sw128(b_base + kk * 32u, 16u, 1024u)
-                         : desc_sw128(b_base + kk * KSTEP * 128u, WBOX_BYTES, 1024u);
-            const uint32_t acc = (kb | kk) != 0 ? 1u : 0u;
-            if (s == 0) {
-              mma_ss<TF32>(d_tmem, desc_sw128(sa + kk * 32u, 16u, 1024u), bdesc, idesc, acc);
-            } else if constexpr (P_TMEM) {
-              mma_ts<TF32>(d_tmem, a_tmem + static_cast<uint32_t>(kb * CK + kk * KSTEP), bdesc, idesc,
-                           acc);
-            } else {
-              mma_ss<TF32>(d_tmem,
-                           desc_sw128(base + p.off_p + kb * kPanelBytes + kk * 32u, 16u, 1024u),
-                           bdesc, idesc, acc);
-            }
-          }
-          if (ring) {
-            tc_commit(bar(kBarEmpty + stage));
-            if (++stage == static_cast<uint32_t>(p.nst)) {
-              stage = 0;
-              phase ^= 1u;
-            }
-          }
-        }
+        if (!issue_phase(it, ph, r, stage, phase)) return false;
         tc_commit(bar(ph < S - 1 ? kBarCFull + r : kBarRFull + r));
-        if (S >= 2 && ph == nph - 1) {
-          tc_commit(bar(kBarPEmpty));
-          // release the resident weights at the end of a batch segment
-          if (RES && it + 1 < t_count && batch_of(it + 1) != b) tc_commit(bar(kBarWEmpty));
+        if (S >= 2 && ph == nph - 1) tc_commit(bar(kBarPEmpty));
+        if (RES && ph == nph - 1 && it + 1 < t_count) {
+          TileCursor n = c;
+          n.next();
+          if (n.b != c.b) tc_commit(bar(kBarWEmpty));  // end of a batch segment
         }
-        if (S == 1 && RES && ph == nph - 1 && it + 1 < t_count && batch_of(it + 1) != b)
-          tc_commit(bar(kBarWEmpty));
         return true;
       });
       // Every MMA issued so far must be complete before tensor memory is freed.
       tc_commit(bar(kBarDrain));
       drain_wait(bar(kBarDrain), 0, p.budget_ns);
     }
-  } else if (warp < 6) {
+  } else if (SPLIT && (warp == 1 || warp == 10)) {
+    // ------------------------------- MMA, GEMM1 issuer (warp 1) and GEMM2 issuer (warp 10)
+    if (lane == 0) {
+      const bool g1 = (warp == 1);
+      uint32_t stage = 0, phase = 0, pf = 0, wl = 0;
+      int cur_b = -1;
+      TileCursor c = first;
+      bool ok = true;
+      for (int it = 0; it < t_count && ok; ++it, c.next()) {
+        if (c.b != cur_b) {  // new resident weights
+          if (!bw.wait(bar(kBarWFull), wl & 1u)) break;
+          ++wl;
+          cur_b = c.b;
+          tc_fence_after();
+        }
+        if (g1) {
+          const int r = lookahead ? (it & 1) : 0;
+          const uint32_t u = lookahead ? static_cast<uint32_t>(it) >> 1 : static_cast<uint32_t>(it);
+          if (!bw.wait(bar(kBarREmpty + r), (u & 1u) ^ 1u)) break;
+          tc_fence_after();
+          if (!issue_phase(it, 0, r, stage, phase)) break;
+          tc_commit(bar(kBarCFull + r));
+        } else {
+          for (int pass = 0; pass < p.npass && ok; ++pass) {
+            if (pass == 0) {
+              if (!bw.wait(bar(kBarPFull), pf & 1u)) {
+                ok = false;
+                break;
+              }
+              ++pf;
+              tc_fence_after();
+            }
+            int r;
+            uint32_t u;
+            zregion(it, pass, r, u);
+            if (!bw.wait(bar(kBarREmpty + r), (u & 1u) ^ 1u)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            if (!issue_phase(it, 1 + pass, r, stage, phase)) {
+              ok = false;
+              break;
+            }
+            tc_commit(bar(kBarRFull + r));
+          }
+          if (!ok) break;
+          tc_commit(bar(kBarPEmpty));
+        }
+        if (it + 1 < t_count) {
+          TileCursor n = c;
+          n.next();
+          if (n.b != c.b) tc_commit(bar(kBarWEmpty));  // this issuer is done with the batch
+        }
+      }
+      const int db = g1 ? kBarDrain : kBarDrain2;
+      tc_commit(bar(db));
+      drain_wait(bar(db), 0, p.budget_ns);
+    }
+  } else if (warp >= 2 && warp < 6) {
     // ---------------------------------------------------------- converters
     if constexpr (S >= 2) {
       const int q = warp & 3;
@@ -535,7 +644,9 @@ __global__ void __launch_bounds__(kChainThreads, 1)
           int r;
           uint32_t u;
           region_use(p, S, it, s, r, u);
-          if (!P_TMEM && s == 0 && !warp_wait(bw, bar(kBarPEmpty), (static_cast<uint32_t>(it) & 1u) ^ 1u)) {
+          // the previous tile's intermediate must be consumed before this
+          // tile's is written (and the converters never run two tiles ahead)
+          if (s == 0 && !warp_wait(bw, bar(kBarPEmpty), (static_cast<uint32_t>(it) & 1u) ^ 1u)) {
             ok = false;
             break;
           }
@@ -556,7 +667,7 @@ __global__ void __launch_bounds__(kChainThreads, 1)
         }
       }
     }
-  } else {
+  } else if (warp >= 6 && warp < 10) {
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;
     const int row = q * 32 + lane;
@@ -565,10 +676,10 @@ __global__ void __launch_bounds__(kChainThreads, 1)
     constexpr int NBOX = NF / OBOX_N;
     uint32_t nbox = 0, gs = 0;
     bool ok = true;
-    for (int it = 0; it < t_count && ok; ++it) {
-      const int tile = t_begin + it * t_step;
-      const int b = tile / p.m_tiles;
-      const int m0 = (tile % p.m_tiles) * 128;
+    TileCursor c = first;
+    for (int it = 0; it < t_count && ok; ++it, c.next()) {
+      const int b = c.b;
+      const int m0 = c.mt * 128;
       for (int pass = 0; pass < p.npass && ok; ++pass) {
         int r;
         uint32_t u;
@@ -600,11 +711,11 @@ __global__ void __launch_bounds__(kChainThreads, 1)
             break;
           }
 #pragma unroll
-          for (int c = 0; c < OBOX_N; c += 32) {
+          for (int cc = 0; cc < OBOX_N; cc += 32) {
             uint32_t v[32];
-            tmem_ld32(tsrc + static_cast<uint32_t>(j * OBOX_N + c), v);
+            tmem_ld32(tsrc + static_cast<uint32_t>(j * OBOX_N + cc), v);
             tmem_wait_ld();
-            store_output_row<OUT>(stg, row, c, v);
+            store_output_row<OUT>(stg, row, cc, v);
           }
           if (j == NBOX - 1) {
             tc_fence_before();

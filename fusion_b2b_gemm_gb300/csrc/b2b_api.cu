@@ -156,6 +156,17 @@ struct b2b_plan_s {
   // tf32 only: the weights transposed to [N][K] before every run
   void* d_wt;
   size_t wt_bytes;
+  // Encoded tensor maps of recent runs, keyed by the pointer set (encoding
+  // costs host time on every call otherwise).  Guarded by `mu`.
+  struct MapSet {
+    const void* key[5];
+    alignas(64) CUtensorMap maps[5];
+    uint64_t stamp;
+  };
+  std::mutex mu;
+  MapSet cache[8];
+  int cache_n;
+  uint64_t clock;
 };
 
 namespace {
@@ -222,38 +233,54 @@ b2b_status_t setup_chain_tc(b2b_plan_s* p) {
   if (c.tmem_cols > 512) return B2B_ERR_UNSUPPORTED;
 
   const bool p_smem = (S >= 2) && p->in_kind != kInTF32;
-  const uint32_t p_bytes =
+  uint32_t p_bytes =
       p_smem ? static_cast<uint32_t>(std::max(p->n1p, S >= 3 ? p->n2p : 0)) * 128u * p->esz : 0u;
   const int maxw = std::max({S >= 2 ? p->n1p : 0, S >= 3 ? p->n2p : 0, nf});
 
-  // Two layouts: weights resident for the whole batch, or streamed per tile.
-  struct Layout { bool res; uint32_t stage, wres0, wres1; int nst, nstg; };
-  auto fit = [&](bool res) -> Layout {
-    Layout L{res, 0, 0, 0, 0, 0};
+  // Layouts in order of preference: weights resident for the whole batch
+  // with two operand images for the intermediate, resident with one image,
+  // or weights streamed per tile.
+  struct Layout { bool res, dbl; uint32_t stage, wres0, wres1; int nst, nstg; };
+  auto fit = [&](bool res, bool dbl) -> Layout {
+    Layout L{res, dbl, 0, 0, 0, 0, 0};
     // resident weights: a ring stage holds a whole A tile (all K panels)
     L.stage = res ? static_cast<uint32_t>(c.kpan0) * kPanelBytes : kPanelBytes + 128u * maxw;
     if (res) {
       L.wres0 = static_cast<uint32_t>(c.kpan0) * 128u * p->n1p;
       L.wres1 = static_cast<uint32_t>(p->n1p / CK) * 128u * nf;
     }
-    const int64_t fixed = int64_t(L.wres0) + L.wres1 + p_bytes + kBarBytes;
+    const int64_t fixed = int64_t(L.wres0) + L.wres1 + int64_t(p_bytes) * (dbl ? 2 : 1) + kBarBytes;
     for (int nstg = 2; nstg >= 1; --nstg) {
       const int64_t room = kSmemBudget - fixed - int64_t(nstg) * kPanelBytes;
       const int nst = room > 0 ? static_cast<int>(std::min<int64_t>(8, room / L.stage)) : 0;
       L.nst = nst;
       L.nstg = nstg;
-      if (nst >= 3) break;
+      if (nst >= 3 || (dbl && nst >= 2)) break;
     }
     return L;
   };
-  Layout L = fit(false);
-  if (S == 2 && c.npass == 1 && c.kpan0 <= 4 &&
-      find_chain_kernel(p->in_kind, p->out_kind, S, p->n1p, p->n2p, nf, true)) {
-    Layout R = fit(true);
-    if (R.nst >= 3) L = R;
+  Layout L = fit(false, false);
+  const bool res_ok = S == 2 && c.npass == 1 && c.kpan0 <= 4 &&
+                      find_chain_kernel(p->in_kind, p->out_kind, S, p->n1p, p->n2p, nf, true);
+  bool p_tmem16 = false;
+  if (res_ok) {
+    // 16-bit, resident weights, lookahead: keep the intermediate in tensor
+    // memory (packed in place in its GEMM1 region, one region per tile
+    // parity), which frees shared memory for a deeper ring.
+    if (p_smem && lookahead) {
+      p_bytes = 0;
+      p_tmem16 = true;
+      L = fit(true, true);
+    } else {
+      const Layout R = fit(true, false);
+      if (R.nst >= 3) L = R;
+    }
   }
   if (L.nst < 2) return B2B_ERR_UNSUPPORTED;
   p->res = L.res;
+  c.dbl_p = L.dbl ? 1 : 0;
+  c.p_tmem = p_tmem16 ? 1 : 0;
+  c.p_bytes = p_bytes;
   c.nst = L.nst;
   c.nstg = L.nstg;
   c.stage_bytes = L.stage;
@@ -261,7 +288,7 @@ b2b_status_t setup_chain_tc(b2b_plan_s* p) {
   c.off_wres0 = static_cast<uint32_t>(L.nst) * L.stage;
   c.off_wres1 = c.off_wres0 + L.wres0;
   c.off_p = c.off_wres1 + L.wres1;
-  c.off_stg = c.off_p + p_bytes;
+  c.off_stg = c.off_p + p_bytes * (L.dbl ? 2u : 1u);
   c.off_bar = c.off_stg + static_cast<uint32_t>(L.nstg) * kPanelBytes;
   p->smem_bytes = static_cast<int>(c.off_bar + kBarBytes + 1024);
   if (p->smem_bytes > kSmemOptin) return B2B_ERR_UNSUPPORTED;
@@ -462,8 +489,8 @@ bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
   return a0 < b0 + nb && b0 < a0 + na;
 }
 
-b2b_status_t run_chain_tc(b2b_plan_s* p, const void* const* W, const void* A, void* D,
-                          cudaStream_t stream) {
+b2b_status_t encode_chain_maps(b2b_plan_s* p, const void* const* W, const void* A, void* D,
+                               CUtensorMap* maps) {
   const int S = p->stages;
   const CUtensorMapDataType in_dt = p->in_kind == kInF16    ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
                                     : p->in_kind == kInBF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
@@ -472,9 +499,34 @@ b2b_status_t run_chain_tc(b2b_plan_s* p, const void* const* W, const void* A, vo
                                      : p->out_kind == kOutBF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
                                                                : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
   const uint32_t CK = 128 / p->esz;
-  alignas(64) CUtensorMap maps[5];
-  std::memset(maps, 0, sizeof(maps));
+  std::memset(maps, 0, 5 * sizeof(CUtensorMap));
   b2b_status_t st = encode_3d(&maps[0], in_dt, p->esz, A, p->K, p->M, p->batch, CK, 128);
+  int64_t kin = p->K;
+  if (p->in_kind == kInTF32) {
+    // the weights as transposed into the workspace ([N][K] per batch)
+    const uint32_t* dst = static_cast<const uint32_t*>(p->d_wt);
+    for (int s = 0; s < S && st == B2B_OK; ++s) {
+      const uint32_t rows = s < S - 1 ? static_cast<uint32_t>(s == 0 ? p->n1p : p->n2p)
+                                      : static_cast<uint32_t>(p->nf);
+      st = encode_3d(&maps[1 + s], in_dt, p->esz, dst, kin, p->N[s], p->batch, CK, rows);
+      dst += p->batch * kin * p->N[s];
+      kin = p->N[s];
+    }
+  } else {
+    for (int s = 0; s < S && st == B2B_OK; ++s) {
+      st = encode_3d(&maps[1 + s], in_dt, p->esz, W[s], p->N[s], kin, p->batch, CK, CK);
+      kin = p->N[s];
+    }
+  }
+  for (int s = S; s < 3; ++s) maps[1 + s] = maps[1];
+  if (st == B2B_OK)
+    st = encode_3d(&maps[4], out_dt, p->osz, D, p->N[S - 1], p->M, p->batch, 128 / p->osz, 128);
+  return st;
+}
+
+b2b_status_t run_chain_tc(b2b_plan_s* p, const void* const* W, const void* A, void* D,
+                          cudaStream_t stream) {
+  const int S = p->stages;
   if (p->in_kind == kInTF32) {
     // The tf32 MMA reads B K-major: transpose every weight to [N][K] first.
     TransposeJob job;
@@ -497,24 +549,28 @@ b2b_status_t run_chain_tc(b2b_plan_s* p, const void* const* W, const void* A, vo
     const dim3 grid((max_c + 31) / 32, (max_r + 31) / 32, static_cast<unsigned>(S * p->batch));
     transpose32_kernel<<<grid, 256, 0, stream>>>(job);
     if (cudaGetLastError() != cudaSuccess) return B2B_ERR_CUDA;
-    kin = p->K;
-    for (int s = 0; s < S && st == B2B_OK; ++s) {
-      const uint32_t rows = s < S - 1 ? static_cast<uint32_t>(s == 0 ? p->n1p : p->n2p)
-                                      : static_cast<uint32_t>(p->nf);
-      st = encode_3d(&maps[1 + s], in_dt, p->esz, job.out[s], kin, p->N[s], p->batch, CK, rows);
-      kin = p->N[s];
-    }
-  } else {
-    int64_t kin = p->K;
-    for (int s = 0; s < S && st == B2B_OK; ++s) {
-      st = encode_3d(&maps[1 + s], in_dt, p->esz, W[s], p->N[s], kin, p->batch, CK, CK);
-      kin = p->N[s];
-    }
   }
-  for (int s = S; s < 3; ++s) maps[1 + s] = maps[1];
-  if (st == B2B_OK)
-    st = encode_3d(&maps[4], out_dt, p->osz, D, p->N[S - 1], p->M, p->batch, 128 / p->osz, 128);
-  if (st != B2B_OK) return st;
+  alignas(64) CUtensorMap maps[5];
+  {
+    const void* key[5] = {A, W[0], S >= 2 ? W[1] : nullptr, S >= 3 ? W[2] : nullptr, D};
+    std::lock_guard<std::mutex> lock(p->mu);
+    ++p->clock;
+    int hit = -1, victim = 0;
+    for (int i = 0; i < p->cache_n; ++i) {
+      if (std::memcmp(p->cache[i].key, key, sizeof(key)) == 0) hit = i;
+      if (p->cache[i].stamp < p->cache[victim].stamp) victim = i;
+    }
+    if (hit < 0) {
+      alignas(64) CUtensorMap fresh[5];
+      const b2b_status_t st = encode_chain_maps(p, W, A, D, fresh);
+      if (st != B2B_OK) return st;
+      hit = p->cache_n < 8 ? p->cache_n++ : victim;
+      std::memcpy(p->cache[hit].key, key, sizeof(key));
+      std::memcpy(p->cache[hit].maps, fresh, sizeof(fresh));
+    }
+    p->cache[hit].stamp = p->clock;
+    std::memcpy(maps, p->cache[hit].maps, sizeof(maps));
+  }
 
   ChainParams prm = p->prm;
   prm.status = p->d_status;

@@ -60,7 +60,9 @@ enum : int {
   kBarDrain = 29,
   kBarCFull = 30,   // [2] region X / Y holds an intermediate for the converters
   kBarDrain2 = 32,
-  kSlotTmem = 33,   // uint32 TMEM base address, then the int abort flag
+  kBarPFull1 = 33,  // second operand image (double-buffered intermediate)
+  kBarPEmpty1 = 34,
+  kSlotTmem = 35,   // uint32 TMEM base address, then the int abort flag
 };
 // Each consumer warpgroup has its own "full" barrier per region, so that it
 // sees every completion of that barrier in order: when the last GEMM reuses
@@ -79,6 +81,9 @@ struct ChainParams {
   int region_col[4];  // X, Y, Z0, Z1 (TMEM column offsets)
   int nz;             // Z buffers for the final accumulator; 0 = reuse X/Y in turn
   int lookahead;      // two-stage only: GEMM1 double-buffered (X, Y) and issued a tile ahead
+  int dbl_p;          // two operand buffers for the intermediate (tile parity), own barriers
+  uint32_t p_bytes;   // bytes of one shared-memory operand image (0: kept in tensor memory)
+  int p_tmem;         // 16-bit intermediate kept in tensor memory (tf32 always is)
   int* status;
   unsigned long long budget_ns;
 };
@@ -179,17 +184,24 @@ template <int IN>
 __device__ __forceinline__ void rearrange_accumulator(uint32_t tsrc, int width, int row,
                                                       uint32_t p_img) {
   using namespace ptx;
+  // two 32-column loads in flight per wait (widths are multiples of 64)
 #pragma unroll 1
-  for (int c0 = 0; c0 < width; c0 += 32) {
-    uint32_t v[32];
-    tmem_ld32(tsrc + static_cast<uint32_t>(c0), v);
+  for (int c0 = 0; c0 < width; c0 += 64) {
+    uint32_t v0[32], v1[32];
+    tmem_ld32(tsrc + static_cast<uint32_t>(c0), v0);
+    tmem_ld32(tsrc + static_cast<uint32_t>(c0 + 32), v1);
     tmem_wait_ld();
     if constexpr (IN == kInTF32) {
 #pragma unroll
-      for (int i = 0; i < 32; ++i) v[i] = to_tf32_rna(v[i]);
-      tmem_st32(tsrc + static_cast<uint32_t>(c0), v);
+      for (int i = 0; i < 32; ++i) {
+        v0[i] = to_tf32_rna(v0[i]);
+        v1[i] = to_tf32_rna(v1[i]);
+      }
+      tmem_st32(tsrc + static_cast<uint32_t>(c0), v0);
+      tmem_st32(tsrc + static_cast<uint32_t>(c0 + 32), v1);
     } else {
-      store_operand_row<IN>(p_img, row, c0, v);
+      store_operand_row<IN>(p_img, row, c0, v0);
+      store_operand_row<IN>(p_img, row, c0 + 32, v1);
     }
   }
   if constexpr (IN == kInTF32) {
@@ -197,6 +209,32 @@ __device__ __forceinline__ void rearrange_accumulator(uint32_t tsrc, int width, 
   } else {
     fence_proxy_async_smem();
   }
+}
+
+// 16-bit intermediate kept in tensor memory as the A operand of the next
+// GEMM: the accumulator row is rounded and packed in place, two K elements
+// per 32-bit column (even K in the low half), so K columns of fp32 become
+// K/2 columns of the operand starting at the region's first column.  Chunk
+// c0 is read before its packed form is written to columns [c0/2, c0/2+32),
+// which never reach an unread chunk.
+template <int IN>
+__device__ __forceinline__ void rearrange_accumulator_tmem16(uint32_t tsrc, int width) {
+  using namespace ptx;
+#pragma unroll 1
+  for (int c0 = 0; c0 < width; c0 += 64) {
+    uint32_t v0[32], v1[32], w[32];
+    tmem_ld32(tsrc + static_cast<uint32_t>(c0), v0);
+    tmem_ld32(tsrc + static_cast<uint32_t>(c0 + 32), v1);
+    tmem_wait_ld();
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      w[i] = (IN == kInF16) ? pack_f16x2(v0[2 * i], v0[2 * i + 1]) : pack_bf16x2(v0[2 * i], v0[2 * i + 1]);
+      w[16 + i] =
+          (IN == kInF16) ? pack_f16x2(v1[2 * i], v1[2 * i + 1]) : pack_bf16x2(v1[2 * i], v1[2 * i + 1]);
+    }
+    tmem_st32(tsrc + static_cast<uint32_t>(c0 / 2), w);
+  }
+  tmem_wait_st();
 }
 
 // Warp-uniform bounded wait: the warp goes on only if every lane saw the phase.
@@ -308,6 +346,8 @@ __global__ void __launch_bounds__(kChainThreads, 1)
     mbar_init(bar(kBarCFull + 1), 1);
     mbar_init(bar(kBarPFull), 128);
     mbar_init(bar(kBarPEmpty), 1);
+    mbar_init(bar(kBarPFull1), 128);
+    mbar_init(bar(kBarPEmpty1), 1);
     mbar_init(bar(kBarEpiSync), 128);
     mbar_init(bar(kBarDrain), 1);
     mbar_init(bar(kBarDrain2), 1);
@@ -402,6 +442,8 @@ __global__ void __launch_bounds__(kChainThreads, 1)
     // the operand of a later stage: which region holds the intermediate
     const uint32_t a_tmem =
         tmem_base + static_cast<uint32_t>(p.region_col[(lookahead && s >= 1) ? (it & 1) : 0]);
+    const uint32_t p_img = base + p.off_p + ((p.dbl_p && (it & 1)) ? p.p_bytes : 0u);
+    const bool a_in_tmem = P_TMEM || p.p_tmem;
     int kin = 0;
     for (int kb = 0; kb < kpan; ++kb) {
       const uint32_t sbase = base + p.off_ring + stage * p.stage_bytes;
@@ -419,11 +461,13 @@ __global__ void __launch_bounds__(kChainThreads, 1)
         const uint32_t acc = (kb | kk) != 0 ? 1u : 0u;
         if (s == 0) {
           mma_ss<TF32>(d_tmem, desc_sw128(sa + kk * 32u, 16u, 1024u), bdesc, idesc, acc);
-        } else if constexpr (P_TMEM) {
-          mma_ts<TF32>(d_tmem, a_tmem + static_cast<uint32_t>(kb * CK + kk * KSTEP), bdesc, idesc, acc);
+        } else if (a_in_tmem) {
+          // 32 bits per column: one tf32 element or two 16-bit elements of K
+          mma_ts<TF32>(d_tmem, a_tmem + static_cast<uint32_t>((kb * CK + kk * KSTEP) * ESZ / 4), bdesc,
+                       idesc, acc);
         } else {
-          mma_ss<TF32>(d_tmem, desc_sw128(base + p.off_p + kb * kPanelBytes + kk * 32u, 16u, 1024u),
-                       bdesc, idesc, acc);
+          mma_ss<TF32>(d_tmem, desc_sw128(p_img + kb * kPanelBytes + kk * 32u, 16u, 1024u), bdesc,
+                       idesc, acc);
         }
       }
       if (ring && ++kin == ppst) {
@@ -592,13 +636,23 @@ __global__ void __launch_bounds__(kChainThreads, 1)
           const int r = lookahead ? (it & 1) : 0;
           const uint32_t u = lookahead ? static_cast<uint32_t>(it) >> 1 : static_cast<uint32_t>(it);
           if (!bw.wait(bar(kBarREmpty + r), (u & 1u) ^ 1u)) break;
+          if (p.p_tmem) {
+            // region r also holds the operand of GEMM2 two tiles back: wait
+            // until that GEMM2 has completed (its own barrier per region)
+            if (!bw.wait(bar(r ? kBarPEmpty1 : kBarPEmpty), (u & 1u) ^ 1u)) break;
+          }
           tc_fence_after();
           if (!issue_phase(it, 0, r, stage, phase)) break;
           tc_commit(bar(kBarCFull + r));
         } else {
           for (int pass = 0; pass < p.npass && ok; ++pass) {
             if (pass == 0) {
-              if (!bw.wait(bar(kBarPFull), pf & 1u)) {
+              // with two operand images each has its own barriers, so that
+              // every wait sees the completions of its barrier in order
+              const bool w = p.dbl_p ? bw.wait(bar((it & 1) ? kBarPFull1 : kBarPFull),
+                                               (static_cast<uint32_t>(it) >> 1) & 1u)
+                                     : bw.wait(bar(kBarPFull), pf & 1u);
+              if (!w) {
                 ok = false;
                 break;
               }
@@ -620,7 +674,7 @@ __global__ void __launch_bounds__(kChainThreads, 1)
             tc_commit(bar(kBarRFull + r));
           }
           if (!ok) break;
-          tc_commit(bar(kBarPEmpty));
+          tc_commit(bar((p.dbl_p && (it & 1)) ? kBarPEmpty1 : kBarPEmpty));
         }
         if (it + 1 < t_count) {
           TileCursor n = c;
@@ -646,9 +700,15 @@ __global__ void __launch_bounds__(kChainThreads, 1)
           region_use(p, S, it, s, r, u);
           // the previous tile's intermediate must be consumed before this
           // tile's is written (and the converters never run two tiles ahead)
-          if (s == 0 && !warp_wait(bw, bar(kBarPEmpty), (static_cast<uint32_t>(it) & 1u) ^ 1u)) {
-            ok = false;
-            break;
+          const bool odd = p.dbl_p && (it & 1);
+          if (s == 0) {
+            const bool w = p.dbl_p ? warp_wait(bw, bar(odd ? kBarPEmpty1 : kBarPEmpty),
+                                               ((static_cast<uint32_t>(it) >> 1) & 1u) ^ 1u)
+                                   : warp_wait(bw, bar(kBarPEmpty), (static_cast<uint32_t>(it) & 1u) ^ 1u);
+            if (!w) {
+              ok = false;
+              break;
+            }
           }
           // region r receives one intermediate per tile (per two tiles for
           // each of the two buffers of a lookahead chain)
@@ -660,27 +720,35 @@ __global__ void __launch_bounds__(kChainThreads, 1)
           tc_fence_after();
           const int width = (s == 0) ? N1P : N2P;
           const uint32_t tsrc = tmem_base + lane_off + static_cast<uint32_t>(p.region_col[r]);
-          rearrange_accumulator<IN>(tsrc, width, row, base + p.off_p);
+          if (!TF32 && p.p_tmem)
+            rearrange_accumulator_tmem16<IN>(tsrc, width);
+          else
+            rearrange_accumulator<IN>(tsrc, width, row, base + p.off_p + (odd ? p.p_bytes : 0u));
           tc_fence_before();
-          mbar_arrive(bar(kBarPFull));
+          mbar_arrive(bar(odd ? kBarPFull1 : kBarPFull));
           mbar_arrive(bar(kBarREmpty + r));
         }
       }
     }
   } else if (warp >= 6 && warp < 10) {
     // ------------------------------------------------------------ epilogue
+    // One named barrier (id 1, 128 threads) per output box.  The loop trip
+    // counts do not depend on data, so after an abort every warp keeps
+    // walking the same loops and reaching the same barriers while skipping
+    // the work: the barriers stay matched and nothing waits forever.
     const int q = warp & 3;
     const int row = q * 32 + lane;
     const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
     const bool elected = (warp == 6 && lane == 0);
     constexpr int NBOX = NF / OBOX_N;
-    uint32_t nbox = 0, gs = 0;
+    constexpr int LDS = OBOX_N / 32;  // 32-column TMEM loads per box (1 or 2)
+    uint32_t nbox = 0;
     bool ok = true;
     TileCursor c = first;
-    for (int it = 0; it < t_count && ok; ++it, c.next()) {
+    for (int it = 0; it < t_count; ++it, c.next()) {
       const int b = c.b;
       const int m0 = c.mt * 128;
-      for (int pass = 0; pass < p.npass && ok; ++pass) {
+      for (int pass = 0; pass < p.npass; ++pass) {
         int r;
         uint32_t u;
         region_use(p, S, it, NPH_FIXED + pass, r, u);
@@ -689,10 +757,7 @@ __global__ void __launch_bounds__(kChainThreads, 1)
             p.nz > 0 ? u
                      : static_cast<uint32_t>(it) * static_cast<uint32_t>(r == 0 ? (p.npass + 1) / 2 : p.npass / 2) +
                            static_cast<uint32_t>(pass / 2);
-        if (!warp_wait(bw, bar(kBarRFull + r), eu & 1u)) {
-          ok = false;
-          break;
-        }
+        if (ok) ok = warp_wait(bw, bar(kBarRFull + r), eu & 1u);
         tc_fence_after();
         const uint32_t tsrc = tmem_base + lane_off + static_cast<uint32_t>(p.region_col[r]);
         const int n0 = pass * NF;
@@ -700,36 +765,32 @@ __global__ void __launch_bounds__(kChainThreads, 1)
         for (int j = 0; j < NBOX; ++j) {
           const uint32_t buf = (p.nstg == 2) ? (nbox & 1u) : 0u;
           const uint32_t stg = base + p.off_stg + buf * kPanelBytes;
-          if (elected && nbox >= static_cast<uint32_t>(p.nstg)) {
+          if (ok) {
+            uint32_t v[LDS][32];
+#pragma unroll
+            for (int l = 0; l < LDS; ++l) tmem_ld32(tsrc + static_cast<uint32_t>(j * OBOX_N + l * 32), v[l]);
+            tmem_wait_ld();
+            if (j == NBOX - 1) {
+              tc_fence_before();
+              mbar_arrive(bar(kBarREmpty + r));
+            }
+#pragma unroll
+            for (int l = 0; l < LDS; ++l) store_output_row<OUT>(stg, row, l * 32, v[l]);
+            fence_proxy_async_smem();
+          }
+          // The store issued for the previous box must have read its staging
+          // buffer before anyone fills that buffer again (next box).
+          if (elected && ok) {
             if (p.nstg == 2)
-              bulk_wait_read<1>();
-            else
               bulk_wait_read<0>();
           }
-          if (!group_sync(bw, bar(kBarEpiSync), gs)) {
-            ok = false;
-            break;
-          }
-#pragma unroll
-          for (int cc = 0; cc < OBOX_N; cc += 32) {
-            uint32_t v[32];
-            tmem_ld32(tsrc + static_cast<uint32_t>(j * OBOX_N + cc), v);
-            tmem_wait_ld();
-            store_output_row<OUT>(stg, row, cc, v);
-          }
-          if (j == NBOX - 1) {
-            tc_fence_before();
-            mbar_arrive(bar(kBarREmpty + r));
-          }
-          fence_proxy_async_smem();
-          if (!group_sync(bw, bar(kBarEpiSync), gs)) {
-            ok = false;
-            break;
-          }
-          if (elected) {
+          named_bar_sync(1, 128);
+          if (elected && ok) {
             tma_store_3d(&tmOut, stg, n0 + j * OBOX_N, m0, b);
             bulk_commit();
+            if (p.nstg == 1) bulk_wait_read<0>();
           }
+          if (p.nstg == 1) named_bar_sync(1, 128);
           ++nbox;
         }
       }

@@ -42,6 +42,22 @@ def dist_env():
     return rank, world, local
 
 
+def max_over_ranks(value: float, device=None) -> float:
+    """Largest value over all ranks (the job is as slow as its slowest rank)."""
+    import torch
+    import torch.distributed as dist
+    if not dist.is_available() or not dist.is_initialized() or dist.get_world_size() == 1:
+        return value
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device if device is not None else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_tflops(world: int, flops_per_rank: int, ms_per_step: float) -> float:
+    """Throughput of the whole job: every rank runs its own replica of the workload."""
+    return world * flops_per_rank / (ms_per_step * 1e-3) / 1e12
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -302,14 +318,29 @@ def roofline_for(w: wl.Workload, kernel_ms: float, peaks: dict, traffic=None):
 PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "traffic.json")
 
 
+def kernel_source_digest() -> str:
+    import hashlib
+    root = os.path.join(ROOT, "fusion_b2b_gemm_gb300", "csrc")
+    h = hashlib.sha256()
+    for f in sorted(os.listdir(root)):
+        if f.endswith((".cu", ".cuh", ".h", ".cpp")):
+            h.update(f.encode())
+            with open(os.path.join(root, f), "rb") as fh:
+                h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
 def recorded_traffic(name: str):
-    """DRAM bytes per launch from the committed ncu summary, if current."""
+    """DRAM bytes per launch from the committed ncu summary, or None when the
+    kernel sources changed since those counters were taken."""
     try:
         with open(PROFILE_TRAFFIC) as f:
             d = json.load(f)
-        return d.get(name)
     except (OSError, ValueError):
         return None
+    if d.get("source_digest") != kernel_source_digest():
+        return None
+    return d.get(name)
 
 
 # --------------------------------------------------------------------- arms --
@@ -387,14 +418,11 @@ def run_ours(args):
     total_ms = graph_time_ms(graph, torch.cuda.current_stream())
     barrier()
     clocks = sampler.stop()
-    if world > 1:
-        t = torch.tensor([total_ms], device=device)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(total_ms, device)
 
     ms_per_step = total_ms / args.steps
     kernel_ms = ms_per_step      # one kernel launch per step, back to back in the graph
-    value = world * w.flops() / (ms_per_step * 1e-3) / 1e12
+    value = whole_job_tflops(world, w.flops(), ms_per_step)
     # eager calls (host launch path included), for reference
     per_eager, _ = event_time_ms(case.fused, min(args.steps, 50), stream)
 
@@ -413,7 +441,8 @@ def run_ours(args):
     barrier()
     e_steps = max(3, min(args.steps, 20))
     _, e_total = event_time_ms(e2e_step, e_steps, stream)
-    e2e_value = world * w.flops() / (e_total / e_steps * 1e-3) / 1e12
+    e_total = max_over_ranks(e_total, device)
+    e2e_value = whole_job_tflops(world, w.flops(), e_total / e_steps)
 
     tensor_peaks = {"f16": peaks["bf16_tflops"], "f16_f32out": peaks["bf16_tflops"], "bf16": peaks["bf16_tflops"],
                     "bf16_f32out": peaks["bf16_tflops"]}

@@ -60,6 +60,9 @@ EncodeTiledFn encode_fn() {
 
 int64_t pad64(int64_t n) { return (n + 63) / 64 * 64; }
 
+// Width of a compiled panel set that holds n columns: 64, 128 or 256.
+int64_t pad_width(int64_t n) { return n <= 64 ? 64 : (n <= 128 ? 128 : 256); }
+
 uint32_t pow2_cols(uint32_t n) {
   uint32_t c = 32;
   while (c < n) c <<= 1;
@@ -176,8 +179,8 @@ namespace {
 b2b_status_t setup_chain_tc(b2b_plan_s* p) {
   const int S = p->stages;
   const int CK = 128 / p->esz;
-  p->n1p = S >= 2 ? static_cast<int>(pad64(p->N[0])) : 64;
-  p->n2p = S >= 3 ? static_cast<int>(pad64(p->N[1])) : 64;
+  p->n1p = S >= 2 ? static_cast<int>(pad_width(p->N[0])) : 64;
+  p->n2p = S >= 3 ? static_cast<int>(pad_width(p->N[1])) : 64;
   const int64_t nlast = p->N[S - 1];
   const int nl = static_cast<int>(std::max<int64_t>(64, pad64(nlast)));
   const int base_z = (S >= 2 ? p->n1p : 0) + (S >= 3 ? p->n2p : 0);

@@ -124,6 +124,9 @@ EDGES = [
     wl.Workload("ragged_tf32", "tf32", 1, 190, 256, (200, 136), "normal", 1.0 / 16, 27),
     wl.Workload("m13_f64", "f64", 3, 13, 64, (64, 64), "uniform", 1.0, 28),
     wl.Workload("small_f64", "f64", 2, 40, 32, (32, 16), "uniform", 1.0, 29),
+    wl.Workload("n1_192_f16", "f16", 2, 200, 64, (192, 136), "normal_fanin", 1.0, 30),
+    wl.Workload("n1_160_tf32", "tf32", 2, 150, 128, (160, 200), "normal", 1.0 / 16, 31),
+    wl.Workload("n2_176_bf16_3", "bf16", 1, 140, 64, (176, 144, 200), "normal_fanin", 1.0, 32),
 ]
 
 

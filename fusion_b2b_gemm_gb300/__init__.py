@@ -19,7 +19,7 @@ __all__ = [
     "b2b_plan_create", "b2b_gemm_plan_create", "b2b_run", "b2b_plan_destroy",
     "b2b_plan_device_status", "b2b_plan_set_wait_budget", "b2b_plan_info",
     "b2b_status_string", "b2b_coordination_matrix", "b2b_probe_operand_image",
-    "b2b_probe_f64_rearrange", "coordination_matrix",
+    "b2b_probe_f64_rearrange", "b2b_run_tf32_noalloc", "coordination_matrix",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -62,6 +62,7 @@ def _load() -> ctypes.CDLL:
         "b2b_coordination_matrix": [i32, i32, ip, ip, ip, ip, ip],
         "b2b_probe_operand_image": [i32, i32, P, P, P],
         "b2b_probe_f64_rearrange": [i32, P, P, P],
+        "b2b_run_tf32_noalloc": [i64, i64, i64, i64, i64, P, P, P, P, P],
     }
     for name, args in sig.items():
         fn = getattr(lib, name)
@@ -86,6 +87,7 @@ b2b_status_string = _lib.b2b_status_string
 b2b_coordination_matrix = _lib.b2b_coordination_matrix
 b2b_probe_operand_image = _lib.b2b_probe_operand_image
 b2b_probe_f64_rearrange = _lib.b2b_probe_f64_rearrange
+b2b_run_tf32_noalloc = _lib.b2b_run_tf32_noalloc
 
 
 def _check(code: int, where: str) -> None:

@@ -769,3 +769,106 @@ b2b_status_t b2b_probe_f64_rearrange(int tiles, const double* cfrag, double* afr
 }
 
 }  // extern "C"
+
+// ----------------------------------------------------------------------------
+// tf32 chain without any allocation.
+//
+// Some callers cannot allocate device memory at all: code running where a
+// cudaMalloc would stall or fail (inside a memory-pool-managed framework that
+// forbids untracked allocations, or after the device memory has been handed
+// out up front), or callers that must not create the plan objects that own
+// device memory.  This entry point needs no plan: the scratch space of the
+// tf32 chain (its weights transposed to [N][K]) is a fixed array in device
+// memory that belongs to the library itself.
+//
+// The array is `kNoAllocScratchWords` 32-bit words (4 MiB) on every GPU that
+// loads the library, held until the process exits.  Its device address is
+// looked up once per device, on the first call made while that device is
+// current; make that first call before any stream capture.  Every call shares
+// the one array and leaves the last call's transposed weights in it; calls
+// whose kernels overlap on the GPU (different streams, no ordering) race on
+// it.  Nothing in it needs to start at zero: each call writes the part it
+// reads before reading it.  A kernel that gives up a bounded wait still
+// returns, but this entry point has no status word to report it.
+namespace {
+
+constexpr size_t kNoAllocScratchWords = size_t(1) << 20;
+__device__ __align__(256) uint32_t g_noalloc_scratch[kNoAllocScratchWords];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_noalloc_mu;
+void* g_noalloc_ptr[kMaxDevices];
+
+b2b_status_t noalloc_scratch(int dev, void** out) {
+  if (dev < 0 || dev >= kMaxDevices) return B2B_ERR_DEVICE;
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  if (!g_noalloc_ptr[dev]) {
+    void* ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || !ptr) {
+      cudaGetLastError();
+      return B2B_ERR_CUDA;
+    }
+    g_noalloc_ptr[dev] = ptr;
+  }
+  *out = g_noalloc_ptr[dev];
+  return B2B_OK;
+}
+
+}  // namespace
+
+extern "C" b2b_status_t b2b_run_tf32_noalloc(int64_t batch, int64_t M, int64_t K, int64_t N1,
+                                             int64_t N2, const void* A, const void* B,
+                                             const void* C, void* D, b2b_stream_t stream) {
+  const int64_t N[3] = {N1, N2, 0};
+  b2b_status_t st = validate_sizes(B2B_TF32, 2, batch, M, K, N);
+  if (st != B2B_OK) return st;
+  if (batch == 0 || M == 0) return B2B_OK;
+  const int64_t words = batch * (K * N1 + N1 * N2);
+  if (words > static_cast<int64_t>(kNoAllocScratchWords)) return B2B_ERR_UNSUPPORTED;
+  if (!A || !B || !C || !D) return B2B_ERR_INVALID_ARG;
+  int dev = 0, sms = 0;
+  st = check_device(&dev, &sms);
+  if (st != B2B_OK) return st;
+  void* scratch = nullptr;
+  st = noalloc_scratch(dev, &scratch);
+  if (st != B2B_OK) return st;
+
+  // A plan on the stack: tiling only, no device memory of its own.
+  b2b_plan_s pl;
+  pl.kind = kPlanChainTC;
+  pl.dtype = B2B_TF32;
+  pl.device = dev;
+  pl.sms = sms;
+  pl.stages = 2;
+  pl.batch = batch;
+  pl.M = M;
+  pl.K = K;
+  pl.N[0] = N1;
+  pl.N[1] = N2;
+  pl.N[2] = 0;
+  pl.budget_ns = kDefaultBudgetNs;
+  pl.d_status = nullptr;
+  pl.d_wt = scratch;
+  pl.wt_bytes = kNoAllocScratchWords * sizeof(uint32_t);
+  pl.cache_n = 0;
+  pl.clock = 0;
+  type_info(B2B_TF32, &pl.in_kind, &pl.out_kind, &pl.esz, &pl.osz);
+  st = setup_chain_tc(&pl);
+  if (st != B2B_OK) return st;
+  if (cudaFuncSetAttribute(pl.fn, cudaFuncAttributeMaxDynamicSharedMemorySize, pl.smem_bytes) !=
+      cudaSuccess) {
+    cudaGetLastError();
+    return B2B_ERR_CUDA;
+  }
+  const void* ins[3] = {A, B, C};
+  for (const void* q : ins)
+    if (reinterpret_cast<uintptr_t>(q) & 15u) return B2B_ERR_ALIGNMENT;
+  if (reinterpret_cast<uintptr_t>(D) & 15u) return B2B_ERR_ALIGNMENT;
+  const size_t in_bytes[3] = {static_cast<size_t>(batch * M * K) * 4, static_cast<size_t>(batch * K * N1) * 4,
+                              static_cast<size_t>(batch * N1 * N2) * 4};
+  const size_t dbytes = static_cast<size_t>(batch * M * N2) * 4;
+  for (int i = 0; i < 3; ++i)
+    if (overlaps(D, dbytes, ins[i], in_bytes[i])) return B2B_ERR_ALIAS;
+  const void* W[3] = {B, C, nullptr};
+  return run_chain_tc(&pl, W, A, D, reinterpret_cast<cudaStream_t>(stream));
+}

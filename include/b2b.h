@@ -185,6 +185,29 @@ b2b_status_t b2b_probe_operand_image(b2b_dtype_t dtype, int width, const void* a
 b2b_status_t b2b_probe_f64_rearrange(int tiles, const double* cfrag, double* afrag,
                                      b2b_stream_t stream);
 
+/*
+ * tf32 chain D = (A.B).C without any device allocation (no counterpart in the
+ * patent; it exists for callers that cannot allocate device memory: code that
+ * runs where cudaMalloc is forbidden or would fail, such as inside a framework
+ * that hands out all device memory itself, and callers that must not create
+ * plan objects, which own device memory).
+ *   Sizes, layout and arguments as for a B2B_TF32 plan with N3 = 0; A, B, C
+ *   and D are the caller's device buffers (fp32, row-major, 16-byte aligned).
+ *   The tf32 weights are transposed into a fixed scratch array owned by the
+ *   library: 4 MiB (2^20 32-bit words) on every GPU that loads the library,
+ *   kept until the process exits.  batch * (K*N1 + N1*N2) must not exceed
+ *   2^20, otherwise B2B_ERR_UNSUPPORTED.
+ *   The first call on a device looks up the array's device address (make it
+ *   before any stream capture).  All calls share the array; calls whose
+ *   kernels overlap on the GPU race on it.  Nothing in it must start at zero.
+ *   No cudaMalloc or cudaFree is made.  Asynchronous on `stream`; a bounded
+ *   wait that runs out inside the kernel is not reported (there is no status
+ *   word).
+ */
+b2b_status_t b2b_run_tf32_noalloc(int64_t batch, int64_t M, int64_t K, int64_t N1, int64_t N2,
+                                  const void* A, const void* B, const void* C, void* D,
+                                  b2b_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -283,6 +283,10 @@ b2b_status_t setup_chain_tc(b2b_plan_s* p) {
   p->res = L.res;
   c.dbl_p = L.dbl ? 1 : 0;
   c.p_tmem = p_tmem16 ? 1 : 0;
+  c.w_merged = 0;
+  if (p->in_kind != kInTF32)
+    for (int s = 0; s < S; ++s)
+      if (p->N[s] % 64 == 0) c.w_merged |= 1 << s;
   c.p_bytes = p_bytes;
   c.nst = L.nst;
   c.nstg = L.nstg;
@@ -486,6 +490,27 @@ b2b_status_t encode_3d(CUtensorMap* map, CUtensorMapDataType dt, int esz, const 
   return r == CUDA_SUCCESS ? B2B_OK : B2B_ERR_CUDA;
 }
 
+// Weight W[b][K][N] (N a multiple of 64) seen as a 4-D tensor
+// (64 columns, K rows, N/64 column blocks, batch): one box of
+// (64, k_rows, blocks, 1) covers k_rows rows of `blocks` adjacent 64-column
+// blocks, and lands in shared memory as `blocks` consecutive 128-byte-wide
+// swizzled panels.
+b2b_status_t encode_w4d(CUtensorMap* map, CUtensorMapDataType dt, int esz, const void* ptr,
+                        int64_t n, int64_t k, int64_t batch, uint32_t k_rows, uint32_t blocks) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return B2B_ERR_CUDA;
+  const cuuint64_t dims[4] = {64, static_cast<cuuint64_t>(k), static_cast<cuuint64_t>(n / 64),
+                              static_cast<cuuint64_t>(batch)};
+  const cuuint64_t strides[3] = {static_cast<cuuint64_t>(n * esz), static_cast<cuuint64_t>(64 * esz),
+                                 static_cast<cuuint64_t>(n * k * esz)};
+  const cuuint32_t box[4] = {64, k_rows, blocks, 1};
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  const CUresult r = fn(map, dt, 4, const_cast<void*>(ptr), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? B2B_OK : B2B_ERR_CUDA;
+}
+
 bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
   if (!a || !b || na == 0 || nb == 0) return false;
   const uintptr_t a0 = reinterpret_cast<uintptr_t>(a), b0 = reinterpret_cast<uintptr_t>(b);
@@ -517,7 +542,15 @@ b2b_status_t encode_chain_maps(b2b_plan_s* p, const void* const* W, const void* 
     }
   } else {
     for (int s = 0; s < S && st == B2B_OK; ++s) {
-      st = encode_3d(&maps[1 + s], in_dt, p->esz, W[s], p->N[s], kin, p->batch, CK, CK);
+      if ((p->prm.w_merged >> s) & 1) {
+        // 4-D view [batch][N/64][K][64]: a whole K panel of every 64-column
+        // block in one box, laid out in shared memory block after block
+        const int64_t width = s < S - 1 ? (s == 0 ? p->n1p : p->n2p) : p->nf;
+        st = encode_w4d(&maps[1 + s], in_dt, p->esz, W[s], p->N[s], kin, p->batch, CK,
+                        static_cast<uint32_t>(width / 64));
+      } else {
+        st = encode_3d(&maps[1 + s], in_dt, p->esz, W[s], p->N[s], kin, p->batch, CK, CK);
+      }
       kin = p->N[s];
     }
   }

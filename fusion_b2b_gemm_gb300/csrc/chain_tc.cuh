@@ -84,6 +84,8 @@ struct ChainParams {
   int dbl_p;          // two operand buffers for the intermediate (tile parity), own barriers
   uint32_t p_bytes;   // bytes of one shared-memory operand image (0: kept in tensor memory)
   int p_tmem;         // 16-bit intermediate kept in tensor memory (tf32 always is)
+  int w_merged;       // bit s: weight s is mapped 4-D (64 cols, K, col blocks, batch), so a
+                      // whole panel (all its 64-column boxes) arrives as one TMA box
   int* status;
   unsigned long long budget_ns;
 };
@@ -506,6 +508,8 @@ __global__ void __launch_bounds__(kChainThreads, 1)
               const uint32_t dst = base + p.off_wres0 + kb * 128u * N1P;
               if constexpr (W_KMAJOR) {
                 tma_load_3d(dst, &tmW0, bar(kBarWFull), kb * CK, 0, b);
+              } else if (p.w_merged & 1) {
+                tma_load_4d(dst, &tmW0, bar(kBarWFull), 0, kb * CK, 0, b);
               } else {
                 for (int j = 0; j < N1P / WBOX_N; ++j)
                   tma_load_3d(dst + j * WBOX_BYTES, &tmW0, bar(kBarWFull), j * WBOX_N, kb * CK, b);
@@ -515,6 +519,8 @@ __global__ void __launch_bounds__(kChainThreads, 1)
               const uint32_t dst = base + p.off_wres1 + kb * 128u * NF;
               if constexpr (W_KMAJOR) {
                 tma_load_3d(dst, &tmW1, bar(kBarWFull), kb * CK, 0, b);
+              } else if (p.w_merged & 2) {
+                tma_load_4d(dst, &tmW1, bar(kBarWFull), 0, kb * CK, 0, b);
               } else {
                 for (int j = 0; j < NF / WBOX_N; ++j)
                   tma_load_3d(dst + j * WBOX_BYTES, &tmW1, bar(kBarWFull), j * WBOX_N, kb * CK, b);
@@ -544,6 +550,9 @@ __global__ void __launch_bounds__(kChainThreads, 1)
               if constexpr (W_KMAJOR) {
                 // one box: `width` rows of the transposed weight, 128 bytes of K
                 tma_load_3d(dst + kPanelBytes, wm, bar(kBarFull + stage), kb * CK, n0, b);
+              } else if ((p.w_merged >> s) & 1) {
+                // one box: all 64-column blocks of this panel
+                tma_load_4d(dst + kPanelBytes, wm, bar(kBarFull + stage), 0, kb * CK, n0 / WBOX_N, b);
               } else {
                 for (int j = 0; j < width / WBOX_N; ++j)
                   tma_load_3d(dst + kPanelBytes + j * WBOX_BYTES, wm, bar(kBarFull + stage),

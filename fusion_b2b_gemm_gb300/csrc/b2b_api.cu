@@ -511,6 +511,24 @@ b2b_status_t encode_w4d(CUtensorMap* map, CUtensorMapDataType dt, int esz, const
   return r == CUDA_SUCCESS ? B2B_OK : B2B_ERR_CUDA;
 }
 
+// Launch with programmatic stream serialization: the kernel may start while
+// the previous kernel in the stream is finishing; it waits (griddepcontrol)
+// before its first global-memory access.
+cudaError_t launch_pdl(const void* fn, dim3 grid, dim3 block, void** args, size_t smem,
+                       cudaStream_t stream) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelExC(&cfg, fn, args);
+}
+
 bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
   if (!a || !b || na == 0 || nb == 0) return false;
   const uintptr_t a0 = reinterpret_cast<uintptr_t>(a), b0 = reinterpret_cast<uintptr_t>(b);
@@ -583,8 +601,12 @@ b2b_status_t run_chain_tc(b2b_plan_s* p, const void* const* W, const void* A, vo
       kin = p->N[s];
     }
     const dim3 grid((max_c + 31) / 32, (max_r + 31) / 32, static_cast<unsigned>(S * p->batch));
-    transpose32_kernel<<<grid, 256, 0, stream>>>(job);
-    if (cudaGetLastError() != cudaSuccess) return B2B_ERR_CUDA;
+    void* targs[1] = {&job};
+    if (launch_pdl(reinterpret_cast<const void*>(&transpose32_kernel), grid, dim3(256), targs, 0,
+                   stream) != cudaSuccess) {
+      cudaGetLastError();
+      return B2B_ERR_CUDA;
+    }
   }
   alignas(64) CUtensorMap maps[5];
   {
@@ -612,8 +634,8 @@ b2b_status_t run_chain_tc(b2b_plan_s* p, const void* const* W, const void* A, vo
   prm.status = p->d_status;
   prm.budget_ns = p->budget_ns;
   void* args[6] = {&maps[0], &maps[1], &maps[2], &maps[3], &maps[4], &prm};
-  const cudaError_t e = cudaLaunchKernel(p->fn, dim3(p->grid), dim3(p->threads), args,
-                                         static_cast<size_t>(p->smem_bytes), stream);
+  const cudaError_t e = launch_pdl(p->fn, dim3(p->grid), dim3(p->threads), args,
+                                   static_cast<size_t>(p->smem_bytes), stream);
   if (e != cudaSuccess) {
     cudaGetLastError();
     return B2B_ERR_CUDA;
@@ -629,8 +651,7 @@ b2b_status_t run_f64(b2b_plan_s* p, const void* A, const void* B, const void* C,
   const double* c = static_cast<const double*>(C);
   double* d = static_cast<double*>(D);
   void* args[5] = {&a, &b, &c, &d, &prm};
-  const cudaError_t e =
-      cudaLaunchKernel(p->fn, dim3(p->grid), dim3(p->threads), args, 0, stream);
+  const cudaError_t e = launch_pdl(p->fn, dim3(p->grid), dim3(p->threads), args, 0, stream);
   if (e != cudaSuccess) {
     cudaGetLastError();
     return B2B_ERR_CUDA;

@@ -66,6 +66,10 @@ __global__ void __launch_bounds__(128) chain_f64_kernel(const double* __restrict
                                                         const double* __restrict__ C,
                                                         double* __restrict__ D, const F64Params p) {
   static_assert(N1 % 8 == 0 && N2 % 8 == 0, "8-column tiles");
+  // Wait for the previous kernel in the stream (programmatic launch).  No
+  // early trigger here: this grid has many more CTAs than fit at once, and
+  // waiting CTAs of the next launch would take their slots.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int lane = threadIdx.x & 31;
   const int g = lane >> 2, t = lane & 3;
   const long long nwarps = static_cast<long long>(gridDim.x) * (blockDim.x >> 5);

@@ -364,6 +364,10 @@ __global__ void __launch_bounds__(kChainThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  // The prologue above may overlap the previous kernel in the stream; no
+  // global memory is touched before that kernel has completed.
+  grid_launch_dependents();
+  grid_dependency_wait();
 
   BoundedWait bw{abort_flag, p.status, p.budget_ns, kTimeoutCode};
 

@@ -10,6 +10,8 @@
 
 #include <cstdint>
 
+#include "ptx.cuh"
+
 namespace b2b {
 
 struct TransposeJob {
@@ -22,6 +24,8 @@ struct TransposeJob {
 
 __global__ void __launch_bounds__(256) transpose32_kernel(const __grid_constant__ TransposeJob job) {
   __shared__ uint32_t tile[32][33];
+  ptx::grid_launch_dependents();
+  ptx::grid_dependency_wait();
   const int z = blockIdx.z;
   const int mat = z / job.batch;
   const int b = z % job.batch;

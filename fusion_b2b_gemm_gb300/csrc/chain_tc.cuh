@@ -774,14 +774,18 @@ __global__ void __launch_bounds__(kChainThreads, 1)
         tc_fence_after();
         const uint32_t tsrc = tmem_base + lane_off + static_cast<uint32_t>(p.region_col[r]);
         const int n0 = pass * NF;
+        // The TMEM load of box j+1 is issued as soon as box j is in shared
+        // memory, so its latency overlaps box j's barrier and store.
+        uint32_t v[LDS][32];
+        if (ok) {
+#pragma unroll
+          for (int l = 0; l < LDS; ++l) tmem_ld32(tsrc + static_cast<uint32_t>(l * 32), v[l]);
+        }
 #pragma unroll 1
         for (int j = 0; j < NBOX; ++j) {
           const uint32_t buf = (p.nstg == 2) ? (nbox & 1u) : 0u;
           const uint32_t stg = base + p.off_stg + buf * kPanelBytes;
           if (ok) {
-            uint32_t v[LDS][32];
-#pragma unroll
-            for (int l = 0; l < LDS; ++l) tmem_ld32(tsrc + static_cast<uint32_t>(j * OBOX_N + l * 32), v[l]);
             tmem_wait_ld();
             if (j == NBOX - 1) {
               tc_fence_before();
@@ -790,6 +794,11 @@ __global__ void __launch_bounds__(kChainThreads, 1)
 #pragma unroll
             for (int l = 0; l < LDS; ++l) store_output_row<OUT>(stg, row, l * 32, v[l]);
             fence_proxy_async_smem();
+            if (j + 1 < NBOX) {
+#pragma unroll
+              for (int l = 0; l < LDS; ++l)
+                tmem_ld32(tsrc + static_cast<uint32_t>((j + 1) * OBOX_N + l * 32), v[l]);
+            }
           }
           // The store issued for the previous box must have read its staging
           // buffer before anyone fills that buffer again (next box).

@@ -17,7 +17,7 @@ from typing import Optional, Sequence, Tuple
 __all__ = [
     "B2BError", "DTYPES", "Plan", "GemmPlan", "library_path",
     "b2b_plan_create", "b2b_gemm_plan_create", "b2b_run", "b2b_plan_destroy",
-    "b2b_plan_device_status", "b2b_plan_set_wait_budget", "b2b_plan_info",
+    "b2b_plan_device_status", "b2b_plan_set_wait_budget", "b2b_plan_set_debug", "b2b_plan_info",
     "b2b_status_string", "b2b_coordination_matrix", "b2b_probe_operand_image",
     "b2b_probe_f64_rearrange", "b2b_run_tf32_noalloc", "coordination_matrix",
 ]
@@ -58,6 +58,7 @@ def _load() -> ctypes.CDLL:
         "b2b_plan_destroy": [P],
         "b2b_plan_device_status": [P, P],
         "b2b_plan_set_wait_budget": [P, u64],
+        "b2b_plan_set_debug": [P, ctypes.c_uint32],
         "b2b_plan_info": [P, ip, ip, ip, ip, ip, ip, ip],
         "b2b_coordination_matrix": [i32, i32, ip, ip, ip, ip, ip],
         "b2b_probe_operand_image": [i32, i32, P, P, P],
@@ -82,6 +83,7 @@ b2b_run = _lib.b2b_run
 b2b_plan_destroy = _lib.b2b_plan_destroy
 b2b_plan_device_status = _lib.b2b_plan_device_status
 b2b_plan_set_wait_budget = _lib.b2b_plan_set_wait_budget
+b2b_plan_set_debug = _lib.b2b_plan_set_debug
 b2b_plan_info = _lib.b2b_plan_info
 b2b_status_string = _lib.b2b_status_string
 b2b_coordination_matrix = _lib.b2b_coordination_matrix
@@ -179,6 +181,10 @@ class Plan:
 
     def set_wait_budget(self, ns: int) -> None:
         _check(_lib.b2b_plan_set_wait_budget(self._h, int(ns)), "b2b_plan_set_wait_budget")
+
+    def set_debug(self, flags: int) -> None:
+        """Test support (see b2b_plan_set_debug in include/b2b.h)."""
+        _check(_lib.b2b_plan_set_debug(self._h, int(flags)), "b2b_plan_set_debug")
 
     def info(self) -> dict:
         vals = [ctypes.c_int() for _ in range(7)]

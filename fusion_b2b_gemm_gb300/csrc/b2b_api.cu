@@ -156,6 +156,7 @@ struct b2b_plan_s {
   F64Params f64;
   int* d_status;
   uint64_t budget_ns;
+  uint32_t debug;
   // tf32 only: the weights transposed to [N][K] before every run
   void* d_wt;
   size_t wt_bytes;
@@ -633,6 +634,7 @@ b2b_status_t run_chain_tc(b2b_plan_s* p, const void* const* W, const void* A, vo
   ChainParams prm = p->prm;
   prm.status = p->d_status;
   prm.budget_ns = p->budget_ns;
+  prm.debug = p->debug;
   void* args[6] = {&maps[0], &maps[1], &maps[2], &maps[3], &maps[4], &prm};
   const cudaError_t e = launch_pdl(p->fn, dim3(p->grid), dim3(p->threads), args,
                                    static_cast<size_t>(p->smem_bytes), stream);
@@ -738,6 +740,13 @@ b2b_status_t b2b_plan_device_status(b2b_plan_t p, b2b_stream_t stream) {
 b2b_status_t b2b_plan_set_wait_budget(b2b_plan_t p, uint64_t budget_ns) {
   if (!p) return B2B_ERR_INVALID_ARG;
   p->budget_ns = budget_ns ? budget_ns : kDefaultBudgetNs;
+  return B2B_OK;
+}
+
+b2b_status_t b2b_plan_set_debug(b2b_plan_t p, uint32_t flags) {
+  if (!p) return B2B_ERR_INVALID_ARG;
+  if (flags & ~B2B_DEBUG_DROP_FIRST_LOAD) return B2B_ERR_INVALID_ARG;
+  p->debug = flags;
   return B2B_OK;
 }
 
@@ -901,6 +910,7 @@ extern "C" b2b_status_t b2b_run_tf32_noalloc(int64_t batch, int64_t M, int64_t K
   pl.N[1] = N2;
   pl.N[2] = 0;
   pl.budget_ns = kDefaultBudgetNs;
+  pl.debug = 0;
   pl.d_status = nullptr;
   pl.d_wt = scratch;
   pl.wt_bytes = kNoAllocScratchWords * sizeof(uint32_t);

@@ -86,6 +86,7 @@ struct ChainParams {
   int p_tmem;         // 16-bit intermediate kept in tensor memory (tf32 always is)
   int w_merged;       // bit s: weight s is mapped 4-D (64 cols, K, col blocks, batch), so a
                       // whole panel (all its 64-column boxes) arrives as one TMA box
+  uint32_t debug;     // test support: bit 0 = arm the first ring stage but never fill it
   int* status;
   unsigned long long budget_ns;
 };
@@ -547,7 +548,10 @@ __global__ void __launch_bounds__(kChainThreads, 1)
           const uint32_t bytes = (s == 0 ? kPanelBytes * static_cast<uint32_t>(ppst) : 0u) +
                                  (RES ? 0u : 128u * static_cast<uint32_t>(width));
           mbar_arrive_expect_tx(bar(kBarFull + stage), bytes);
-          for (int q = 0; q < ppst; ++q) {
+          // test support: the very first stage is armed but never filled, so
+          // the MMA thread's bounded wait on it must run out
+          const bool drop = (p.debug & 1u) && issued == 0;
+          for (int q = 0; q < ppst && !drop; ++q) {
             const int kb = kb0 + q;
             if (s == 0) tma_load_3d(dst + q * kPanelBytes, &tmA, bar(kBarFull + stage), kb * CK, m0, b);
             if constexpr (!RES) {

@@ -129,6 +129,20 @@ b2b_status_t b2b_plan_device_status(b2b_plan_t plan, b2b_stream_t stream);
 b2b_status_t b2b_plan_set_wait_budget(b2b_plan_t plan, uint64_t budget_ns);
 
 /*
+ * Test support for failure detection.  With B2B_DEBUG_DROP_FIRST_LOAD set,
+ * the next runs of a tensor-core plan arm the first shared-memory stage of
+ * every CTA but never copy data into it, so the MMA thread's wait on that
+ * stage runs out after the plan's wait budget; every role then leaves its
+ * loops, in-flight copies and MMAs are drained, tensor memory is freed, and
+ * b2b_plan_device_status reports B2B_ERR_TIMEOUT.  The output is not written.
+ * No fault, trap or unbounded wait is involved.  Other flag bits are
+ * rejected (B2B_ERR_INVALID_ARG); 0 restores normal runs.  fp64 plans (which
+ * have no waits) ignore the flag.
+ */
+#define B2B_DEBUG_DROP_FIRST_LOAD 1u
+b2b_status_t b2b_plan_set_debug(b2b_plan_t plan, uint32_t flags);
+
+/*
  * Describe a plan: kernel launches per b2b_run, grid size, threads per CTA,
  * dynamic shared memory per CTA, tensor-memory columns, ring depth and the
  * number of passes of the last GEMM.  Any pointer may be NULL.

@@ -461,21 +461,31 @@ __global__ void __launch_bounds__(kChainThreads, 1)
       const uint32_t sa = sbase + static_cast<uint32_t>(kin) * kPanelBytes;
       const uint32_t b_base =
           RES ? base + wres + static_cast<uint32_t>(kb) * 128u * width : sbase + kPanelBytes;
+      auto bdesc = [&](int kk) -> uint64_t {
+        return W_KMAJOR ? desc_sw128(b_base + kk * 32u, 16u, 1024u)
+                        : desc_sw128(b_base + kk * KSTEP * 128u, WBOX_BYTES, 1024u);
+      };
+      const uint32_t acc0 = kb != 0 ? 1u : 0u;
+      // The MMAs of one panel are issued back to back, with the choice of
+      // operand source made once per panel: a branch between consecutive
+      // tcgen05.mma instructions was measured to cost a third of the
+      // tensor-pipe rate (M=128, N=256: 171 instead of 128 cycles per MMA).
+      if (s == 0) {
 #pragma unroll
-      for (int kk = 0; kk < CK / KSTEP; ++kk) {
-        const uint64_t bdesc = W_KMAJOR ? desc_sw128(b_base + kk * 32u, 16u, 1024u)
-                                        : desc_sw128(b_base + kk * KSTEP * 128u, WBOX_BYTES, 1024u);
-        const uint32_t acc = (kb | kk) != 0 ? 1u : 0u;
-        if (s == 0) {
-          mma_ss<TF32>(d_tmem, desc_sw128(sa + kk * 32u, 16u, 1024u), bdesc, idesc, acc);
-        } else if (a_in_tmem) {
-          // 32 bits per column: one tf32 element or two 16-bit elements of K
-          mma_ts<TF32>(d_tmem, a_tmem + static_cast<uint32_t>((kb * CK + kk * KSTEP) * ESZ / 4), bdesc,
-                       idesc, acc);
-        } else {
-          mma_ss<TF32>(d_tmem, desc_sw128(p_img + kb * kPanelBytes + kk * 32u, 16u, 1024u), bdesc,
-                       idesc, acc);
-        }
+        for (int kk = 0; kk < CK / KSTEP; ++kk)
+          mma_ss<TF32>(d_tmem, desc_sw128(sa + kk * 32u, 16u, 1024u), bdesc(kk), idesc, kk ? 1u : acc0);
+      } else if (a_in_tmem) {
+        // 32 bits per column: one tf32 element or two 16-bit elements of K
+        const uint32_t ak = a_tmem + static_cast<uint32_t>(kb * CK * ESZ / 4);
+#pragma unroll
+        for (int kk = 0; kk < CK / KSTEP; ++kk)
+          mma_ts<TF32>(d_tmem, ak + static_cast<uint32_t>(kk * KSTEP * ESZ / 4), bdesc(kk), idesc,
+                       kk ? 1u : acc0);
+      } else {
+        const uint32_t pk = p_img + static_cast<uint32_t>(kb) * kPanelBytes;
+#pragma unroll
+        for (int kk = 0; kk < CK / KSTEP; ++kk)
+          mma_ss<TF32>(d_tmem, desc_sw128(pk + kk * 32u, 16u, 1024u), bdesc(kk), idesc, kk ? 1u : acc0);
       }
       if (ring && ++kin == ppst) {
         kin = 0;

@@ -71,13 +71,23 @@ uint32_t pow2_cols(uint32_t n) {
 
 const ChainKernelEntry* find_chain_kernel(int in, int out, int S, int n1p, int n2p, int nf,
                                           bool res) {
-  const ChainTable tables[] = {chain_table_f16(), chain_table_bf16(), chain_table_s3_f16(), chain_table_s3_bf16(), chain_table_tf32()};
+  const ChainTable tables[] = {chain_table_f16(), chain_table_bf16(), chain_table_tf32()};
   for (const ChainTable& t : tables)
     for (int i = 0; i < t.count; ++i) {
       const ChainKernelEntry& e = t.entries[i];
       if (e.in == in && e.out == out && e.S == S && e.nf == nf && e.res == res &&
           (S < 2 || e.n1p == n1p) && (S < 3 || e.n2p == n2p))
         return &e;
+    }
+  return nullptr;
+}
+
+const Chain3Entry* find_chain3_kernel(int in, int out, int n1p, int n2p, int nf) {
+  const Chain3Table tables[] = {chain3_table_f16(), chain3_table_bf16()};
+  for (const Chain3Table& t : tables)
+    for (int i = 0; i < t.count; ++i) {
+      const Chain3Entry& e = t.entries[i];
+      if (e.in == in && e.out == out && e.n1p == n1p && e.n2p == n2p && e.nf == nf) return &e;
     }
   return nullptr;
 }
@@ -151,6 +161,9 @@ struct b2b_plan_s {
   int n1p, n2p, nf;
   bool res;
   ChainParams prm;
+  // Three-stage 16-bit chains run chain3_kernel on clusters of two CTAs.
+  bool s3;
+  Chain3Params p3;
   int smem_bytes, grid, threads;
   const void* fn;
   F64Params f64;
@@ -175,15 +188,66 @@ struct b2b_plan_s {
 
 namespace {
 
+// Three-stage 16-bit chains (chain3_kernel): 256-row tiles on CTA pairs,
+// padded widths of 128 or 256, the last GEMM in passes of up to 256 columns;
+// shared memory holds the operand image of the intermediate, two staging
+// buffers, and the weight and A rings in what is left.
+b2b_status_t setup_chain3(b2b_plan_s* p) {
+  p->s3 = true;
+  p->n1p = static_cast<int>(std::max<int64_t>(128, pad_width(p->N[0])));
+  p->n2p = static_cast<int>(std::max<int64_t>(128, pad_width(p->N[1])));
+  p->nf = p->N[2] > 128 ? 256 : 128;
+  p->res = false;
+  Chain3Params& c = p->p3;
+  std::memset(&c, 0, sizeof(c));
+  c.batch = static_cast<int>(p->batch);
+  c.M = static_cast<int>(p->M);
+  c.K = static_cast<int>(p->K);
+  c.m_tiles = static_cast<int>((p->M + 255) / 256);
+  const int64_t tiles = p->batch * c.m_tiles;
+  if (tiles > (1ll << 30)) return B2B_ERR_UNSUPPORTED;
+  c.total_tiles = static_cast<int>(tiles);
+  c.npass = static_cast<int>((p->N[2] + p->nf - 1) / p->nf);
+  c.kpan0 = static_cast<int>((p->K + 63) / 64);
+  c.wstage = 64u * static_cast<uint32_t>(std::max({p->n1p, p->n2p, p->nf}));
+  const uint32_t p_bytes = 256u * static_cast<uint32_t>(std::max(p->n1p, p->n2p));
+  c.nstg = 2;  // two 4 KB buffers per epilogue warp
+  const int64_t room = kSmemBudget - kBarBytes - int64_t(p_bytes) - int64_t(c.nstg) * kPanelBytes;
+  // half of the room to each ring, at most eight stages each
+  c.nsta = static_cast<int>(std::min<int64_t>(8, room / 2 / kPanelBytes));
+  c.nst = static_cast<int>(std::min<int64_t>(8, (room - int64_t(c.nsta) * kPanelBytes) / c.wstage));
+  if (c.nst < 2 || c.nsta < 2) return B2B_ERR_UNSUPPORTED;
+  c.off_ring = 0;
+  c.off_aring = static_cast<uint32_t>(c.nst) * c.wstage;
+  c.off_p = c.off_aring + static_cast<uint32_t>(c.nsta) * kPanelBytes;
+  c.off_stg = c.off_p + p_bytes;
+  c.off_bar = c.off_stg + static_cast<uint32_t>(c.nstg) * kPanelBytes;
+  p->smem_bytes = static_cast<int>(c.off_bar + kBarBytes + 1024);
+  if (p->smem_bytes > kSmemOptin) return B2B_ERR_UNSUPPORTED;
+  // a weight whose width is a multiple of 64 is read one 4-D box per half panel
+  c.w_merged = (p->N[0] % 64 == 0 ? 1 : 0) | (p->N[1] % 64 == 0 ? 2 : 0) | (p->N[2] % 64 == 0 ? 4 : 0);
+  const Chain3Entry* e = find_chain3_kernel(p->in_kind, p->out_kind, p->n1p, p->n2p, p->nf);
+  if (!e) return B2B_ERR_UNSUPPORTED;
+  p->fn = e->fn;
+  p->threads = kChainThreads;
+  // the number of co-resident clusters is known once the kernel's shared
+  // memory size is set (pair_grid)
+  p->grid = static_cast<int>(std::min<int64_t>(2 * tiles, p->sms & ~1));
+  return B2B_OK;
+}
+
 // Tiling of a tcgen05 chain: padded widths, final-pass width, tensor-memory
 // regions, shared-memory carve-up, and whether the weights stay resident.
 b2b_status_t setup_chain_tc(b2b_plan_s* p) {
   const int S = p->stages;
+  if (S == 3 && p->in_kind != kInTF32) return setup_chain3(p);
+  p->s3 = false;
   const int CK = 128 / p->esz;
+  const int64_t wmin = 64;
   p->n1p = S >= 2 ? static_cast<int>(pad_width(p->N[0])) : 64;
   p->n2p = S >= 3 ? static_cast<int>(pad_width(p->N[1])) : 64;
   const int64_t nlast = p->N[S - 1];
-  const int nl = static_cast<int>(std::max<int64_t>(64, pad64(nlast)));
+  const int nl = static_cast<int>(std::max<int64_t>(wmin, pad64(nlast)));
   const int base_z = (S >= 2 ? p->n1p : 0) + (S >= 3 ? p->n2p : 0);
 
   int nf = 0, nz = -1, lookahead = 0;
@@ -194,17 +258,17 @@ b2b_status_t setup_chain_tc(b2b_plan_s* p) {
     const int base_la = 2 * p->n1p;
     for (int k = 2; k >= 1 && nz < 0; --k)
       for (int c : cands)
-        if (c <= nl && base_la + k * c <= 512) { nf = c; nz = k; lookahead = 1; break; }
+        if (c >= wmin && c <= nl && base_la + k * c <= 512) { nf = c; nz = k; lookahead = 1; break; }
   }
   if (nz < 0)
     for (int c : cands)
-      if (c <= nl && base_z + 2 * c <= 512) { nf = c; nz = 2; break; }
+      if (c >= wmin && c <= nl && base_z + 2 * c <= 512) { nf = c; nz = 2; break; }
   if (nz < 0)
     for (int c : cands)
-      if (c <= nl && base_z + c <= 512) { nf = c; nz = 1; break; }
+      if (c >= wmin && c <= nl && base_z + c <= 512) { nf = c; nz = 1; break; }
   if (nz < 0 && S == 3)
     for (int c : cands)
-      if (c <= nl && c <= p->n1p && c <= p->n2p) { nf = c; nz = 0; break; }
+      if (c >= wmin && c <= nl && c <= p->n1p && c <= p->n2p) { nf = c; nz = 0; break; }
   if (nz < 0) return B2B_ERR_UNSUPPORTED;
   if (nf == 0) return B2B_ERR_UNSUPPORTED;
   p->nf = nf;
@@ -243,12 +307,14 @@ b2b_status_t setup_chain_tc(b2b_plan_s* p) {
 
   // Layouts in order of preference: weights resident for the whole batch
   // with two operand images for the intermediate, resident with one image,
-  // or weights streamed per tile.
-  struct Layout { bool res, dbl; uint32_t stage, wres0, wres1; int nst, nstg; };
+  // or weights streamed per tile (a ring of weight panels and a separate
+  // ring of A panels).
+  struct Layout { bool res, dbl; uint32_t stage, wres0, wres1; int nst, nsta, nstg; };
   auto fit = [&](bool res, bool dbl) -> Layout {
-    Layout L{res, dbl, 0, 0, 0, 0, 0};
-    // resident weights: a ring stage holds a whole A tile (all K panels)
-    L.stage = res ? static_cast<uint32_t>(c.kpan0) * kPanelBytes : kPanelBytes + 128u * maxw;
+    Layout L{res, dbl, 0, 0, 0, 0, 0, 0};
+    // resident: a ring stage holds a whole A tile (all K panels); streamed:
+    // one weight panel
+    L.stage = res ? static_cast<uint32_t>(c.kpan0) * kPanelBytes : 128u * static_cast<uint32_t>(maxw);
     if (res) {
       L.wres0 = static_cast<uint32_t>(c.kpan0) * 128u * p->n1p;
       L.wres1 = static_cast<uint32_t>(p->n1p / CK) * 128u * nf;
@@ -256,10 +322,20 @@ b2b_status_t setup_chain_tc(b2b_plan_s* p) {
     const int64_t fixed = int64_t(L.wres0) + L.wres1 + int64_t(p_bytes) * (dbl ? 2 : 1) + kBarBytes;
     for (int nstg = 2; nstg >= 1; --nstg) {
       const int64_t room = kSmemBudget - fixed - int64_t(nstg) * kPanelBytes;
-      const int nst = room > 0 ? static_cast<int>(std::min<int64_t>(8, room / L.stage)) : 0;
-      L.nst = nst;
       L.nstg = nstg;
-      if (nst >= 3 || (dbl && nst >= 2)) break;
+      if (res) {
+        L.nst = room > 0 ? static_cast<int>(std::min<int64_t>(8, room / L.stage)) : 0;
+        L.nsta = 0;
+        if (L.nst >= 3 || (dbl && L.nst >= 2)) break;
+      } else {
+        // up to four weight panels in flight; the rest of the room (up to
+        // eight panels) for A
+        const int64_t wroom = room - 2 * int64_t(kPanelBytes);
+        L.nst = wroom > 0 ? static_cast<int>(std::min<int64_t>(4, wroom / L.stage)) : 0;
+        const int64_t aroom = room - int64_t(L.nst) * L.stage;
+        L.nsta = aroom > 0 ? static_cast<int>(std::min<int64_t>(8, aroom / kPanelBytes)) : 0;
+        if (L.nst >= 3 && L.nsta >= 4) break;
+      }
     }
     return L;
   };
@@ -280,7 +356,7 @@ b2b_status_t setup_chain_tc(b2b_plan_s* p) {
       if (R.nst >= 3) L = R;
     }
   }
-  if (L.nst < 2) return B2B_ERR_UNSUPPORTED;
+  if (L.nst < 2 || (!L.res && L.nsta < 2)) return B2B_ERR_UNSUPPORTED;
   p->res = L.res;
   c.dbl_p = L.dbl ? 1 : 0;
   c.p_tmem = p_tmem16 ? 1 : 0;
@@ -290,10 +366,12 @@ b2b_status_t setup_chain_tc(b2b_plan_s* p) {
       if (p->N[s] % 64 == 0) c.w_merged |= 1 << s;
   c.p_bytes = p_bytes;
   c.nst = L.nst;
+  c.nsta = L.nsta;
   c.nstg = L.nstg;
   c.stage_bytes = L.stage;
   c.off_ring = 0;
-  c.off_wres0 = static_cast<uint32_t>(L.nst) * L.stage;
+  c.off_aring = static_cast<uint32_t>(L.nst) * L.stage;
+  c.off_wres0 = c.off_aring + static_cast<uint32_t>(L.nsta) * kPanelBytes;
   c.off_wres1 = c.off_wres0 + L.wres0;
   c.off_p = c.off_wres1 + L.wres1;
   c.off_stg = c.off_p + p_bytes * (L.dbl ? 2u : 1u);
@@ -307,6 +385,30 @@ b2b_status_t setup_chain_tc(b2b_plan_s* p) {
   p->fn = e->fn;
   p->threads = kChainThreads;
   p->grid = static_cast<int>(std::min<int64_t>(c.total_tiles, p->sms));
+  return B2B_OK;
+}
+
+// A paired chain runs one persistent cluster of two CTAs per tile slot: as
+// many clusters as can be resident at once (clusters must fit within a GPC,
+// so this can be fewer than half the SMs), at most one per 256-row tile.
+b2b_status_t pair_grid(b2b_plan_s* p) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(p->grid));
+  cfg.blockDim = dim3(static_cast<unsigned>(p->threads));
+  cfg.dynamicSmemBytes = static_cast<size_t>(p->smem_bytes);
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int clusters = 0;
+  if (cudaOccupancyMaxActiveClusters(&clusters, p->fn, &cfg) != cudaSuccess || clusters < 1) {
+    cudaGetLastError();
+    return B2B_ERR_UNSUPPORTED;
+  }
+  p->grid = 2 * static_cast<int>(std::min<int64_t>(p->p3.total_tiles, clusters));
   return B2B_OK;
 }
 
@@ -443,6 +545,7 @@ b2b_status_t create_common(b2b_plan_t* out, b2b_dtype_t dt, int stages, bool sin
       cudaGetLastError();
       st = B2B_ERR_CUDA;
     }
+    if (st == B2B_OK && p->s3) st = pair_grid(p);
   }
   if (st == B2B_OK) {
     p->d_status = nullptr;
@@ -516,17 +619,21 @@ b2b_status_t encode_w4d(CUtensorMap* map, CUtensorMapDataType dt, int esz, const
 // the previous kernel in the stream is finishing; it waits (griddepcontrol)
 // before its first global-memory access.
 cudaError_t launch_pdl(const void* fn, dim3 grid, dim3 block, void** args, size_t smem,
-                       cudaStream_t stream) {
+                       cudaStream_t stream, int cluster = 1) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
   cfg.blockDim = block;
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = static_cast<unsigned>(cluster);
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = cluster > 1 ? 2 : 1;
   return cudaLaunchKernelExC(&cfg, fn, args);
 }
 
@@ -559,6 +666,18 @@ b2b_status_t encode_chain_maps(b2b_plan_s* p, const void* const* W, const void* 
       dst += p->batch * kin * p->N[s];
       kin = p->N[s];
     }
+  } else if (p->s3) {
+    // CTA pairs: each CTA loads half of a panel's 64-column blocks
+    for (int s = 0; s < 3 && st == B2B_OK; ++s) {
+      if ((p->p3.w_merged >> s) & 1) {
+        const int64_t width = s == 0 ? p->n1p : (s == 1 ? p->n2p : p->nf);
+        st = encode_w4d(&maps[1 + s], in_dt, p->esz, W[s], p->N[s], kin, p->batch, CK,
+                        static_cast<uint32_t>(width / 128));
+      } else {
+        st = encode_3d(&maps[1 + s], in_dt, p->esz, W[s], p->N[s], kin, p->batch, CK, CK);
+      }
+      kin = p->N[s];
+    }
   } else {
     for (int s = 0; s < S && st == B2B_OK; ++s) {
       if ((p->prm.w_merged >> s) & 1) {
@@ -574,8 +693,9 @@ b2b_status_t encode_chain_maps(b2b_plan_s* p, const void* const* W, const void* 
     }
   }
   for (int s = S; s < 3; ++s) maps[1 + s] = maps[1];
+  // (three-stage chains: every epilogue warp stores its own 32 rows)
   if (st == B2B_OK)
-    st = encode_3d(&maps[4], out_dt, p->osz, D, p->N[S - 1], p->M, p->batch, 128 / p->osz, 128);
+    st = encode_3d(&maps[4], out_dt, p->osz, D, p->N[S - 1], p->M, p->batch, 128 / p->osz, p->s3 ? 32 : 128);
   return st;
 }
 
@@ -635,9 +755,14 @@ b2b_status_t run_chain_tc(b2b_plan_s* p, const void* const* W, const void* A, vo
   prm.status = p->d_status;
   prm.budget_ns = p->budget_ns;
   prm.debug = p->debug;
-  void* args[6] = {&maps[0], &maps[1], &maps[2], &maps[3], &maps[4], &prm};
+  Chain3Params prm3 = p->p3;
+  prm3.status = p->d_status;
+  prm3.budget_ns = p->budget_ns;
+  prm3.debug = p->debug;
+  void* args[6] = {&maps[0], &maps[1], &maps[2], &maps[3], &maps[4],
+                   p->s3 ? static_cast<void*>(&prm3) : static_cast<void*>(&prm)};
   const cudaError_t e = launch_pdl(p->fn, dim3(p->grid), dim3(p->threads), args,
-                                   static_cast<size_t>(p->smem_bytes), stream);
+                                   static_cast<size_t>(p->smem_bytes), stream, p->s3 ? 2 : 1);
   if (e != cudaSuccess) {
     cudaGetLastError();
     return B2B_ERR_CUDA;
@@ -758,9 +883,9 @@ b2b_status_t b2b_plan_info(b2b_plan_t p, int* launches, int* grid, int* threads,
   if (grid) *grid = p->grid;
   if (threads) *threads = p->threads;
   if (smem) *smem = p->smem_bytes;
-  if (tmem_cols) *tmem_cols = tc ? static_cast<int>(p->prm.tmem_cols) : 0;
-  if (ring_stages) *ring_stages = tc ? p->prm.nst : 0;
-  if (passes) *passes = tc ? p->prm.npass : 1;
+  if (tmem_cols) *tmem_cols = !tc ? 0 : (p->s3 ? 512 : static_cast<int>(p->prm.tmem_cols));
+  if (ring_stages) *ring_stages = !tc ? 0 : (p->s3 ? p->p3.nst : p->prm.nst);
+  if (passes) *passes = !tc ? 1 : (p->s3 ? p->p3.npass : p->prm.npass);
   return B2B_OK;
 }
 

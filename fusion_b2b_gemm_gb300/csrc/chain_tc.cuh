@@ -25,7 +25,10 @@
 //              weights are resident; then warp 10 issues GEMM2)
 //   warps 2-5  converters: accumulator -> operand (the rearrangement)
 //   warps 6-9  epilogue: accumulator -> output type -> swizzled staging -> TMA store
-//   warp 10    second MMA-issuing thread (resident-weight chains)
+//   warp 10    second MMA-issuing thread (resident-weight chains), or the
+//              producer of the A ring (streamed weights: the A panels have a
+//              ring of their own, so that the next tile's A is read from HBM
+//              while the current tile's later GEMMs run)
 // Every wait is bounded (ptx::BoundedWait); on a timeout the CTA raises an
 // abort flag, every role leaves its loop, in-flight copies and MMAs are
 // drained, tensor memory is freed and the status word reports the timeout.
@@ -63,6 +66,8 @@ enum : int {
   kBarPFull1 = 33,  // second operand image (double-buffered intermediate)
   kBarPEmpty1 = 34,
   kSlotTmem = 35,   // uint32 TMEM base address, then the int abort flag
+  kBarAFull = 36,   // [8] A-ring stage filled by TMA (streamed weights)
+  kBarAEmpty = 44,  // [8] A-ring stage consumed by the MMAs
 };
 // Each consumer warpgroup has its own "full" barrier per region, so that it
 // sees every completion of that barrier in order: when the last GEMM reuses
@@ -74,9 +79,10 @@ struct ChainParams {
   int m_tiles, total_tiles;
   int npass;          // passes of the final GEMM (NF columns each)
   int kpan0;          // 128-byte K panels of A (ceil(K / panel width))
-  int nst;            // ring depth
+  int nst;            // ring depth (weight panels when streamed, A tiles when resident)
+  int nsta;           // streamed weights: depth of the separate ring of A panels
   int nstg;           // output staging buffers (1 or 2)
-  uint32_t off_ring, stage_bytes, off_wres0, off_wres1, off_p, off_stg, off_bar;
+  uint32_t off_ring, stage_bytes, off_aring, off_wres0, off_wres1, off_p, off_stg, off_bar;
   uint32_t tmem_cols;
   int region_col[4];  // X, Y, Z0, Z1 (TMEM column offsets)
   int nz;             // Z buffers for the final accumulator; 0 = reuse X/Y in turn
@@ -338,6 +344,8 @@ __global__ void __launch_bounds__(kChainThreads, 1)
     for (int i = 0; i < 8; ++i) {
       mbar_init(bar(kBarFull + i), 1);
       mbar_init(bar(kBarEmpty + i), 1);
+      mbar_init(bar(kBarAFull + i), 1);
+      mbar_init(bar(kBarAEmpty + i), 1);
     }
     mbar_init(bar(kBarWFull), 1);
     mbar_init(bar(kBarWEmpty), SPLIT ? 2 : 1);
@@ -437,7 +445,8 @@ __global__ void __launch_bounds__(kChainThreads, 1)
   // One GEMM phase issued by the calling thread: operands from the ring
   // and/or resident weights and/or the intermediate, accumulator in region r.
   // `stage`/`phase` track the ring; returns false on abort.
-  auto issue_phase = [&](int it, int ph, int r, uint32_t& stage, uint32_t& phase) -> bool {
+  auto issue_phase = [&](int it, int ph, int r, uint32_t& stage, uint32_t& phase, uint32_t& astage,
+                         uint32_t& aphase) -> bool {
     const int s = ph < S - 1 ? ph : S - 1;
     const int width = stage_width(s);
     const int kpan = stage_kpan(s);
@@ -456,11 +465,14 @@ __global__ void __launch_bounds__(kChainThreads, 1)
       const uint32_t sbase = base + p.off_ring + stage * p.stage_bytes;
       if (ring && kin == 0) {
         if (!bw.wait(bar(kBarFull + stage), phase)) return false;
+        if (!RES && s == 0 && !bw.wait(bar(kBarAFull + astage), aphase)) return false;
         tc_fence_after();
       }
-      const uint32_t sa = sbase + static_cast<uint32_t>(kin) * kPanelBytes;
-      const uint32_t b_base =
-          RES ? base + wres + static_cast<uint32_t>(kb) * 128u * width : sbase + kPanelBytes;
+      // resident weights: the stage is a whole A tile; streamed: the stage is
+      // one weight panel and A comes from its own ring
+      const uint32_t sa = RES ? sbase + static_cast<uint32_t>(kin) * kPanelBytes
+                              : base + p.off_aring + astage * static_cast<uint32_t>(kPanelBytes);
+      const uint32_t b_base = RES ? base + wres + static_cast<uint32_t>(kb) * 128u * width : sbase;
       auto bdesc = [&](int kk) -> uint64_t {
         return W_KMAJOR ? desc_sw128(b_base + kk * 32u, 16u, 1024u)
                         : desc_sw128(b_base + kk * KSTEP * 128u, WBOX_BYTES, 1024u);
@@ -493,6 +505,13 @@ __global__ void __launch_bounds__(kChainThreads, 1)
         if (++stage == static_cast<uint32_t>(p.nst)) {
           stage = 0;
           phase ^= 1u;
+        }
+        if (!RES && s == 0) {
+          tc_commit(bar(kBarAEmpty + astage));
+          if (++astage == static_cast<uint32_t>(p.nsta)) {
+            astage = 0;
+            aphase ^= 1u;
+          }
         }
       }
     }
@@ -555,27 +574,27 @@ __global__ void __launch_bounds__(kChainThreads, 1)
         for (int kb0 = 0; kb0 < kpan; kb0 += ppst) {
           if (!bw.wait(bar(kBarEmpty + stage), phase ^ 1u)) return false;
           const uint32_t dst = base + p.off_ring + stage * p.stage_bytes;
-          const uint32_t bytes = (s == 0 ? kPanelBytes * static_cast<uint32_t>(ppst) : 0u) +
-                                 (RES ? 0u : 128u * static_cast<uint32_t>(width));
-          mbar_arrive_expect_tx(bar(kBarFull + stage), bytes);
+          // (resident weights: the stage is an A tile; streamed: a weight panel)
+          const uint32_t bytes = RES ? kPanelBytes * static_cast<uint32_t>(ppst)
+                                     : 128u * static_cast<uint32_t>(width);
+          const uint32_t fb = bar(kBarFull + stage);
+          mbar_arrive_expect_tx(fb, bytes);
           // test support: the very first stage is armed but never filled, so
           // the MMA thread's bounded wait on it must run out
           const bool drop = (p.debug & 1u) && issued == 0;
           for (int q = 0; q < ppst && !drop; ++q) {
             const int kb = kb0 + q;
-            if (s == 0) tma_load_3d(dst + q * kPanelBytes, &tmA, bar(kBarFull + stage), kb * CK, m0, b);
-            if constexpr (!RES) {
-              if constexpr (W_KMAJOR) {
-                // one box: `width` rows of the transposed weight, 128 bytes of K
-                tma_load_3d(dst + kPanelBytes, wm, bar(kBarFull + stage), kb * CK, n0, b);
-              } else if ((p.w_merged >> s) & 1) {
-                // one box: all 64-column blocks of this panel
-                tma_load_4d(dst + kPanelBytes, wm, bar(kBarFull + stage), 0, kb * CK, n0 / WBOX_N, b);
-              } else {
-                for (int j = 0; j < width / WBOX_N; ++j)
-                  tma_load_3d(dst + kPanelBytes + j * WBOX_BYTES, wm, bar(kBarFull + stage),
-                              n0 + j * WBOX_N, kb * CK, b);
-              }
+            if constexpr (RES) {
+              tma_load_3d(dst + q * kPanelBytes, &tmA, fb, kb * CK, m0, b);
+            } else if constexpr (W_KMAJOR) {
+              // one box: `width` rows of the transposed weight, 128 bytes of K
+              tma_load_3d(dst, wm, fb, kb * CK, n0, b);
+            } else if ((p.w_merged >> s) & 1) {
+              // one box: all 64-column blocks of this panel
+              tma_load_4d(dst, wm, fb, 0, kb * CK, n0 / WBOX_N, b);
+            } else {
+              for (int j = 0; j < width / WBOX_N; ++j)
+                tma_load_3d(dst + j * WBOX_BYTES, wm, fb, n0 + j * WBOX_N, kb * CK, b);
             }
           }
           ++issued;
@@ -599,7 +618,7 @@ __global__ void __launch_bounds__(kChainThreads, 1)
   } else if (warp == 1 && !SPLIT) {
     // ---------------------------------------------- MMA (single issuer)
     if (lane == 0) {
-      uint32_t stage = 0, phase = 0, pf = 0, wl = 0;
+      uint32_t stage = 0, phase = 0, pf = 0, wl = 0, astage = 0, aphase = 0;
       int cur_b = -1;
       for_each_phase([&](int it, int ph, const TileCursor& c) -> bool {
         if (ph == 0) {
@@ -630,7 +649,7 @@ __global__ void __launch_bounds__(kChainThreads, 1)
         region_use(p, S, it, ph, r, u);
         if (!bw.wait(bar(kBarREmpty + r), (u & 1u) ^ 1u)) return false;
         tc_fence_after();
-        if (!issue_phase(it, ph, r, stage, phase)) return false;
+        if (!issue_phase(it, ph, r, stage, phase, astage, aphase)) return false;
         tc_commit(bar(ph < S - 1 ? kBarCFull + r : kBarRFull + r));
         if (S >= 2 && ph == nph - 1) tc_commit(bar(kBarPEmpty));
         if (RES && ph == nph - 1 && it + 1 < t_count) {
@@ -648,7 +667,7 @@ __global__ void __launch_bounds__(kChainThreads, 1)
     // ------------------------------- MMA, GEMM1 issuer (warp 1) and GEMM2 issuer (warp 10)
     if (lane == 0) {
       const bool g1 = (warp == 1);
-      uint32_t stage = 0, phase = 0, pf = 0, wl = 0;
+      uint32_t stage = 0, phase = 0, pf = 0, wl = 0, astage = 0, aphase = 0;
       int cur_b = -1;
       TileCursor c = first;
       bool ok = true;
@@ -669,7 +688,7 @@ __global__ void __launch_bounds__(kChainThreads, 1)
             if (!bw.wait(bar(r ? kBarPEmpty1 : kBarPEmpty), (u & 1u) ^ 1u)) break;
           }
           tc_fence_after();
-          if (!issue_phase(it, 0, r, stage, phase)) break;
+          if (!issue_phase(it, 0, r, stage, phase, astage, aphase)) break;
           tc_commit(bar(kBarCFull + r));
         } else {
           for (int pass = 0; pass < p.npass && ok; ++pass) {
@@ -694,7 +713,7 @@ __global__ void __launch_bounds__(kChainThreads, 1)
               break;
             }
             tc_fence_after();
-            if (!issue_phase(it, 1 + pass, r, stage, phase)) {
+            if (!issue_phase(it, 1 + pass, r, stage, phase, astage, aphase)) {
               ok = false;
               break;
             }
@@ -713,6 +732,44 @@ __global__ void __launch_bounds__(kChainThreads, 1)
       tc_commit(bar(db));
       drain_wait(bar(db), 0, p.budget_ns);
     }
+  } else if (!RES && warp == 10) {
+    // ------------------------------------------------- A-ring producer
+    // The A panels of every tile, in order, as far ahead as the A ring
+    // allows: the next tile's A arrives while this tile's later GEMMs run.
+    if (lane == 0) {
+      uint32_t as = 0, aph = 0;
+      uint64_t aissued = 0;
+      TileCursor c = first;
+      bool ok = true;
+      // (a single GEMM reads A once per pass of its N columns)
+      const int reads = (S == 1) ? p.npass : 1;
+      for (int it = 0; it < t_count && ok; ++it, c.next()) {
+        const int m0 = c.mt * 128;
+        for (int kq = 0; kq < reads * p.kpan0 && ok; ++kq) {
+          const int kb = kq % p.kpan0;
+          if (!bw.wait(bar(kBarAEmpty + as), aph ^ 1u)) {
+            ok = false;
+            break;
+          }
+          const uint32_t fb = bar(kBarAFull + as);
+          mbar_arrive_expect_tx(fb, kPanelBytes);
+          tma_load_3d(base + p.off_aring + as * static_cast<uint32_t>(kPanelBytes), &tmA, fb, kb * CK, m0, c.b);
+          ++aissued;
+          if (++as == static_cast<uint32_t>(p.nsta)) {
+            as = 0;
+            aph ^= 1u;
+          }
+        }
+      }
+      // copies still in flight must land before the CTA exits
+      const uint64_t n = static_cast<uint64_t>(p.nsta);
+      const uint64_t tail = aissued < n ? aissued : n;
+      for (uint64_t j = 0; j < tail; ++j) {
+        const uint64_t idx = aissued - 1 - j;
+        drain_wait(bar(kBarAFull + static_cast<int>(idx % n)), static_cast<uint32_t>((idx / n) & 1u),
+                   p.budget_ns);
+      }
+    }
   } else if (warp >= 2 && warp < 6) {
     // ---------------------------------------------------------- converters
     if constexpr (S >= 2) {
@@ -728,32 +785,29 @@ __global__ void __launch_bounds__(kChainThreads, 1)
           // the previous tile's intermediate must be consumed before this
           // tile's is written (and the converters never run two tiles ahead)
           const bool odd = p.dbl_p && (it & 1);
-          if (s == 0) {
-            const bool w = p.dbl_p ? warp_wait(bw, bar(odd ? kBarPEmpty1 : kBarPEmpty),
-                                               ((static_cast<uint32_t>(it) >> 1) & 1u) ^ 1u)
-                                   : warp_wait(bw, bar(kBarPEmpty), (static_cast<uint32_t>(it) & 1u) ^ 1u);
-            if (!w) {
-              ok = false;
-              break;
-            }
+          if (s == 0 && ok) {
+            ok = p.dbl_p ? warp_wait(bw, bar(odd ? kBarPEmpty1 : kBarPEmpty),
+                                     ((static_cast<uint32_t>(it) >> 1) & 1u) ^ 1u)
+                         : warp_wait(bw, bar(kBarPEmpty), (static_cast<uint32_t>(it) & 1u) ^ 1u);
           }
           // region r receives one intermediate per tile (per two tiles for
           // each of the two buffers of a lookahead chain)
           const uint32_t cu = lookahead ? static_cast<uint32_t>(it) >> 1 : static_cast<uint32_t>(it);
-          if (!warp_wait(bw, bar(kBarCFull + r), cu & 1u)) {
-            ok = false;
-            break;
+          if (ok) ok = warp_wait(bw, bar(kBarCFull + r), cu & 1u);
+          if (ok) {
+            tc_fence_after();
+            const int width = (s == 0) ? N1P : N2P;
+            const uint32_t tsrc = tmem_base + lane_off + static_cast<uint32_t>(p.region_col[r]);
+            if (!TF32 && p.p_tmem)
+              rearrange_accumulator_tmem16<IN>(tsrc, width);
+            else
+              rearrange_accumulator<IN>(tsrc, width, row, base + p.off_p + (odd ? p.p_bytes : 0u));
+            tc_fence_before();
           }
-          tc_fence_after();
-          const int width = (s == 0) ? N1P : N2P;
-          const uint32_t tsrc = tmem_base + lane_off + static_cast<uint32_t>(p.region_col[r]);
-          if (!TF32 && p.p_tmem)
-            rearrange_accumulator_tmem16<IN>(tsrc, width);
-          else
-            rearrange_accumulator<IN>(tsrc, width, row, base + p.off_p + (odd ? p.p_bytes : 0u));
-          tc_fence_before();
-          mbar_arrive(bar(odd ? kBarPFull1 : kBarPFull));
-          mbar_arrive(bar(kBarREmpty + r));
+          if (ok) {
+            mbar_arrive(bar(odd ? kBarPFull1 : kBarPFull));
+            mbar_arrive(bar(kBarREmpty + r));
+          }
         }
       }
     }

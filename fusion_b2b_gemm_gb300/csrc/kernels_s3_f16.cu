@@ -1,64 +1,26 @@
-// Three-stage tcgen05 chain kernels, fp16 inputs.
+// Three-stage chain kernels (CTA pairs), fp16 inputs.
 #include "registry.h"
 
 namespace b2b {
 namespace {
-const ChainKernelEntry kEntries[] = {
-    B2B_CHAIN_ENTRY(kInF16, kOutF16, 3, 64, 64, 64, false),
-    B2B_CHAIN_ENTRY(kInF16, kOutF16, 3, 64, 64, 128, false),
-    B2B_CHAIN_ENTRY(kInF16, kOutF16, 3, 64, 64, 256, false),
-    B2B_CHAIN_ENTRY(kInF16, kOutF16, 3, 64, 128, 64, false),
-    B2B_CHAIN_ENTRY(kInF16, kOutF16, 3, 64, 128, 128, false),
-    B2B_CHAIN_ENTRY(kInF16, kOutF16, 3, 64, 128, 256, false),
-    B2B_CHAIN_ENTRY(kInF16, kOutF16, 3, 64, 256, 64, false),
-    B2B_CHAIN_ENTRY(kInF16, kOutF16, 3, 64, 256, 128, false),
-    B2B_CHAIN_ENTRY(kInF16, kOutF16, 3, 64, 256, 256, false),
-    B2B_CHAIN_ENTRY(kInF16, kOutF16, 3, 128, 64, 64, false),
-    B2B_CHAIN_ENTRY(kInF16, kOutF16, 3, 128, 64, 128, false),
-    B2B_CHAIN_ENTRY(kInF16, kOutF16, 3, 128, 64, 256, false),
-    B2B_CHAIN_ENTRY(kInF16, kOutF16, 3, 128, 128, 64, false),
-    B2B_CHAIN_ENTRY(kInF16, kOutF16, 3, 128, 128, 128, false),
-    B2B_CHAIN_ENTRY(kInF16, kOutF16, 3, 128, 128, 256, false),
-    B2B_CHAIN_ENTRY(kInF16, kOutF16, 3, 128, 256, 64, false),
-    B2B_CHAIN_ENTRY(kInF16, kOutF16, 3, 128, 256, 128, false),
-    B2B_CHAIN_ENTRY(kInF16, kOutF16, 3, 128, 256, 256, false),
-    B2B_CHAIN_ENTRY(kInF16, kOutF16, 3, 256, 64, 64, false),
-    B2B_CHAIN_ENTRY(kInF16, kOutF16, 3, 256, 64, 128, false),
-    B2B_CHAIN_ENTRY(kInF16, kOutF16, 3, 256, 64, 256, false),
-    B2B_CHAIN_ENTRY(kInF16, kOutF16, 3, 256, 128, 64, false),
-    B2B_CHAIN_ENTRY(kInF16, kOutF16, 3, 256, 128, 128, false),
-    B2B_CHAIN_ENTRY(kInF16, kOutF16, 3, 256, 128, 256, false),
-    B2B_CHAIN_ENTRY(kInF16, kOutF16, 3, 256, 256, 64, false),
-    B2B_CHAIN_ENTRY(kInF16, kOutF16, 3, 256, 256, 128, false),
-    B2B_CHAIN_ENTRY(kInF16, kOutF16, 3, 256, 256, 256, false),
-    B2B_CHAIN_ENTRY(kInF16, kOutF32, 3, 64, 64, 64, false),
-    B2B_CHAIN_ENTRY(kInF16, kOutF32, 3, 64, 64, 128, false),
-    B2B_CHAIN_ENTRY(kInF16, kOutF32, 3, 64, 64, 256, false),
-    B2B_CHAIN_ENTRY(kInF16, kOutF32, 3, 64, 128, 64, false),
-    B2B_CHAIN_ENTRY(kInF16, kOutF32, 3, 64, 128, 128, false),
-    B2B_CHAIN_ENTRY(kInF16, kOutF32, 3, 64, 128, 256, false),
-    B2B_CHAIN_ENTRY(kInF16, kOutF32, 3, 64, 256, 64, false),
-    B2B_CHAIN_ENTRY(kInF16, kOutF32, 3, 64, 256, 128, false),
-    B2B_CHAIN_ENTRY(kInF16, kOutF32, 3, 64, 256, 256, false),
-    B2B_CHAIN_ENTRY(kInF16, kOutF32, 3, 128, 64, 64, false),
-    B2B_CHAIN_ENTRY(kInF16, kOutF32, 3, 128, 64, 128, false),
-    B2B_CHAIN_ENTRY(kInF16, kOutF32, 3, 128, 64, 256, false),
-    B2B_CHAIN_ENTRY(kInF16, kOutF32, 3, 128, 128, 64, false),
-    B2B_CHAIN_ENTRY(kInF16, kOutF32, 3, 128, 128, 128, false),
-    B2B_CHAIN_ENTRY(kInF16, kOutF32, 3, 128, 128, 256, false),
-    B2B_CHAIN_ENTRY(kInF16, kOutF32, 3, 128, 256, 64, false),
-    B2B_CHAIN_ENTRY(kInF16, kOutF32, 3, 128, 256, 128, false),
-    B2B_CHAIN_ENTRY(kInF16, kOutF32, 3, 128, 256, 256, false),
-    B2B_CHAIN_ENTRY(kInF16, kOutF32, 3, 256, 64, 64, false),
-    B2B_CHAIN_ENTRY(kInF16, kOutF32, 3, 256, 64, 128, false),
-    B2B_CHAIN_ENTRY(kInF16, kOutF32, 3, 256, 64, 256, false),
-    B2B_CHAIN_ENTRY(kInF16, kOutF32, 3, 256, 128, 64, false),
-    B2B_CHAIN_ENTRY(kInF16, kOutF32, 3, 256, 128, 128, false),
-    B2B_CHAIN_ENTRY(kInF16, kOutF32, 3, 256, 128, 256, false),
-    B2B_CHAIN_ENTRY(kInF16, kOutF32, 3, 256, 256, 64, false),
-    B2B_CHAIN_ENTRY(kInF16, kOutF32, 3, 256, 256, 128, false),
-    B2B_CHAIN_ENTRY(kInF16, kOutF32, 3, 256, 256, 256, false),
+const Chain3Entry kEntries[] = {
+    B2B_CHAIN3_ENTRY(kInF16, kOutF16, 128, 128, 128),
+    B2B_CHAIN3_ENTRY(kInF16, kOutF16, 128, 128, 256),
+    B2B_CHAIN3_ENTRY(kInF16, kOutF16, 128, 256, 128),
+    B2B_CHAIN3_ENTRY(kInF16, kOutF16, 128, 256, 256),
+    B2B_CHAIN3_ENTRY(kInF16, kOutF16, 256, 128, 128),
+    B2B_CHAIN3_ENTRY(kInF16, kOutF16, 256, 128, 256),
+    B2B_CHAIN3_ENTRY(kInF16, kOutF16, 256, 256, 128),
+    B2B_CHAIN3_ENTRY(kInF16, kOutF16, 256, 256, 256),
+    B2B_CHAIN3_ENTRY(kInF16, kOutF32, 128, 128, 128),
+    B2B_CHAIN3_ENTRY(kInF16, kOutF32, 128, 128, 256),
+    B2B_CHAIN3_ENTRY(kInF16, kOutF32, 128, 256, 128),
+    B2B_CHAIN3_ENTRY(kInF16, kOutF32, 128, 256, 256),
+    B2B_CHAIN3_ENTRY(kInF16, kOutF32, 256, 128, 128),
+    B2B_CHAIN3_ENTRY(kInF16, kOutF32, 256, 128, 256),
+    B2B_CHAIN3_ENTRY(kInF16, kOutF32, 256, 256, 128),
+    B2B_CHAIN3_ENTRY(kInF16, kOutF32, 256, 256, 256),
 };
 }  // namespace
-ChainTable chain_table_s3_f16() { return {kEntries, static_cast<int>(sizeof(kEntries) / sizeof(kEntries[0]))}; }
+Chain3Table chain3_table_f16() { return {kEntries, static_cast<int>(sizeof(kEntries) / sizeof(kEntries[0]))}; }
 }  // namespace b2b

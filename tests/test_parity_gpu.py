@@ -80,6 +80,12 @@ EXACT = [
     wl.Workload("x_bf16_3", "bf16", 1, 300, 512, (256, 256, 512), "int", 1, 13),
     wl.Workload("x_tf32", "tf32", 1, 333, 256, (256, 256), "int", 2, 14),
     wl.Workload("x_f64", "f64", 2, 77, 64, (64, 64), "int", 2, 15),
+    # three-stage chains run as CTA pairs sharing each MMA (256-row tiles):
+    # padded narrow widths, batches whose last pair tile is half past M, the
+    # final GEMM in one, two (Z buffers) or three passes
+    wl.Workload("x_f16_3_narrow", "f16", 3, 384, 64, (64, 64, 64), "int", 1, 16),
+    wl.Workload("x_bf16_f32out_3", "bf16_f32out", 2, 200, 128, (128, 128, 256), "int", 1, 17),
+    wl.Workload("x_f16_f32out_3", "f16_f32out", 1, 700, 192, (96, 160, 384), "int", 1, 18),
 ]
 
 
@@ -127,6 +133,9 @@ EDGES = [
     wl.Workload("n1_192_f16", "f16", 2, 200, 64, (192, 136), "normal_fanin", 1.0, 30),
     wl.Workload("n1_160_tf32", "tf32", 2, 150, 128, (160, 200), "normal", 1.0 / 16, 31),
     wl.Workload("n2_176_bf16_3", "bf16", 1, 140, 64, (176, 144, 200), "normal_fanin", 1.0, 32),
+    wl.Workload("m100_bf16_3", "bf16", 1, 100, 64, (256, 128, 72), "normal_fanin", 1.0, 33),
+    wl.Workload("batch3_m384_f16_3", "f16", 3, 384, 64, (128, 64, 128), "normal_fanin", 1.0, 34),
+    wl.Workload("k_tail_bf16_3", "bf16", 2, 300, 200, (128, 128, 128), "normal_fanin", 1.0, 35),
 ]
 
 

@@ -23,9 +23,10 @@
 // Roles (352 threads, one CTA per SM, persistent over 256-row tiles):
 //   warp 0     weight-panel producer (this CTA's half of each panel)
 //   warp 1     TMEM allocation (both CTAs); the even CTA's lane 0 issues MMAs
-//   warps 2-5  converters (accumulator -> operand image)
-//   warps 6-9  epilogue (accumulator -> output type -> staging -> TMA store,
-//              each warp its own 32 rows)
+//   warps 2-9  converters (accumulator -> operand image), half of the
+//              columns each for the two warps that share a TMEM lane quadrant
+//   warps 6-9  also the epilogue (accumulator -> output type -> staging ->
+//              TMA store, each warp its own 32 rows)
 //   warp 10    A-panel producer (a ring of its own, so that the next tile's
 //              A is read from HBM while this tile's later GEMMs run)
 // Every wait is bounded; after an abort the converter and epilogue loops are
@@ -47,7 +48,7 @@ enum : int {
   k3PFull = 34,     // [2] P1 / P2 written in both CTAs (even CTA's)
   k3PEmpty = 36,    // last pass of a tile complete: the operand image is free
   k3RFull = 37,     // [2] X / Y holds a pass product (epilogue)
-  k3REmpty = 39,    // [2] X / Y drained in both CTAs (even CTA's)
+  k3REmpty = 39,    // [2] X / Y pass product drained in both CTAs (even CTA's)
   k3Drain = 41,     // every MMA complete (exit)
   k3SlotTmem = 42,  // uint32 TMEM base, then the int abort flag
 };
@@ -134,11 +135,10 @@ __global__ void __launch_bounds__(kChainThreads, 1)
   grid_dependency_wait();
 
   BoundedWait bw{abort_flag, p.status, p.budget_ns, kTimeoutCode};
-  // Waits on barriers that threads of the peer CTA arrive on acquire at
-  // cluster scope; waits on copy and MMA completions at CTA scope (cheaper,
-  // and the MMA thread waits for every stage).
+  // Waits on barriers that threads of the peer CTA arrive on (the same
+  // default-scope wait: the cluster-scope acquire form costs more and the
+  // remote arrives are ordered by the barrier itself).
   BoundedWait bwm = bw;
-  bwm.cluster_scope = true;
   auto lbar = [&](int i) -> uint32_t { return mapa_shared(bar(i), 0); };
 
   // 256-row tiles, strided over the clusters; this CTA's 128 rows of each.
@@ -259,10 +259,11 @@ __global__ void __launch_bounds__(kChainThreads, 1)
     // ------------------------------------------- MMA (even CTA, lane 0)
     if (lane == 0 && leader) {
       uint32_t stage = 0, phase = 0, as = 0, aph = 0;
-      uint32_t u[2] = {0u, 0u};  // products written to X / Y so far
+      uint32_t u[2] = {0u, 0u};  // pass products written to X / Y so far
       bool ok = true;
-      // region r's previous product has been drained (by the converters or
-      // the epilogue, in both CTAs)
+      // region r's last pass product has been drained by the epilogue in
+      // both CTAs (an accumulator of GEMM1 / GEMM2 there has been read once
+      // the converters reported its operand image complete)
       auto drained = [&](int r) -> bool { return u[r] == 0 || bwm.wait(bar(k3REmpty + r), (u[r] - 1u) & 1u); };
       // One weight stage: four MMAs with A from the A ring (a_smem) or from
       // the operand image (K panel kb)
@@ -304,7 +305,6 @@ __global__ void __launch_bounds__(kChainThreads, 1)
         }
         if (!ok) break;
         tc_commit<CG>(bar(k3CFull + 0));
-        ++u[0];
         // GEMM2 -> Y, A = P1
         ok = bwm.wait(bar(k3PFull + 0), par) && drained(1);
         if (!ok) break;
@@ -315,7 +315,6 @@ __global__ void __launch_bounds__(kChainThreads, 1)
         }
         if (!ok) break;
         tc_commit<CG>(bar(k3CFull + 1));
-        ++u[1];
         // passes of GEMM3 -> X, Y, X, ..., A = P2
         ok = bwm.wait(bar(k3PFull + 1), par);
         const uint32_t idesc = make_idesc(FMT, NF, 256u, true);
@@ -335,38 +334,24 @@ __global__ void __launch_bounds__(kChainThreads, 1)
       tc_commit<CG>(bar(k3Drain));
       drain_wait(bar(k3Drain), 0, p.budget_ns);
     }
-  } else if (warp >= 2 && warp < 6) {
-    // ---------------------------------------------------------- converters
-    // X (GEMM1) then Y (GEMM2) of every tile into the operand image; the
-    // image is free once the previous tile's last pass has completed (P1)
-    // or once GEMM2 has (P2, implied by GEMM2's completion barrier).
-    const int row = (warp & 3) * 32 + lane;
-    const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
-    bool ok = true;
-    for (int it = 0; it < t_count; ++it) {
-      const uint32_t par = static_cast<uint32_t>(it) & 1u;
-      for (int g = 0; g < 2; ++g) {
-        if (g == 0 && it > 0 && ok) ok = warp_wait(bw, bar(k3PEmpty), par ^ 1u);
-        if (ok) ok = warp_wait(bw, bar(k3CFull + g), par);
-        if (ok) {
-          tc_fence_after();
-          rearrange_accumulator<IN>(tmem_base + lane_off + (g == 0 ? kX : kY), g == 0 ? N1P : N2P, row, p_img);
-          tc_fence_before();
-        }
-        named_bar_sync(2, 128);
-        if (warp == 2 && lane == 0 && ok) {
-          mbar_arrive_cluster(lbar(k3PFull + g));
-          mbar_arrive_cluster(lbar(k3REmpty + g));
-        }
-      }
-    }
-  } else if (warp >= 6 && warp < 10) {
-    // ------------------------------------------------------------ epilogue
-    // Each warp converts and stores its own 32 rows (boxes of 32 rows x 128
-    // bytes) through two staging buffers of its own, so the warps never wait
-    // for each other except once per pass, when the region has been read.
+  } else if (warp >= 2 && warp < 10) {
+    // ----------------------------------------- converters (warps 2-9) and
+    // ---------------------------------------------------- epilogue (6-9)
+    // Every tile: GEMM1's accumulator (X) then GEMM2's (Y) into the operand
+    // image, by all eight warps (warp w reads TMEM lanes 32 (w % 4) .. + 31;
+    // warps 2-5 take the low half of the columns, warps 6-9 the high half),
+    // then warps 6-9 store the passes of the last GEMM.  The image is free
+    // once the previous tile's last pass has completed (P1) or once GEMM2 has
+    // (P2, implied by GEMM2's completion barrier).
     const int q = warp & 3;
+    const int row = q * 32 + lane;
+    const int h = warp < 6 ? 0 : 1;
     const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
+    const bool epi = (warp >= 6);
+    // epilogue: each warp converts and stores its own 32 rows (boxes of 32
+    // rows x 128 bytes) through two staging buffers of its own, so the warps
+    // never wait for each other except once per pass, when the region has
+    // been read
     const uint32_t wstg = base + p.off_stg + static_cast<uint32_t>(q) * 2u * 4096u;
     const bool elected = (warp == 6 && lane == 0);
     constexpr int NBOX = NF / OBOX_N;
@@ -376,6 +361,21 @@ __global__ void __launch_bounds__(kChainThreads, 1)
     bool ok = true;
     TileCursor c = first;
     for (int it = 0; it < t_count; ++it, c.next()) {
+      const uint32_t par = static_cast<uint32_t>(it) & 1u;
+      for (int g = 0; g < 2; ++g) {
+        if (g == 0 && it > 0 && ok) ok = warp_wait(bw, bar(k3PEmpty), par ^ 1u);
+        if (ok) ok = warp_wait(bw, bar(k3CFull + g), par);
+        if (ok) {
+          tc_fence_after();
+          const int half = (g == 0 ? N1P : N2P) / 2;
+          rearrange_accumulator<IN>(tmem_base + lane_off + (g == 0 ? kX : kY) + static_cast<uint32_t>(h * half),
+                                    half, row, p_img + static_cast<uint32_t>(h * half / 64) * kPanelBytes);
+          tc_fence_before();
+        }
+        named_bar_sync(2, 256);
+        if (warp == 2 && lane == 0 && ok) mbar_arrive_cluster(lbar(k3PFull + g));
+      }
+      if (!epi) continue;
       const int mw = row0(c.mt) + q * 32;  // this warp's first row
       for (int j = 0; j < p.npass; ++j) {
         const int r = j & 1;
@@ -421,7 +421,7 @@ __global__ void __launch_bounds__(kChainThreads, 1)
         }
       }
     }
-    if (lane == 0) bulk_wait_all();
+    if (epi && lane == 0) bulk_wait_all();
   }
 
   __syncthreads();

@@ -71,9 +71,11 @@ __device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
   return r;
 }
 // Arrive on an mbarrier given by its cluster address (own or peer CTA).
+// Default semantics: a .release.cluster arrive was measured at about 1,100
+// cycles (it waits for the thread's earlier memory operations to become
+// visible cluster-wide), the default form at a small fraction of that.
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t bar_cl) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar_cl)
-               : "memory");
+  asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(bar_cl) : "memory");
 }
 __device__ __forceinline__ void mbar_arrive_expect_tx_cluster(uint32_t bar_cl, uint32_t bytes) {
   asm volatile("mbarrier.arrive.expect_tx.release.cluster.shared::cluster.b64 _, [%0], %1;" ::"r"(

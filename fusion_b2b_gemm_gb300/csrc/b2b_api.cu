@@ -304,6 +304,11 @@ b2b_status_t setup_chain_tc(b2b_plan_s* p) {
   uint32_t p_bytes =
       p_smem ? static_cast<uint32_t>(std::max(p->n1p, S >= 3 ? p->n2p : 0)) * 128u * p->esz : 0u;
   const int maxw = std::max({S >= 2 ? p->n1p : 0, S >= 3 ? p->n2p : 0, nf});
+  // Streamed weights: A panels get a ring of their own when CTAs run more
+  // than one tile (the next tile's A then loads during this tile's later
+  // GEMMs); with one tile per CTA A shares each GEMM1 stage with its weight
+  // panel (one wait per stage instead of two).
+  const bool split_a = c.total_tiles > p->sms;
 
   // Layouts in order of preference: weights resident for the whole batch
   // with two operand images for the intermediate, resident with one image,
@@ -313,8 +318,9 @@ b2b_status_t setup_chain_tc(b2b_plan_s* p) {
   auto fit = [&](bool res, bool dbl) -> Layout {
     Layout L{res, dbl, 0, 0, 0, 0, 0, 0};
     // resident: a ring stage holds a whole A tile (all K panels); streamed:
-    // one weight panel
-    L.stage = res ? static_cast<uint32_t>(c.kpan0) * kPanelBytes : 128u * static_cast<uint32_t>(maxw);
+    // one weight panel (behind its A panel when A has no ring of its own)
+    L.stage = res ? static_cast<uint32_t>(c.kpan0) * kPanelBytes
+                  : 128u * static_cast<uint32_t>(maxw) + (split_a ? 0u : kPanelBytes);
     if (res) {
       L.wres0 = static_cast<uint32_t>(c.kpan0) * 128u * p->n1p;
       L.wres1 = static_cast<uint32_t>(p->n1p / CK) * 128u * nf;
@@ -327,7 +333,7 @@ b2b_status_t setup_chain_tc(b2b_plan_s* p) {
         L.nst = room > 0 ? static_cast<int>(std::min<int64_t>(8, room / L.stage)) : 0;
         L.nsta = 0;
         if (L.nst >= 3 || (dbl && L.nst >= 2)) break;
-      } else {
+      } else if (split_a) {
         // up to four weight panels in flight; the rest of the room (up to
         // eight panels) for A
         const int64_t wroom = room - 2 * int64_t(kPanelBytes);
@@ -335,6 +341,10 @@ b2b_status_t setup_chain_tc(b2b_plan_s* p) {
         const int64_t aroom = room - int64_t(L.nst) * L.stage;
         L.nsta = aroom > 0 ? static_cast<int>(std::min<int64_t>(8, aroom / kPanelBytes)) : 0;
         if (L.nst >= 3 && L.nsta >= 4) break;
+      } else {
+        L.nst = room > 0 ? static_cast<int>(std::min<int64_t>(8, room / L.stage)) : 0;
+        L.nsta = 0;
+        if (L.nst >= 3) break;
       }
     }
     return L;
@@ -356,7 +366,7 @@ b2b_status_t setup_chain_tc(b2b_plan_s* p) {
       if (R.nst >= 3) L = R;
     }
   }
-  if (L.nst < 2 || (!L.res && L.nsta < 2)) return B2B_ERR_UNSUPPORTED;
+  if (L.nst < 2 || (!L.res && split_a && L.nsta < 2)) return B2B_ERR_UNSUPPORTED;
   p->res = L.res;
   c.dbl_p = L.dbl ? 1 : 0;
   c.p_tmem = p_tmem16 ? 1 : 0;

@@ -80,7 +80,8 @@ struct ChainParams {
   int npass;          // passes of the final GEMM (NF columns each)
   int kpan0;          // 128-byte K panels of A (ceil(K / panel width))
   int nst;            // ring depth (weight panels when streamed, A tiles when resident)
-  int nsta;           // streamed weights: depth of the separate ring of A panels
+  int nsta;           // streamed weights: depth of the separate ring of A panels (0: A shares
+                      // each GEMM1 stage with its weight panel)
   int nstg;           // output staging buffers (1 or 2)
   uint32_t off_ring, stage_bytes, off_aring, off_wres0, off_wres1, off_p, off_stg, off_bar;
   uint32_t tmem_cols;
@@ -402,6 +403,10 @@ __global__ void __launch_bounds__(kChainThreads, 1)
   first.init(t_begin, t_step, p.m_tiles);
   const int nph = NPH_FIXED + p.npass;
   const bool lookahead = p.lookahead != 0;
+  // streamed weights with CTAs that run several tiles: A panels come through
+  // a ring of their own (warp 10), so the next tile's A is read from HBM
+  // while this tile's later GEMMs run
+  const bool split_a = !RES && p.nsta > 0;
 
   auto stage_width = [](int s) -> int { return s < S - 1 ? (s == 0 ? N1P : N2P) : NF; };
   auto stage_kpan = [&](int s) -> int { return s == 0 ? p.kpan0 : (s == 1 ? N1P / CK : N2P / CK); };
@@ -465,14 +470,16 @@ __global__ void __launch_bounds__(kChainThreads, 1)
       const uint32_t sbase = base + p.off_ring + stage * p.stage_bytes;
       if (ring && kin == 0) {
         if (!bw.wait(bar(kBarFull + stage), phase)) return false;
-        if (!RES && s == 0 && !bw.wait(bar(kBarAFull + astage), aphase)) return false;
+        if (split_a && s == 0 && !bw.wait(bar(kBarAFull + astage), aphase)) return false;
         tc_fence_after();
       }
       // resident weights: the stage is a whole A tile; streamed: the stage is
-      // one weight panel and A comes from its own ring
+      // one weight panel, with A from its own ring or (GEMM1 without an A
+      // ring) in front of the weight panel
       const uint32_t sa = RES ? sbase + static_cast<uint32_t>(kin) * kPanelBytes
-                              : base + p.off_aring + astage * static_cast<uint32_t>(kPanelBytes);
-      const uint32_t b_base = RES ? base + wres + static_cast<uint32_t>(kb) * 128u * width : sbase;
+                              : (split_a ? base + p.off_aring + astage * static_cast<uint32_t>(kPanelBytes) : sbase);
+      const uint32_t b_base = RES ? base + wres + static_cast<uint32_t>(kb) * 128u * width
+                                  : sbase + (split_a || s != 0 ? 0u : static_cast<uint32_t>(kPanelBytes));
       auto bdesc = [&](int kk) -> uint64_t {
         return W_KMAJOR ? desc_sw128(b_base + kk * 32u, 16u, 1024u)
                         : desc_sw128(b_base + kk * KSTEP * 128u, WBOX_BYTES, 1024u);
@@ -506,7 +513,7 @@ __global__ void __launch_bounds__(kChainThreads, 1)
           stage = 0;
           phase ^= 1u;
         }
-        if (!RES && s == 0) {
+        if (split_a && s == 0) {
           tc_commit(bar(kBarAEmpty + astage));
           if (++astage == static_cast<uint32_t>(p.nsta)) {
             astage = 0;
@@ -574,9 +581,12 @@ __global__ void __launch_bounds__(kChainThreads, 1)
         for (int kb0 = 0; kb0 < kpan; kb0 += ppst) {
           if (!bw.wait(bar(kBarEmpty + stage), phase ^ 1u)) return false;
           const uint32_t dst = base + p.off_ring + stage * p.stage_bytes;
-          // (resident weights: the stage is an A tile; streamed: a weight panel)
+          // (resident weights: the stage is an A tile; streamed: a weight panel,
+          // behind its A panel in GEMM1 stages when A has no ring of its own)
+          const bool a_here = !RES && !split_a && s == 0;
+          const uint32_t wofs = a_here ? static_cast<uint32_t>(kPanelBytes) : 0u;
           const uint32_t bytes = RES ? kPanelBytes * static_cast<uint32_t>(ppst)
-                                     : 128u * static_cast<uint32_t>(width);
+                                     : 128u * static_cast<uint32_t>(width) + wofs;
           const uint32_t fb = bar(kBarFull + stage);
           mbar_arrive_expect_tx(fb, bytes);
           // test support: the very first stage is armed but never filled, so
@@ -586,15 +596,18 @@ __global__ void __launch_bounds__(kChainThreads, 1)
             const int kb = kb0 + q;
             if constexpr (RES) {
               tma_load_3d(dst + q * kPanelBytes, &tmA, fb, kb * CK, m0, b);
-            } else if constexpr (W_KMAJOR) {
-              // one box: `width` rows of the transposed weight, 128 bytes of K
-              tma_load_3d(dst, wm, fb, kb * CK, n0, b);
-            } else if ((p.w_merged >> s) & 1) {
-              // one box: all 64-column blocks of this panel
-              tma_load_4d(dst, wm, fb, 0, kb * CK, n0 / WBOX_N, b);
             } else {
-              for (int j = 0; j < width / WBOX_N; ++j)
-                tma_load_3d(dst + j * WBOX_BYTES, wm, fb, n0 + j * WBOX_N, kb * CK, b);
+              if (a_here) tma_load_3d(dst, &tmA, fb, kb * CK, m0, b);
+              if constexpr (W_KMAJOR) {
+                // one box: `width` rows of the transposed weight, 128 bytes of K
+                tma_load_3d(dst + wofs, wm, fb, kb * CK, n0, b);
+              } else if ((p.w_merged >> s) & 1) {
+                // one box: all 64-column blocks of this panel
+                tma_load_4d(dst + wofs, wm, fb, 0, kb * CK, n0 / WBOX_N, b);
+              } else {
+                for (int j = 0; j < width / WBOX_N; ++j)
+                  tma_load_3d(dst + wofs + j * WBOX_BYTES, wm, fb, n0 + j * WBOX_N, kb * CK, b);
+              }
             }
           }
           ++issued;
@@ -736,7 +749,7 @@ __global__ void __launch_bounds__(kChainThreads, 1)
     // ------------------------------------------------- A-ring producer
     // The A panels of every tile, in order, as far ahead as the A ring
     // allows: the next tile's A arrives while this tile's later GEMMs run.
-    if (lane == 0) {
+    if (lane == 0 && split_a) {
       uint32_t as = 0, aph = 0;
       uint64_t aissued = 0;
       TileCursor c = first;

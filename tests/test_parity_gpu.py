@@ -136,6 +136,10 @@ EDGES = [
     wl.Workload("m100_bf16_3", "bf16", 1, 100, 64, (256, 128, 72), "normal_fanin", 1.0, 33),
     wl.Workload("batch3_m384_f16_3", "f16", 3, 384, 64, (128, 64, 128), "normal_fanin", 1.0, 34),
     wl.Workload("k_tail_bf16_3", "bf16", 2, 300, 200, (128, 128, 128), "normal_fanin", 1.0, 35),
+    # streamed weights with more tiles than SMs: A panels through their own ring
+    wl.Workload("streamed_many_f16", "f16", 1, 40000, 512, (128, 128), "normal_fanin", 1.0, 36),
+    wl.Workload("streamed_many_tf32", "tf32", 2, 10000, 96, (64, 64), "normal", 1.0 / 16, 37),
+    wl.Workload("streamed_many_bf16_npass", "bf16", 1, 20000, 64, (128, 384), "normal_fanin", 1.0, 38),
 ]
 
 

@@ -229,7 +229,7 @@ b2b_status_t setup_chain3(b2b_plan_s* p) {
   const Chain3Entry* e = find_chain3_kernel(p->in_kind, p->out_kind, p->n1p, p->n2p, p->nf);
   if (!e) return B2B_ERR_UNSUPPORTED;
   p->fn = e->fn;
-  p->threads = kChainThreads;
+  p->threads = kChain3Threads;
   // the number of co-resident clusters is known once the kernel's shared
   // memory size is set (pair_grid)
   p->grid = static_cast<int>(std::min<int64_t>(2 * tiles, p->sms & ~1));

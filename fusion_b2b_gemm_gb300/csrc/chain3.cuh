@@ -29,6 +29,11 @@
 //              TMA store, each warp its own 32 rows)
 //   warp 10    A-panel producer (a ring of its own, so that the next tile's
 //              A is read from HBM while this tile's later GEMMs run)
+//   warp 11    stage watcher (even CTA): waits for every stage's copies in
+//              the MMAs' order and publishes the count in shared memory,
+//              which the MMA thread polls at a fraction of the cost of an
+//              mbarrier wait (the tensor pipe queues only about two MMAs, so
+//              the MMA thread's own waits would leave it idle)
 // Every wait is bounded; after an abort the converter and epilogue loops are
 // still walked to the end with the work skipped, so that named barriers stay
 // matched, and the two CTAs meet at a cluster barrier before exit.
@@ -45,13 +50,16 @@ enum : int {
   k3AFull = 16,     // [8] A stage filled (even CTA's)
   k3AEmpty = 24,    // [8] A stage consumed
   k3CFull = 32,     // [2] GEMM1 (X) / GEMM2 (Y) accumulator complete (converters)
-  k3PFull = 34,     // [2] P1 / P2 written in both CTAs (even CTA's)
-  k3PEmpty = 36,    // last pass of a tile complete: the operand image is free
-  k3RFull = 37,     // [2] X / Y holds a pass product (epilogue)
-  k3REmpty = 39,    // [2] X / Y pass product drained in both CTAs (even CTA's)
-  k3Drain = 41,     // every MMA complete (exit)
-  k3SlotTmem = 42,  // uint32 TMEM base, then the int abort flag
+  k3PChunk = 34,    // [2][2] half c of P1 / P2 written in both CTAs (even CTA's)
+  k3PEmpty = 38,    // last pass of a tile complete: the operand image is free
+  k3RFull = 39,     // [2] X / Y holds a pass product (epilogue)
+  k3REmpty = 41,    // [2] X / Y pass product drained in both CTAs (even CTA's)
+  k3Drain = 43,     // every MMA complete (exit)
+  k3SlotTmem = 44,  // uint32 TMEM base, then the int abort flag
+  k3SlotReady = 45, // uint32: weight stages whose operands have landed (even CTA)
 };
+
+constexpr int kChain3Threads = 384;
 
 struct Chain3Params {
   int batch, M, K;
@@ -68,7 +76,7 @@ struct Chain3Params {
 };
 
 template <int IN, int OUT, int N1P, int N2P, int NF>
-__global__ void __launch_bounds__(kChainThreads, 1)
+__global__ void __launch_bounds__(kChain3Threads, 1)
     chain3_kernel(const __grid_constant__ CUtensorMap tmA,
                   const __grid_constant__ CUtensorMap tmW0,
                   const __grid_constant__ CUtensorMap tmW1,
@@ -113,13 +121,15 @@ __global__ void __launch_bounds__(kChainThreads, 1)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(bar(k3CFull + i), 1);
-      mbar_init(bar(k3PFull + i), 2);
+      mbar_init(bar(k3PChunk + 2 * i), 2);
+      mbar_init(bar(k3PChunk + 2 * i + 1), 2);
       mbar_init(bar(k3RFull + i), 1);
       mbar_init(bar(k3REmpty + i), 2);
     }
     mbar_init(bar(k3PEmpty), 1);
     mbar_init(bar(k3Drain), 1);
     *abort_flag = 0;
+    *reinterpret_cast<volatile uint32_t*>(gbase + p.off_bar + 8 * k3SlotReady) = 0u;
     fence_barrier_init();
   }
   if (warp == 1) {
@@ -255,6 +265,29 @@ __global__ void __launch_bounds__(kChainThreads, 1)
                    p.budget_ns);
       }
     }
+  } else if (warp == 11) {
+    // ------------------------------------------ stage watcher (even CTA)
+    if (lane == 0 && leader) {
+      uint32_t stage = 0, phase = 0, as = 0, aph = 0, n = 0;
+      const uint32_t ready = bar(k3SlotReady);
+      const int per_tile = np1 + np2 + p.npass * np3;
+      bool ok = true;
+      for (int it = 0; it < t_count && ok; ++it) {
+        for (int q = 0; q < per_tile && ok; ++q) {
+          ok = bw.wait(bar(k3Full + stage), phase) && (q >= np1 || bw.wait(bar(k3AFull + as), aph));
+          if (!ok) break;
+          if (++stage == static_cast<uint32_t>(p.nst)) {
+            stage = 0;
+            phase ^= 1u;
+          }
+          if (q < np1 && ++as == static_cast<uint32_t>(p.nsta)) {
+            as = 0;
+            aph ^= 1u;
+          }
+          st_release_shared(ready, ++n);
+        }
+      }
+    }
   } else if (warp == 1) {
     // ------------------------------------------- MMA (even CTA, lane 0)
     if (lane == 0 && leader) {
@@ -267,9 +300,33 @@ __global__ void __launch_bounds__(kChainThreads, 1)
       auto drained = [&](int r) -> bool { return u[r] == 0 || bwm.wait(bar(k3REmpty + r), (u[r] - 1u) & 1u); };
       // One weight stage: four MMAs with A from the A ring (a_smem) or from
       // the operand image (K panel kb)
-      auto stage_mmas = [&](uint32_t d, uint32_t idesc, bool a_smem, int kb) -> bool {
-        if (!bw.wait(bar(k3Full + stage), phase)) return false;
-        if (a_smem && !bw.wait(bar(k3AFull + as), aph)) return false;
+      // stage number `consumed` has landed once the watcher's count exceeds it
+      uint32_t consumed = 0, seen = 0;
+      const uint32_t ready = bar(k3SlotReady);
+      auto stage_ready = [&]() -> bool {
+        if (seen > consumed) return true;
+        seen = ld_acquire_shared(ready);
+        if (seen > consumed) return true;
+        const uint64_t t0 = globaltimer_ns();
+        for (;;) {
+          for (int i = 0; i < 32; ++i) {
+            seen = ld_acquire_shared(ready);
+            if (seen > consumed) return true;
+          }
+          if (*abort_flag) return false;
+          if (globaltimer_ns() - t0 > p.budget_ns) {
+            bw.raise();
+            return false;
+          }
+        }
+      };
+      // chunk >= 0: the K panels from kb on need half `chunk` of the operand
+      // image, whose barrier is waited for here
+      auto stage_mmas = [&](uint32_t d, uint32_t idesc, bool a_smem, int kb, int chunk = -1,
+                            uint32_t cpar = 0) -> bool {
+        if (!stage_ready()) return false;
+        if (chunk >= 0 && !bwm.wait(bar(chunk), cpar)) return false;
+        ++consumed;
         tc_fence_after();
         const uint32_t wb = base + p.off_ring + stage * p.wstage;
         const uint32_t sa = a_smem ? base + p.off_aring + as * static_cast<uint32_t>(kPanelBytes)
@@ -305,25 +362,27 @@ __global__ void __launch_bounds__(kChainThreads, 1)
         }
         if (!ok) break;
         tc_commit<CG>(bar(k3CFull + 0));
-        // GEMM2 -> Y, A = P1
-        ok = bwm.wait(bar(k3PFull + 0), par) && drained(1);
+        // GEMM2 -> Y, A = P1, each half as soon as the converters finish it
+        ok = drained(1);
         if (!ok) break;
-        tc_fence_after();
         {
           const uint32_t idesc = make_idesc(FMT, N2P, 256u, true);
-          for (int kb = 0; kb < np2 && ok; ++kb) ok = stage_mmas(tmem_base + kY, idesc, false, kb);
+          for (int kb = 0; kb < np2 && ok; ++kb)
+            ok = stage_mmas(tmem_base + kY, idesc, false, kb,
+                            kb == 0 ? k3PChunk : (kb == np2 / 2 ? k3PChunk + 1 : -1), par);
         }
         if (!ok) break;
         tc_commit<CG>(bar(k3CFull + 1));
-        // passes of GEMM3 -> X, Y, X, ..., A = P2
-        ok = bwm.wait(bar(k3PFull + 1), par);
+        // passes of GEMM3 -> X, Y, X, ..., A = P2 (the first pass takes each
+        // half as soon as the converters finish it)
         const uint32_t idesc = make_idesc(FMT, NF, 256u, true);
         for (int j = 0; j < p.npass && ok; ++j) {
           const int r = j & 1;
           ok = drained(r);
           if (!ok) break;
-          tc_fence_after();
-          for (int kb = 0; kb < np3 && ok; ++kb) ok = stage_mmas(tmem_base + (r ? kY : kX), idesc, false, kb);
+          for (int kb = 0; kb < np3 && ok; ++kb)
+            ok = stage_mmas(tmem_base + (r ? kY : kX), idesc, false, kb,
+                            j != 0 ? -1 : (kb == 0 ? k3PChunk + 2 : (kb == np3 / 2 ? k3PChunk + 3 : -1)), par);
           if (!ok) break;
           tc_commit<CG>(bar(k3RFull + r));
           ++u[r];
@@ -365,15 +424,25 @@ __global__ void __launch_bounds__(kChainThreads, 1)
       for (int g = 0; g < 2; ++g) {
         if (g == 0 && it > 0 && ok) ok = warp_wait(bw, bar(k3PEmpty), par ^ 1u);
         if (ok) ok = warp_wait(bw, bar(k3CFull + g), par);
-        if (ok) {
-          tc_fence_after();
-          const int half = (g == 0 ? N1P : N2P) / 2;
-          rearrange_accumulator<IN>(tmem_base + lane_off + (g == 0 ? kX : kY) + static_cast<uint32_t>(h * half),
-                                    half, row, p_img + static_cast<uint32_t>(h * half / 64) * kPanelBytes);
-          tc_fence_before();
+        if (ok) tc_fence_after();
+        // a 256-column accumulator in two halves (each warp 64 columns of
+        // each), reported one at a time; a 128-column one in one step
+        const int width = g == 0 ? N1P : N2P;
+        const int nch = width == 256 ? 2 : 1;
+        const int cw = width / (2 * nch);  // columns per warp and chunk
+        for (int ch = 0; ch < nch; ++ch) {
+          if (ok) {
+            const int c0 = ch * (width / nch) + h * cw;
+            rearrange_accumulator<IN>(tmem_base + lane_off + (g == 0 ? kX : kY) + static_cast<uint32_t>(c0), cw,
+                                      row, p_img + static_cast<uint32_t>(c0 / 64) * kPanelBytes);
+            tc_fence_before();
+          }
+          named_bar_sync(2, 256);
+          if (warp == 2 && lane == 0 && ok) {
+            mbar_arrive_cluster(lbar(k3PChunk + 2 * g + ch));
+            if (nch == 1) mbar_arrive_cluster(lbar(k3PChunk + 2 * g + 1));
+          }
         }
-        named_bar_sync(2, 256);
-        if (warp == 2 && lane == 0 && ok) mbar_arrive_cluster(lbar(k3PFull + g));
       }
       if (!epi) continue;
       const int mw = row0(c.mt) + q * 32;  // this warp's first row

@@ -260,6 +260,12 @@ b2b_status_t setup_chain_tc(b2b_plan_s* p) {
       for (int c : cands)
         if (c >= wmin && c <= nl && base_la + k * c <= 512) { nf = c; nz = k; lookahead = 1; break; }
   }
+  // One tile per CTA: nothing to overlap across tiles, so one wide final
+  // accumulator (fewer, larger MMAs) beats two narrower alternating ones.
+  const bool one_tile = p->batch * ((p->M + 127) / 128) <= p->sms;
+  if (nz < 0 && one_tile)
+    for (int c : cands)
+      if (c >= wmin && c <= nl && base_z + c <= 512 && c >= std::min(nl, 256)) { nf = c; nz = 1; break; }
   if (nz < 0)
     for (int c : cands)
       if (c >= wmin && c <= nl && base_z + 2 * c <= 512) { nf = c; nz = 2; break; }

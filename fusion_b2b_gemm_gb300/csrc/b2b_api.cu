@@ -424,7 +424,15 @@ b2b_status_t pair_grid(b2b_plan_s* p) {
     cudaGetLastError();
     return B2B_ERR_UNSUPPORTED;
   }
-  p->grid = 2 * static_cast<int>(std::min<int64_t>(p->p3.total_tiles, clusters));
+  // Leftover tiles (when the tiles do not divide evenly among the clusters)
+  // are shared by two clusters each, one half of the last GEMM's passes
+  // apiece, if that leaves no cluster idle and there are passes to share.
+  Chain3Params& c = p->p3;
+  const int64_t total = c.total_tiles;
+  const int64_t ncl = std::min<int64_t>(clusters, c.npass >= 2 ? 2 * total : total);
+  p->grid = 2 * static_cast<int>(ncl);
+  const int64_t left = total % ncl;
+  c.split = (c.npass >= 2 && left > 0 && 2 * left <= ncl) ? static_cast<int>(left) : 0;
   return B2B_OK;
 }
 

@@ -70,10 +70,46 @@ struct Chain3Params {
   uint32_t wstage;           // bytes of a weight stage (half of the widest panel)
   uint32_t off_ring, off_aring, off_p, off_stg, off_bar;
   int w_merged;              // bit s: weight s is read as one 4-D box per half panel
+  int split;                 // leftover tiles whose passes are split between two clusters
   uint32_t debug;            // test support: bit 0 = the first weight stage is never filled
   int* status;
   unsigned long long budget_ns;
 };
+
+// Work units of a cluster.  Tiles are dealt to the clusters in strides; when
+// they do not divide evenly, the `split` leftover tiles are each shared by two
+// clusters, one taking the first half of the last GEMM's passes and the other
+// the rest (both compute GEMM1 and GEMM2), and these half units come first.
+// That shortens the longest cluster's work and starts half of the clusters
+// out of step with the others, which spreads their HBM-bound GEMM1 phases.
+struct Chain3Unit {
+  int b, mt, p0, p1;  // batch, 256-row tile, passes [p0, p1)
+};
+__device__ __forceinline__ int chain3_units(const Chain3Params& p, int cid, int ncl) {
+  if (p.split > 0) return p.total_tiles / ncl + (cid < 2 * p.split ? 1 : 0);
+  return cid < p.total_tiles ? (p.total_tiles - cid + ncl - 1) / ncl : 0;
+}
+__device__ __forceinline__ Chain3Unit chain3_unit(const Chain3Params& p, int cid, int ncl, int i) {
+  int tile, p0 = 0, p1 = p.npass;
+  if (p.split > 0 && cid < 2 * p.split) {
+    if (i == 0) {
+      tile = (p.total_tiles / ncl) * ncl + (cid >> 1);
+      const int h = (p.npass + 1) / 2;
+      p0 = (cid & 1) ? h : 0;
+      p1 = (cid & 1) ? p.npass : h;
+    } else {
+      tile = cid + (i - 1) * ncl;
+    }
+  } else {
+    tile = cid + i * ncl;
+  }
+  Chain3Unit u;
+  u.b = tile / p.m_tiles;
+  u.mt = tile - u.b * p.m_tiles;
+  u.p0 = p0;
+  u.p1 = p1;
+  return u;
+}
 
 template <int IN, int OUT, int N1P, int N2P, int NF>
 __global__ void __launch_bounds__(kChain3Threads, 1)
@@ -151,12 +187,11 @@ __global__ void __launch_bounds__(kChain3Threads, 1)
   BoundedWait bwm = bw;
   auto lbar = [&](int i) -> uint32_t { return mapa_shared(bar(i), 0); };
 
-  // 256-row tiles, strided over the clusters; this CTA's 128 rows of each.
+  // Work units (256-row tiles, or halves of their last GEMM) of this
+  // cluster; this CTA's 128 rows of each.
   const int cid = static_cast<int>(blockIdx.x >> 1);
   const int ncl = static_cast<int>(gridDim.x >> 1);
-  const int t_count = cid < p.total_tiles ? (p.total_tiles - cid + ncl - 1) / ncl : 0;
-  TileCursor first;
-  first.init(cid, ncl, p.m_tiles);
+  const int t_count = chain3_units(p, cid, ncl);
   auto row0 = [&](int mt) -> int { return mt * 256 + static_cast<int>(rank) * 128; };
   const uint32_t p_img = base + p.off_p;
 
@@ -173,10 +208,10 @@ __global__ void __launch_bounds__(kChain3Threads, 1)
       prefetch_tmap(&tmOut);
       uint32_t stage = 0, phase = 0;
       uint64_t issued = 0;
-      TileCursor c = first;
       bool ok = true;
-      const int per_tile = np1 + np2 + p.npass * np3;
-      for (int it = 0; it < t_count && ok; ++it, c.next()) {
+      for (int it = 0; it < t_count && ok; ++it) {
+        const Chain3Unit c = chain3_unit(p, cid, ncl, it);
+        const int per_tile = np1 + np2 + (c.p1 - c.p0) * np3;
         for (int q = 0; q < per_tile; ++q) {
           if (!bw.wait(bar(k3Empty + stage), phase ^ 1u)) {
             ok = false;
@@ -192,7 +227,8 @@ __global__ void __launch_bounds__(kChain3Threads, 1)
           } else {
             const int r = q - np1 - np2;
             const int j = r / np3;
-            s = 2; wm = &tmW2; kb = r - j * np3; wcols = NF / 2; n0 = j * NF + static_cast<int>(rank) * wcols;
+            s = 2; wm = &tmW2; kb = r - j * np3; wcols = NF / 2;
+            n0 = (c.p0 + j) * NF + static_cast<int>(rank) * wcols;
           }
           const uint32_t dst = base + p.off_ring + stage * p.wstage;
           const uint32_t fb = lbar(k3Full + stage);
@@ -232,9 +268,9 @@ __global__ void __launch_bounds__(kChain3Threads, 1)
       prefetch_tmap(&tmA);
       uint32_t as = 0, aph = 0;
       uint64_t issued = 0;
-      TileCursor c = first;
       bool ok = true;
-      for (int it = 0; it < t_count && ok; ++it, c.next()) {
+      for (int it = 0; it < t_count && ok; ++it) {
+        const Chain3Unit c = chain3_unit(p, cid, ncl, it);
         const int m0 = row0(c.mt);
         for (int kb = 0; kb < np1; ++kb) {
           // The ring holds the first nsta panels of a tile well ahead of
@@ -270,9 +306,10 @@ __global__ void __launch_bounds__(kChain3Threads, 1)
     if (lane == 0 && leader) {
       uint32_t stage = 0, phase = 0, as = 0, aph = 0, n = 0;
       const uint32_t ready = bar(k3SlotReady);
-      const int per_tile = np1 + np2 + p.npass * np3;
       bool ok = true;
       for (int it = 0; it < t_count && ok; ++it) {
+        const Chain3Unit c = chain3_unit(p, cid, ncl, it);
+        const int per_tile = np1 + np2 + (c.p1 - c.p0) * np3;
         for (int q = 0; q < per_tile && ok; ++q) {
           ok = bw.wait(bar(k3Full + stage), phase) && (q >= np1 || bw.wait(bar(k3AFull + as), aph));
           if (!ok) break;
@@ -351,6 +388,7 @@ __global__ void __launch_bounds__(kChain3Threads, 1)
         return true;
       };
       for (int it = 0; it < t_count && ok; ++it) {
+        const Chain3Unit c = chain3_unit(p, cid, ncl, it);
         const uint32_t par = static_cast<uint32_t>(it) & 1u;
         // GEMM1 -> X
         ok = drained(0);
@@ -373,16 +411,17 @@ __global__ void __launch_bounds__(kChain3Threads, 1)
         }
         if (!ok) break;
         tc_commit<CG>(bar(k3CFull + 1));
-        // passes of GEMM3 -> X, Y, X, ..., A = P2 (the first pass takes each
-        // half as soon as the converters finish it)
+        // the unit's passes of GEMM3 -> X, Y, X, ..., A = P2 (the first pass
+        // writes X, drained long ago, and takes each half of P2 as soon as
+        // the converters finish it)
         const uint32_t idesc = make_idesc(FMT, NF, 256u, true);
-        for (int j = 0; j < p.npass && ok; ++j) {
-          const int r = j & 1;
+        for (int j = c.p0; j < c.p1 && ok; ++j) {
+          const int r = (j - c.p0) & 1;
           ok = drained(r);
           if (!ok) break;
           for (int kb = 0; kb < np3 && ok; ++kb)
             ok = stage_mmas(tmem_base + (r ? kY : kX), idesc, false, kb,
-                            j != 0 ? -1 : (kb == 0 ? k3PChunk + 2 : (kb == np3 / 2 ? k3PChunk + 3 : -1)), par);
+                            j != c.p0 ? -1 : (kb == 0 ? k3PChunk + 2 : (kb == np3 / 2 ? k3PChunk + 3 : -1)), par);
           if (!ok) break;
           tc_commit<CG>(bar(k3RFull + r));
           ++u[r];
@@ -418,8 +457,8 @@ __global__ void __launch_bounds__(kChain3Threads, 1)
     uint32_t k[2] = {0u, 0u};
     uint32_t nbox = 0;
     bool ok = true;
-    TileCursor c = first;
-    for (int it = 0; it < t_count; ++it, c.next()) {
+    for (int it = 0; it < t_count; ++it) {
+      const Chain3Unit c = chain3_unit(p, cid, ncl, it);
       const uint32_t par = static_cast<uint32_t>(it) & 1u;
       for (int g = 0; g < 2; ++g) {
         if (g == 0 && it > 0 && ok) ok = warp_wait(bw, bar(k3PEmpty), par ^ 1u);
@@ -446,8 +485,8 @@ __global__ void __launch_bounds__(kChain3Threads, 1)
       }
       if (!epi) continue;
       const int mw = row0(c.mt) + q * 32;  // this warp's first row
-      for (int j = 0; j < p.npass; ++j) {
-        const int r = j & 1;
+      for (int j = c.p0; j < c.p1; ++j) {
+        const int r = (j - c.p0) & 1;
         if (ok) ok = warp_wait(bw, bar(k3RFull + r), k[r] & 1u);
         ++k[r];
         tc_fence_after();

@@ -209,17 +209,15 @@ b2b_status_t setup_chain3(b2b_plan_s* p) {
   c.total_tiles = static_cast<int>(tiles);
   c.npass = static_cast<int>((p->N[2] + p->nf - 1) / p->nf);
   c.kpan0 = static_cast<int>((p->K + 63) / 64);
-  c.wstage = 64u * static_cast<uint32_t>(std::max({p->n1p, p->n2p, p->nf}));
   const uint32_t p_bytes = 256u * static_cast<uint32_t>(std::max(p->n1p, p->n2p));
   c.nstg = 2;  // two 4 KB buffers per epilogue warp
   const int64_t room = kSmemBudget - kBarBytes - int64_t(p_bytes) - int64_t(c.nstg) * kPanelBytes;
-  // half of the room to each ring, at most eight stages each
-  c.nsta = static_cast<int>(std::min<int64_t>(8, room / 2 / kPanelBytes));
-  c.nst = static_cast<int>(std::min<int64_t>(8, (room - int64_t(c.nsta) * kPanelBytes) / c.wstage));
-  if (c.nst < 2 || c.nsta < 2) return B2B_ERR_UNSUPPORTED;
+  // the rest of shared memory: ring slots of 16 KB (an A panel or a weight
+  // half panel each), at most sixteen
+  c.nslot = static_cast<int>(std::min<int64_t>(16, room / kPanelBytes));
+  if (c.nslot < 4) return B2B_ERR_UNSUPPORTED;
   c.off_ring = 0;
-  c.off_aring = static_cast<uint32_t>(c.nst) * c.wstage;
-  c.off_p = c.off_aring + static_cast<uint32_t>(c.nsta) * kPanelBytes;
+  c.off_p = static_cast<uint32_t>(c.nslot) * kPanelBytes;
   c.off_stg = c.off_p + p_bytes;
   c.off_bar = c.off_stg + static_cast<uint32_t>(c.nstg) * kPanelBytes;
   p->smem_bytes = static_cast<int>(c.off_bar + kBarBytes + 1024);
@@ -908,7 +906,7 @@ b2b_status_t b2b_plan_info(b2b_plan_t p, int* launches, int* grid, int* threads,
   if (threads) *threads = p->threads;
   if (smem) *smem = p->smem_bytes;
   if (tmem_cols) *tmem_cols = !tc ? 0 : (p->s3 ? 512 : static_cast<int>(p->prm.tmem_cols));
-  if (ring_stages) *ring_stages = !tc ? 0 : (p->s3 ? p->p3.nst : p->prm.nst);
+  if (ring_stages) *ring_stages = !tc ? 0 : (p->s3 ? p->p3.nslot : p->prm.nst);
   if (passes) *passes = !tc ? 1 : (p->s3 ? p->p3.npass : p->prm.npass);
   return B2B_OK;
 }

@@ -21,15 +21,16 @@
 // the MMAs of the next.
 //
 // Roles (352 threads, one CTA per SM, persistent over 256-row tiles):
-//   warp 0     weight-panel producer (this CTA's half of each panel)
+//   warp 0     producer: one ring of 16 KB slots in the order the MMAs read
+//              them (GEMM1: an A panel and this CTA's half of a weight panel;
+//              GEMM2 and the passes: a weight half panel), so the weights of
+//              GEMM2 and of the passes can have the whole ring in flight
 //   warp 1     TMEM allocation (both CTAs); the even CTA's lane 0 issues MMAs
 //   warps 2-9  converters (accumulator -> operand image), half of the
 //              columns each for the two warps that share a TMEM lane quadrant
 //   warps 6-9  also the epilogue (accumulator -> output type -> staging ->
 //              TMA store, each warp its own 32 rows)
-//   warp 10    A-panel producer (a ring of its own, so that the next tile's
-//              A is read from HBM while this tile's later GEMMs run)
-//   warp 11    stage watcher (even CTA): waits for every stage's copies in
+//   warp 11    slot watcher (even CTA): waits for every slot's copies in
 //              the MMAs' order and publishes the count in shared memory,
 //              which the MMA thread polls at a fraction of the cost of an
 //              mbarrier wait (the tensor pipe queues only about two MMAs, so
@@ -45,10 +46,8 @@ namespace b2b {
 
 // Barrier slots (8 bytes each) at Chain3Params::off_bar.
 enum : int {
-  k3Full = 0,       // [8] weight stage filled (even CTA's: armed by it for both CTAs' copies)
-  k3Empty = 8,      // [8] weight stage consumed
-  k3AFull = 16,     // [8] A stage filled (even CTA's)
-  k3AEmpty = 24,    // [8] A stage consumed
+  k3Full = 0,       // [16] ring slot filled (even CTA's: armed by it for both CTAs' copies)
+  k3Empty = 16,     // [16] ring slot consumed
   k3CFull = 32,     // [2] GEMM1 (X) / GEMM2 (Y) accumulator complete (converters)
   k3PChunk = 34,    // [2][2] half c of P1 / P2 written in both CTAs (even CTA's)
   k3PEmpty = 38,    // last pass of a tile complete: the operand image is free
@@ -56,7 +55,7 @@ enum : int {
   k3REmpty = 41,    // [2] X / Y pass product drained in both CTAs (even CTA's)
   k3Drain = 43,     // every MMA complete (exit)
   k3SlotTmem = 44,  // uint32 TMEM base, then the int abort flag
-  k3SlotReady = 45, // uint32: weight stages whose operands have landed (even CTA)
+  k3SlotReady = 45, // uint32: ring slots whose copies have landed (even CTA)
 };
 
 constexpr int kChain3Threads = 384;
@@ -66,9 +65,8 @@ struct Chain3Params {
   int m_tiles, total_tiles;  // 256-row tiles per batch, in all
   int npass;                 // NF-column passes of the last GEMM
   int kpan0;                 // 64-element K panels of A
-  int nst, nsta, nstg;       // weight-ring, A-ring and staging depths
-  uint32_t wstage;           // bytes of a weight stage (half of the widest panel)
-  uint32_t off_ring, off_aring, off_p, off_stg, off_bar;
+  int nslot, nstg;           // ring slots (16 KB each) and staging buffers per warp
+  uint32_t off_ring, off_p, off_stg, off_bar;
   int w_merged;              // bit s: weight s is read as one 4-D box per half panel
   int split;                 // leftover tiles whose passes are split between two clusters
   uint32_t debug;            // test support: bit 0 = the first weight stage is never filled
@@ -149,11 +147,9 @@ __global__ void __launch_bounds__(kChain3Threads, 1)
   const bool leader = (rank == 0);
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < 8; ++i) {
+    for (int i = 0; i < 16; ++i) {
       mbar_init(bar(k3Full + i), 1);
       mbar_init(bar(k3Empty + i), 1);
-      mbar_init(bar(k3AFull + i), 1);
-      mbar_init(bar(k3AEmpty + i), 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(bar(k3CFull + i), 1);
@@ -195,50 +191,65 @@ __global__ void __launch_bounds__(kChain3Threads, 1)
   auto row0 = [&](int mt) -> int { return mt * 256 + static_cast<int>(rank) * 128; };
   const uint32_t p_img = base + p.off_p;
 
-  // Weight stages of one tile, in the order the MMAs read them: GEMM1
-  // (kpan0 panels), GEMM2 (N1P / 64), then every pass (N2P / 64 each).
+  // Ring slots of one unit, in the order the MMAs read them: GEMM1 (kpan0
+  // panels, two slots each: A, weight), GEMM2 (N1P / 64 slots), then every
+  // pass of the unit (N2P / 64 slots each).
   const int np1 = p.kpan0, np2 = N1P / CK, np3 = N2P / CK;
 
   if (warp == 0) {
-    // ---------------------------------------------------- weight producer
+    // ------------------------------------------------------------ producer
     if (lane == 0) {
+      prefetch_tmap(&tmA);
       prefetch_tmap(&tmW0);
       prefetch_tmap(&tmW1);
       prefetch_tmap(&tmW2);
       prefetch_tmap(&tmOut);
-      uint32_t stage = 0, phase = 0;
+      uint32_t slot = 0, phase = 0;
       uint64_t issued = 0;
       bool ok = true;
       for (int it = 0; it < t_count && ok; ++it) {
         const Chain3Unit c = chain3_unit(p, cid, ncl, it);
-        const int per_tile = np1 + np2 + (c.p1 - c.p0) * np3;
-        for (int q = 0; q < per_tile; ++q) {
-          if (!bw.wait(bar(k3Empty + stage), phase ^ 1u)) {
+        const int m0 = row0(c.mt);
+        // the ring reaches only a few panels into the next unit's GEMM1: pull
+        // the next unit's A into L2 now
+        if (it + 1 < t_count) {
+          const Chain3Unit n = chain3_unit(p, cid, ncl, it + 1);
+          for (int q = 0; q < np1; ++q) tma_prefetch_l2_3d(&tmA, q * CK, row0(n.mt), n.b);
+        }
+        const int per_unit = 2 * np1 + np2 + (c.p1 - c.p0) * np3;
+        for (int q = 0; q < per_unit; ++q) {
+          if (!bw.wait(bar(k3Empty + slot), phase ^ 1u)) {
             ok = false;
             break;
           }
-          // which weight, K panel, and this CTA's columns
-          const CUtensorMap* wm;
-          int kb, n0, wcols, s;
-          if (q < np1) {
-            s = 0; wm = &tmW0; kb = q; wcols = N1P / 2; n0 = static_cast<int>(rank) * wcols;
-          } else if (q < np1 + np2) {
-            s = 1; wm = &tmW1; kb = q - np1; wcols = N2P / 2; n0 = static_cast<int>(rank) * wcols;
+          // which operand, K panel and (weights) this CTA's columns
+          const CUtensorMap* wm = nullptr;
+          int kb, n0 = 0, wcols = 0, s = -1;
+          if (q < 2 * np1) {
+            kb = q >> 1;
+            if (q & 1) {
+              s = 0; wm = &tmW0; wcols = N1P / 2; n0 = static_cast<int>(rank) * wcols;
+            }
+          } else if (q < 2 * np1 + np2) {
+            s = 1; wm = &tmW1; kb = q - 2 * np1; wcols = N2P / 2; n0 = static_cast<int>(rank) * wcols;
           } else {
-            const int r = q - np1 - np2;
+            const int r = q - 2 * np1 - np2;
             const int j = r / np3;
             s = 2; wm = &tmW2; kb = r - j * np3; wcols = NF / 2;
             n0 = (c.p0 + j) * NF + static_cast<int>(rank) * wcols;
           }
-          const uint32_t dst = base + p.off_ring + stage * p.wstage;
-          const uint32_t fb = lbar(k3Full + stage);
-          // Only the even CTA arms its barrier, for both CTAs' halves; the odd
+          const uint32_t dst = base + p.off_ring + slot * static_cast<uint32_t>(kPanelBytes);
+          const uint32_t fb = lbar(k3Full + slot);
+          const uint32_t bytes = s < 0 ? static_cast<uint32_t>(kPanelBytes) : 128u * static_cast<uint32_t>(wcols);
+          // Only the even CTA arms its barrier, for both CTAs' copies; the odd
           // CTA's copies may land first (the transaction count then dips
           // below zero until the arming, which the barrier allows).
-          if (leader) mbar_arrive_expect_tx(bar(k3Full + stage), 2u * 128u * static_cast<uint32_t>(wcols));
-          // test support: the very first stage is armed but never filled
+          if (leader) mbar_arrive_expect_tx(bar(k3Full + slot), 2u * bytes);
+          // test support: the very first slot is armed but never filled
           if (!((p.debug & 1u) && issued == 0)) {
-            if ((p.w_merged >> s) & 1) {
+            if (s < 0) {
+              tma_load_3d_pair(dst, &tmA, fb, kb * CK, m0, c.b);
+            } else if ((p.w_merged >> s) & 1) {
               tma_load_4d_pair(dst, wm, fb, 0, kb * CK, n0 / WBOX_N, c.b);
             } else {
               for (int j = 0; j < wcols / WBOX_N; ++j)
@@ -246,15 +257,15 @@ __global__ void __launch_bounds__(kChain3Threads, 1)
             }
           }
           ++issued;
-          if (++stage == static_cast<uint32_t>(p.nst)) {
-            stage = 0;
+          if (++slot == static_cast<uint32_t>(p.nslot)) {
+            slot = 0;
             phase ^= 1u;
           }
         }
       }
       // copies in flight land before exit (the even CTA's barriers count both
       // CTAs' copies; the odd CTA waits at the cluster barrier before exit)
-      const uint64_t n = static_cast<uint64_t>(p.nst);
+      const uint64_t n = static_cast<uint64_t>(p.nslot);
       const uint64_t tail = !leader ? 0 : (issued < n ? issued : n);
       for (uint64_t j = 0; j < tail; ++j) {
         const uint64_t idx = issued - 1 - j;
@@ -262,64 +273,21 @@ __global__ void __launch_bounds__(kChain3Threads, 1)
                    p.budget_ns);
       }
     }
-  } else if (warp == 10) {
-    // --------------------------------------------------------- A producer
-    if (lane == 0) {
-      prefetch_tmap(&tmA);
-      uint32_t as = 0, aph = 0;
-      uint64_t issued = 0;
-      bool ok = true;
-      for (int it = 0; it < t_count && ok; ++it) {
-        const Chain3Unit c = chain3_unit(p, cid, ncl, it);
-        const int m0 = row0(c.mt);
-        for (int kb = 0; kb < np1; ++kb) {
-          // The ring holds the first nsta panels of a tile well ahead of
-          // GEMM1; the later ones are loaded only as GEMM1 frees stages, so
-          // pull them into L2 now, a tile ahead.
-          if (kb == 0)
-            for (int q = p.nsta; q < np1; ++q) tma_prefetch_l2_3d(&tmA, q * CK, m0, c.b);
-          if (!bw.wait(bar(k3AEmpty + as), aph ^ 1u)) {
-            ok = false;
-            break;
-          }
-          const uint32_t fb = lbar(k3AFull + as);
-          if (leader) mbar_arrive_expect_tx(bar(k3AFull + as), 2u * kPanelBytes);
-          tma_load_3d_pair(base + p.off_aring + as * static_cast<uint32_t>(kPanelBytes), &tmA, fb, kb * CK,
-                           m0, c.b);
-          ++issued;
-          if (++as == static_cast<uint32_t>(p.nsta)) {
-            as = 0;
-            aph ^= 1u;
-          }
-        }
-      }
-      const uint64_t n = static_cast<uint64_t>(p.nsta);
-      const uint64_t tail = !leader ? 0 : (issued < n ? issued : n);
-      for (uint64_t j = 0; j < tail; ++j) {
-        const uint64_t idx = issued - 1 - j;
-        drain_wait(bar(k3AFull + static_cast<int>(idx % n)), static_cast<uint32_t>((idx / n) & 1u),
-                   p.budget_ns);
-      }
-    }
   } else if (warp == 11) {
-    // ------------------------------------------ stage watcher (even CTA)
+    // ------------------------------------------- slot watcher (even CTA)
     if (lane == 0 && leader) {
-      uint32_t stage = 0, phase = 0, as = 0, aph = 0, n = 0;
+      uint32_t slot = 0, phase = 0, n = 0;
       const uint32_t ready = bar(k3SlotReady);
       bool ok = true;
       for (int it = 0; it < t_count && ok; ++it) {
         const Chain3Unit c = chain3_unit(p, cid, ncl, it);
-        const int per_tile = np1 + np2 + (c.p1 - c.p0) * np3;
-        for (int q = 0; q < per_tile && ok; ++q) {
-          ok = bw.wait(bar(k3Full + stage), phase) && (q >= np1 || bw.wait(bar(k3AFull + as), aph));
+        const int per_unit = 2 * np1 + np2 + (c.p1 - c.p0) * np3;
+        for (int q = 0; q < per_unit && ok; ++q) {
+          ok = bw.wait(bar(k3Full + slot), phase);
           if (!ok) break;
-          if (++stage == static_cast<uint32_t>(p.nst)) {
-            stage = 0;
+          if (++slot == static_cast<uint32_t>(p.nslot)) {
+            slot = 0;
             phase ^= 1u;
-          }
-          if (q < np1 && ++as == static_cast<uint32_t>(p.nsta)) {
-            as = 0;
-            aph ^= 1u;
           }
           st_release_shared(ready, ++n);
         }
@@ -328,7 +296,7 @@ __global__ void __launch_bounds__(kChain3Threads, 1)
   } else if (warp == 1) {
     // ------------------------------------------- MMA (even CTA, lane 0)
     if (lane == 0 && leader) {
-      uint32_t stage = 0, phase = 0, as = 0, aph = 0;
+      uint32_t slot = 0;
       uint32_t u[2] = {0u, 0u};  // pass products written to X / Y so far
       bool ok = true;
       // region r's last pass product has been drained by the epilogue in
@@ -337,18 +305,19 @@ __global__ void __launch_bounds__(kChain3Threads, 1)
       auto drained = [&](int r) -> bool { return u[r] == 0 || bwm.wait(bar(k3REmpty + r), (u[r] - 1u) & 1u); };
       // One weight stage: four MMAs with A from the A ring (a_smem) or from
       // the operand image (K panel kb)
-      // stage number `consumed` has landed once the watcher's count exceeds it
+      // the next `need` slots have landed once the watcher's count reaches
+      // consumed + need
       uint32_t consumed = 0, seen = 0;
       const uint32_t ready = bar(k3SlotReady);
-      auto stage_ready = [&]() -> bool {
-        if (seen > consumed) return true;
+      auto stage_ready = [&](uint32_t need) -> bool {
+        if (seen >= consumed + need) return true;
         seen = ld_acquire_shared(ready);
-        if (seen > consumed) return true;
+        if (seen >= consumed + need) return true;
         const uint64_t t0 = globaltimer_ns();
         for (;;) {
           for (int i = 0; i < 32; ++i) {
             seen = ld_acquire_shared(ready);
-            if (seen > consumed) return true;
+            if (seen >= consumed + need) return true;
           }
           if (*abort_flag) return false;
           if (globaltimer_ns() - t0 > p.budget_ns) {
@@ -358,33 +327,28 @@ __global__ void __launch_bounds__(kChain3Threads, 1)
         }
       };
       // chunk >= 0: the K panels from kb on need half `chunk` of the operand
-      // image, whose barrier is waited for here
+      // image, whose barrier is waited for here.  GEMM1 (a_smem): the A panel
+      // is in this slot and the weight half panel in the next.
       auto stage_mmas = [&](uint32_t d, uint32_t idesc, bool a_smem, int kb, int chunk = -1,
                             uint32_t cpar = 0) -> bool {
-        if (!stage_ready()) return false;
+        const uint32_t need = a_smem ? 2u : 1u;
+        if (!stage_ready(need)) return false;
         if (chunk >= 0 && !bwm.wait(bar(chunk), cpar)) return false;
-        ++consumed;
+        consumed += need;
         tc_fence_after();
-        const uint32_t wb = base + p.off_ring + stage * p.wstage;
-        const uint32_t sa = a_smem ? base + p.off_aring + as * static_cast<uint32_t>(kPanelBytes)
+        const uint32_t s0 = slot;
+        const uint32_t s1 = a_smem ? (slot + 1u == static_cast<uint32_t>(p.nslot) ? 0u : slot + 1u) : slot;
+        const uint32_t wb = base + p.off_ring + s1 * static_cast<uint32_t>(kPanelBytes);
+        const uint32_t sa = a_smem ? base + p.off_ring + s0 * static_cast<uint32_t>(kPanelBytes)
                                    : p_img + static_cast<uint32_t>(kb) * kPanelBytes;
         const uint32_t acc0 = kb != 0 ? 1u : 0u;
 #pragma unroll
         for (int kk = 0; kk < CK / KSTEP; ++kk)
           mma_ss<false, CG>(d, desc_sw128(sa + kk * 32u, 16u, 1024u),
                             desc_sw128(wb + kk * KSTEP * 128u, WBOX_BYTES, 1024u), idesc, kk ? 1u : acc0);
-        tc_commit<CG>(bar(k3Empty + stage));
-        if (++stage == static_cast<uint32_t>(p.nst)) {
-          stage = 0;
-          phase ^= 1u;
-        }
-        if (a_smem) {
-          tc_commit<CG>(bar(k3AEmpty + as));
-          if (++as == static_cast<uint32_t>(p.nsta)) {
-            as = 0;
-            aph ^= 1u;
-          }
-        }
+        tc_commit<CG>(bar(k3Empty + s0));
+        if (a_smem) tc_commit<CG>(bar(k3Empty + s1));
+        slot = s1 + 1u == static_cast<uint32_t>(p.nslot) ? 0u : s1 + 1u;
         return true;
       };
       for (int it = 0; it < t_count && ok; ++it) {

@@ -6,7 +6,8 @@ device memory and streams.  There is no fallback: if the library is missing
 this module raises on import, telling how to build it.
 
 Low-level functions carry the C names (``b2b_plan_create``, ``b2b_run``,
-...); :class:`Plan` and :class:`GemmPlan` wrap them for torch tensors.
+...); :class:`Plan`, :class:`ChainPlan` and :class:`GemmPlan` wrap them for
+torch tensors.
 """
 from __future__ import annotations
 
@@ -15,8 +16,9 @@ import os
 from typing import Optional, Sequence, Tuple
 
 __all__ = [
-    "B2BError", "DTYPES", "Plan", "GemmPlan", "library_path",
-    "b2b_plan_create", "b2b_gemm_plan_create", "b2b_run", "b2b_plan_destroy",
+    "B2BError", "DTYPES", "MAX_STAGES", "Plan", "ChainPlan", "GemmPlan", "library_path",
+    "b2b_plan_create", "b2b_chain_plan_create", "b2b_gemm_plan_create", "b2b_run", "b2b_chain_run",
+    "b2b_plan_destroy",
     "b2b_plan_device_status", "b2b_plan_set_wait_budget", "b2b_plan_set_debug", "b2b_plan_info",
     "b2b_status_string", "b2b_coordination_matrix", "b2b_probe_operand_image",
     "b2b_probe_f64_rearrange", "b2b_run_tf32_noalloc", "coordination_matrix",
@@ -27,6 +29,7 @@ _LIB_PATH = os.path.join(_HERE, "_lib", "libb2b.so")
 
 # b2b_dtype_t
 DTYPES = {"f16_f32out": 0, "f16": 1, "bf16": 2, "tf32": 3, "f64": 4, "bf16_f32out": 5}
+MAX_STAGES = 8  # B2B_MAX_STAGES
 STATUS = {0: "B2B_OK", 1: "B2B_ERR_INVALID_ARG", 2: "B2B_ERR_UNSUPPORTED", 3: "B2B_ERR_ALIGNMENT",
           4: "B2B_ERR_ALIAS", 5: "B2B_ERR_DEVICE", 6: "B2B_ERR_CUDA", 7: "B2B_ERR_TIMEOUT"}
 
@@ -53,6 +56,8 @@ def _load() -> ctypes.CDLL:
     ip = ctypes.POINTER(ctypes.c_int)
     sig = {
         "b2b_plan_create": [ctypes.POINTER(P), i32, i64, i64, i64, i64, i64, i64],
+        "b2b_chain_plan_create": [ctypes.POINTER(P), i32, i64, i64, i64, i32, ctypes.POINTER(i64)],
+        "b2b_chain_run": [P, P, ctypes.POINTER(P), P, P],
         "b2b_gemm_plan_create": [ctypes.POINTER(P), i32, i64, i64, i64, i64],
         "b2b_run": [P, P, P, P, P, P, P],
         "b2b_plan_destroy": [P],
@@ -78,6 +83,8 @@ _lib = _load()
 
 # -- raw C entry points (same names as the C ABI) ---------------------------
 b2b_plan_create = _lib.b2b_plan_create
+b2b_chain_plan_create = _lib.b2b_chain_plan_create
+b2b_chain_run = _lib.b2b_chain_run
 b2b_gemm_plan_create = _lib.b2b_gemm_plan_create
 b2b_run = _lib.b2b_run
 b2b_plan_destroy = _lib.b2b_plan_destroy
@@ -170,10 +177,13 @@ class Plan:
             for h, d in zip(host_inputs, dev_inputs):
                 d.copy_(h, non_blocking=True)
                 h2d += h.numel() * h.element_size()
-            args = list(dev_inputs) + [None] * (4 - len(dev_inputs))
-            self.run(args[0], args[1], args[2], args[3], dev_out, stream=s)
+            self._run_inputs(list(dev_inputs), dev_out, s)
             host_out.copy_(dev_out, non_blocking=True)
         return h2d, host_out.numel() * host_out.element_size()
+
+    def _run_inputs(self, inputs, D, stream):
+        args = inputs + [None] * (4 - len(inputs))
+        self.run(args[0], args[1], args[2], args[3], D, stream=stream)
 
     def status(self, stream=None) -> int:
         """Synchronise and return the device status word (0 = OK)."""
@@ -203,6 +213,37 @@ class Plan:
             self.close()
         except Exception:
             pass
+
+
+class ChainPlan(Plan):
+    """A cascade of GEMMs E = (..((A.W[0]).W[1])..).W[S-1], 1 <= S <= MAX_STAGES.
+
+    ``widths`` are the output widths N[0..S-1] of the GEMMs.
+    """
+
+    def __init__(self, dtype: str, batch: int, M: int, K: int, widths: Sequence[int]):
+        if dtype not in DTYPES:
+            raise ValueError(f"unknown dtype {dtype!r}; one of {sorted(DTYPES)}")
+        widths = tuple(int(w) for w in widths)
+        self.dtype = dtype
+        self.batch, self.M, self.K = batch, M, K
+        self.N = widths
+        h = ctypes.c_void_p()
+        arr = (ctypes.c_int64 * max(1, len(widths)))(*widths)
+        _check(_lib.b2b_chain_plan_create(ctypes.byref(h), DTYPES[dtype], batch, M, K, len(widths), arr),
+               "b2b_chain_plan_create")
+        self._h = h
+
+    def run(self, A, Ws: Sequence, D=None, stream=None):
+        """Launch on ``stream`` (default: torch's current stream); returns D."""
+        if D is None:
+            D = self.empty_out(A.device)
+        ptrs = (ctypes.c_void_p * max(1, len(Ws)))(*[_ptr(w) for w in Ws])
+        _check(_lib.b2b_chain_run(self._h, _ptr(A), ptrs, _ptr(D), _stream_handle(stream)), "b2b_chain_run")
+        return D
+
+    def _run_inputs(self, inputs, D, stream):
+        self.run(inputs[0], inputs[1:], D, stream=stream)
 
 
 class GemmPlan(Plan):

@@ -25,6 +25,8 @@
 
 using namespace b2b;
 
+static_assert(kMaxStages == B2B_MAX_STAGES, "stage limit of the C interface");
+
 namespace {
 
 constexpr uint64_t kDefaultBudgetNs = 2000000000ull;
@@ -82,12 +84,12 @@ const ChainKernelEntry* find_chain_kernel(int in, int out, int S, int n1p, int n
   return nullptr;
 }
 
-const Chain3Entry* find_chain3_kernel(int in, int out, int n1p, int n2p, int nf) {
-  const Chain3Table tables[] = {chain3_table_f16(), chain3_table_bf16()};
-  for (const Chain3Table& t : tables)
+const ChainNEntry* find_chainn_kernel(int in, int out, int nf) {
+  const ChainNTable tables[] = {chainn_table_f16(), chainn_table_bf16()};
+  for (const ChainNTable& t : tables)
     for (int i = 0; i < t.count; ++i) {
-      const Chain3Entry& e = t.entries[i];
-      if (e.in == in && e.out == out && e.n1p == n1p && e.n2p == n2p && e.nf == nf) return &e;
+      const ChainNEntry& e = t.entries[i];
+      if (e.in == in && e.out == out && e.nf == nf) return &e;
     }
   return nullptr;
 }
@@ -156,14 +158,15 @@ struct b2b_plan_s {
   int device;
   int sms;
   int stages;
-  int64_t batch, M, K, N[3];
+  int64_t batch, M, K, N[kMaxStages];
   int in_kind, out_kind, esz, osz;
   int n1p, n2p, nf;
   bool res;
   ChainParams prm;
-  // Three-stage 16-bit chains run chain3_kernel on clusters of two CTAs.
-  bool s3;
-  Chain3Params p3;
+  // Cascades of 16-bit GEMMs with three or more stages (or an intermediate
+  // wider than 256 columns) run chainn_kernel on clusters of two CTAs.
+  bool sn;
+  ChainNParams pn;
   int smem_bytes, grid, threads;
   const void* fn;
   F64Params f64;
@@ -176,8 +179,8 @@ struct b2b_plan_s {
   // Encoded tensor maps of recent runs, keyed by the pointer set (encoding
   // costs host time on every call otherwise).  Guarded by `mu`.
   struct MapSet {
-    const void* key[5];
-    alignas(64) CUtensorMap maps[5];
+    const void* key[kMaxStages + 2];
+    ChainNMaps maps;
     uint64_t stamp;
   };
   std::mutex mu;
@@ -188,28 +191,43 @@ struct b2b_plan_s {
 
 namespace {
 
-// Three-stage 16-bit chains (chain3_kernel): 256-row tiles on CTA pairs,
-// padded widths of 128 or 256, the last GEMM in passes of up to 256 columns;
-// shared memory holds the operand image of the intermediate, two staging
-// buffers, and the weight and A rings in what is left.
-b2b_status_t setup_chain3(b2b_plan_s* p) {
-  p->s3 = true;
-  p->n1p = static_cast<int>(std::max<int64_t>(128, pad_width(p->N[0])));
-  p->n2p = static_cast<int>(std::max<int64_t>(128, pad_width(p->N[1])));
-  p->nf = p->N[2] > 128 ? 256 : 128;
+// Cascades of 16-bit GEMMs on CTA pairs (chainn_kernel): 256-row tiles,
+// intermediates padded to a multiple of 128 columns (at most 512), every GEMM
+// in passes of at most 256 columns; shared memory holds the operand image of
+// the widest intermediate, two staging buffers per epilogue warp, and the
+// ring of 16 KB slots in what is left.
+b2b_status_t setup_chainn(b2b_plan_s* p) {
+  const int S = p->stages;
+  p->sn = true;
   p->res = false;
-  Chain3Params& c = p->p3;
+  ChainNParams& c = p->pn;
   std::memset(&c, 0, sizeof(c));
   c.batch = static_cast<int>(p->batch);
   c.M = static_cast<int>(p->M);
   c.K = static_cast<int>(p->K);
+  c.S = S;
   c.m_tiles = static_cast<int>((p->M + 255) / 256);
   const int64_t tiles = p->batch * c.m_tiles;
   if (tiles > (1ll << 30)) return B2B_ERR_UNSUPPORTED;
   c.total_tiles = static_cast<int>(tiles);
-  c.npass = static_cast<int>((p->N[2] + p->nf - 1) / p->nf);
-  c.kpan0 = static_cast<int>((p->K + 63) / 64);
-  const uint32_t p_bytes = 256u * static_cast<uint32_t>(std::max(p->n1p, p->n2p));
+  p->nf = p->N[S - 1] > 128 ? 256 : 128;
+  int wmax = 0;
+  c.kpan[0] = static_cast<int>((p->K + 63) / 64);
+  for (int s = 0; s < S - 1; ++s) {
+    const int w = static_cast<int>((p->N[s] + 127) / 128 * 128);
+    if (w > 512) return B2B_ERR_UNSUPPORTED;
+    c.wpad[s] = w;
+    // passes of 256 columns where they tile the width, else of 128
+    c.pw[s] = (w % 256 == 0) ? 256 : 128;
+    c.kpan[s + 1] = w / 64;
+    c.slots0 += (w / c.pw[s]) * c.kpan[s] * (s == 0 ? 2 : 1);
+    wmax = std::max(wmax, w);
+  }
+  c.pw[S - 1] = p->nf;
+  c.npass = static_cast<int>((p->N[S - 1] + p->nf - 1) / p->nf);
+  p->n1p = c.wpad[0];
+  p->n2p = S >= 3 ? c.wpad[1] : 0;
+  const uint32_t p_bytes = 256u * static_cast<uint32_t>(wmax);
   c.nstg = 2;  // two 4 KB buffers per epilogue warp
   const int64_t room = kSmemBudget - kBarBytes - int64_t(p_bytes) - int64_t(c.nstg) * kPanelBytes;
   // the rest of shared memory: ring slots of 16 KB (an A panel or a weight
@@ -223,11 +241,13 @@ b2b_status_t setup_chain3(b2b_plan_s* p) {
   p->smem_bytes = static_cast<int>(c.off_bar + kBarBytes + 1024);
   if (p->smem_bytes > kSmemOptin) return B2B_ERR_UNSUPPORTED;
   // a weight whose width is a multiple of 64 is read one 4-D box per half panel
-  c.w_merged = (p->N[0] % 64 == 0 ? 1 : 0) | (p->N[1] % 64 == 0 ? 2 : 0) | (p->N[2] % 64 == 0 ? 4 : 0);
-  const Chain3Entry* e = find_chain3_kernel(p->in_kind, p->out_kind, p->n1p, p->n2p, p->nf);
+  c.w_merged = 0;
+  for (int s = 0; s < S; ++s)
+    if (p->N[s] % 64 == 0) c.w_merged |= 1 << s;
+  const ChainNEntry* e = find_chainn_kernel(p->in_kind, p->out_kind, p->nf);
   if (!e) return B2B_ERR_UNSUPPORTED;
   p->fn = e->fn;
-  p->threads = kChain3Threads;
+  p->threads = kChainNThreads;
   // the number of co-resident clusters is known once the kernel's shared
   // memory size is set (pair_grid)
   p->grid = static_cast<int>(std::min<int64_t>(2 * tiles, p->sms & ~1));
@@ -238,8 +258,8 @@ b2b_status_t setup_chain3(b2b_plan_s* p) {
 // regions, shared-memory carve-up, and whether the weights stay resident.
 b2b_status_t setup_chain_tc(b2b_plan_s* p) {
   const int S = p->stages;
-  if (S == 3 && p->in_kind != kInTF32) return setup_chain3(p);
-  p->s3 = false;
+  if (p->in_kind != kInTF32 && (S >= 3 || (S == 2 && p->N[0] > 256))) return setup_chainn(p);
+  p->sn = false;
   const int CK = 128 / p->esz;
   const int64_t wmin = 64;
   p->n1p = S >= 2 ? static_cast<int>(pad_width(p->N[0])) : 64;
@@ -425,7 +445,7 @@ b2b_status_t pair_grid(b2b_plan_s* p) {
   // Leftover tiles (when the tiles do not divide evenly among the clusters)
   // are shared by two clusters each, one half of the last GEMM's passes
   // apiece, if that leaves no cluster idle and there are passes to share.
-  Chain3Params& c = p->p3;
+  ChainNParams& c = p->pn;
   const int64_t total = c.total_tiles;
   const int64_t ncl = std::min<int64_t>(clusters, c.npass >= 2 ? 2 * total : total);
   p->grid = 2 * static_cast<int>(ncl);
@@ -480,7 +500,7 @@ b2b_status_t setup_f64(b2b_plan_s* p) {
 
 b2b_status_t validate_sizes(b2b_dtype_t dt, int stages, int64_t batch, int64_t M, int64_t K,
                             const int64_t* N) {
-  if (batch < 0 || M < 0 || K < 1) return B2B_ERR_INVALID_ARG;
+  if (batch < 0 || M < 0 || K < 1 || stages < 1 || stages > kMaxStages) return B2B_ERR_INVALID_ARG;
   for (int s = 0; s < stages; ++s)
     if (N[s] < 1) return B2B_ERR_INVALID_ARG;
   if (batch > (1 << 24) || M > (1ll << 30) || K > (1 << 20)) return B2B_ERR_UNSUPPORTED;
@@ -492,7 +512,7 @@ b2b_status_t validate_sizes(b2b_dtype_t dt, int stages, int64_t batch, int64_t M
       if (K % 8) return B2B_ERR_UNSUPPORTED;
       for (int s = 0; s < stages; ++s) {
         if (N[s] % 8) return B2B_ERR_UNSUPPORTED;
-        if (s < stages - 1 && N[s] > 256) return B2B_ERR_UNSUPPORTED;
+        if (s < stages - 1 && N[s] > 512) return B2B_ERR_UNSUPPORTED;
         if (N[s] > 4096) return B2B_ERR_UNSUPPORTED;
       }
       return B2B_OK;
@@ -547,7 +567,7 @@ b2b_status_t create_common(b2b_plan_t* out, b2b_dtype_t dt, int stages, bool sin
   p->batch = batch;
   p->M = M;
   p->K = K;
-  for (int s = 0; s < 3; ++s) p->N[s] = s < stages ? N[s] : 0;
+  for (int s = 0; s < kMaxStages; ++s) p->N[s] = s < stages ? N[s] : 0;
   p->budget_ns = kDefaultBudgetNs;
   type_info(dt, &p->in_kind, &p->out_kind, &p->esz, &p->osz);
   if (batch == 0 || M == 0) {
@@ -567,7 +587,7 @@ b2b_status_t create_common(b2b_plan_t* out, b2b_dtype_t dt, int stages, bool sin
       cudaGetLastError();
       st = B2B_ERR_CUDA;
     }
-    if (st == B2B_OK && p->s3) st = pair_grid(p);
+    if (st == B2B_OK && p->sn) st = pair_grid(p);
   }
   if (st == B2B_OK) {
     p->d_status = nullptr;
@@ -666,7 +686,7 @@ bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
 }
 
 b2b_status_t encode_chain_maps(b2b_plan_s* p, const void* const* W, const void* A, void* D,
-                               CUtensorMap* maps) {
+                               ChainNMaps* maps) {
   const int S = p->stages;
   const CUtensorMapDataType in_dt = p->in_kind == kInF16    ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
                                     : p->in_kind == kInBF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
@@ -675,8 +695,8 @@ b2b_status_t encode_chain_maps(b2b_plan_s* p, const void* const* W, const void* 
                                      : p->out_kind == kOutBF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
                                                                : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
   const uint32_t CK = 128 / p->esz;
-  std::memset(maps, 0, 5 * sizeof(CUtensorMap));
-  b2b_status_t st = encode_3d(&maps[0], in_dt, p->esz, A, p->K, p->M, p->batch, CK, 128);
+  std::memset(maps, 0, sizeof(*maps));
+  b2b_status_t st = encode_3d(&maps->a, in_dt, p->esz, A, p->K, p->M, p->batch, CK, 128);
   int64_t kin = p->K;
   if (p->in_kind == kInTF32) {
     // the weights as transposed into the workspace ([N][K] per batch)
@@ -684,19 +704,18 @@ b2b_status_t encode_chain_maps(b2b_plan_s* p, const void* const* W, const void* 
     for (int s = 0; s < S && st == B2B_OK; ++s) {
       const uint32_t rows = s < S - 1 ? static_cast<uint32_t>(s == 0 ? p->n1p : p->n2p)
                                       : static_cast<uint32_t>(p->nf);
-      st = encode_3d(&maps[1 + s], in_dt, p->esz, dst, kin, p->N[s], p->batch, CK, rows);
+      st = encode_3d(&maps->w[s], in_dt, p->esz, dst, kin, p->N[s], p->batch, CK, rows);
       dst += p->batch * kin * p->N[s];
       kin = p->N[s];
     }
-  } else if (p->s3) {
-    // CTA pairs: each CTA loads half of a panel's 64-column blocks
-    for (int s = 0; s < 3 && st == B2B_OK; ++s) {
-      if ((p->p3.w_merged >> s) & 1) {
-        const int64_t width = s == 0 ? p->n1p : (s == 1 ? p->n2p : p->nf);
-        st = encode_w4d(&maps[1 + s], in_dt, p->esz, W[s], p->N[s], kin, p->batch, CK,
-                        static_cast<uint32_t>(width / 128));
+  } else if (p->sn) {
+    // CTA pairs: each CTA loads half of a pass's 64-column blocks
+    for (int s = 0; s < S && st == B2B_OK; ++s) {
+      if ((p->pn.w_merged >> s) & 1) {
+        st = encode_w4d(&maps->w[s], in_dt, p->esz, W[s], p->N[s], kin, p->batch, CK,
+                        static_cast<uint32_t>(p->pn.pw[s] / 128));
       } else {
-        st = encode_3d(&maps[1 + s], in_dt, p->esz, W[s], p->N[s], kin, p->batch, CK, CK);
+        st = encode_3d(&maps->w[s], in_dt, p->esz, W[s], p->N[s], kin, p->batch, CK, CK);
       }
       kin = p->N[s];
     }
@@ -706,18 +725,18 @@ b2b_status_t encode_chain_maps(b2b_plan_s* p, const void* const* W, const void* 
         // 4-D view [batch][N/64][K][64]: a whole K panel of every 64-column
         // block in one box, laid out in shared memory block after block
         const int64_t width = s < S - 1 ? (s == 0 ? p->n1p : p->n2p) : p->nf;
-        st = encode_w4d(&maps[1 + s], in_dt, p->esz, W[s], p->N[s], kin, p->batch, CK,
+        st = encode_w4d(&maps->w[s], in_dt, p->esz, W[s], p->N[s], kin, p->batch, CK,
                         static_cast<uint32_t>(width / 64));
       } else {
-        st = encode_3d(&maps[1 + s], in_dt, p->esz, W[s], p->N[s], kin, p->batch, CK, CK);
+        st = encode_3d(&maps->w[s], in_dt, p->esz, W[s], p->N[s], kin, p->batch, CK, CK);
       }
       kin = p->N[s];
     }
   }
-  for (int s = S; s < 3; ++s) maps[1 + s] = maps[1];
-  // (three-stage chains: every epilogue warp stores its own 32 rows)
+  for (int s = S; s < kMaxStages; ++s) maps->w[s] = maps->w[0];
+  // (paired chains: every epilogue warp stores its own 32 rows)
   if (st == B2B_OK)
-    st = encode_3d(&maps[4], out_dt, p->osz, D, p->N[S - 1], p->M, p->batch, 128 / p->osz, p->s3 ? 32 : 128);
+    st = encode_3d(&maps->out, out_dt, p->osz, D, p->N[S - 1], p->M, p->batch, 128 / p->osz, p->sn ? 32 : 128);
   return st;
 }
 
@@ -751,9 +770,12 @@ b2b_status_t run_chain_tc(b2b_plan_s* p, const void* const* W, const void* A, vo
       return B2B_ERR_CUDA;
     }
   }
-  alignas(64) CUtensorMap maps[5];
+  ChainNMaps maps;
   {
-    const void* key[5] = {A, W[0], S >= 2 ? W[1] : nullptr, S >= 3 ? W[2] : nullptr, D};
+    const void* key[kMaxStages + 2];
+    key[0] = A;
+    key[1] = D;
+    for (int s = 0; s < kMaxStages; ++s) key[2 + s] = s < S ? W[s] : nullptr;
     std::lock_guard<std::mutex> lock(p->mu);
     ++p->clock;
     int hit = -1, victim = 0;
@@ -762,29 +784,35 @@ b2b_status_t run_chain_tc(b2b_plan_s* p, const void* const* W, const void* A, vo
       if (p->cache[i].stamp < p->cache[victim].stamp) victim = i;
     }
     if (hit < 0) {
-      alignas(64) CUtensorMap fresh[5];
-      const b2b_status_t st = encode_chain_maps(p, W, A, D, fresh);
+      ChainNMaps fresh;
+      const b2b_status_t st = encode_chain_maps(p, W, A, D, &fresh);
       if (st != B2B_OK) return st;
       hit = p->cache_n < 8 ? p->cache_n++ : victim;
       std::memcpy(p->cache[hit].key, key, sizeof(key));
-      std::memcpy(p->cache[hit].maps, fresh, sizeof(fresh));
+      std::memcpy(&p->cache[hit].maps, &fresh, sizeof(fresh));
     }
     p->cache[hit].stamp = p->clock;
-    std::memcpy(maps, p->cache[hit].maps, sizeof(maps));
+    std::memcpy(&maps, &p->cache[hit].maps, sizeof(maps));
   }
 
-  ChainParams prm = p->prm;
-  prm.status = p->d_status;
-  prm.budget_ns = p->budget_ns;
-  prm.debug = p->debug;
-  Chain3Params prm3 = p->p3;
-  prm3.status = p->d_status;
-  prm3.budget_ns = p->budget_ns;
-  prm3.debug = p->debug;
-  void* args[6] = {&maps[0], &maps[1], &maps[2], &maps[3], &maps[4],
-                   p->s3 ? static_cast<void*>(&prm3) : static_cast<void*>(&prm)};
-  const cudaError_t e = launch_pdl(p->fn, dim3(p->grid), dim3(p->threads), args,
-                                   static_cast<size_t>(p->smem_bytes), stream, p->s3 ? 2 : 1);
+  cudaError_t e;
+  if (p->sn) {
+    ChainNParams prm = p->pn;
+    prm.status = p->d_status;
+    prm.budget_ns = p->budget_ns;
+    prm.debug = p->debug;
+    void* args[2] = {&maps, &prm};
+    e = launch_pdl(p->fn, dim3(p->grid), dim3(p->threads), args, static_cast<size_t>(p->smem_bytes),
+                   stream, 2);
+  } else {
+    ChainParams prm = p->prm;
+    prm.status = p->d_status;
+    prm.budget_ns = p->budget_ns;
+    prm.debug = p->debug;
+    void* args[6] = {&maps.a, &maps.w[0], &maps.w[1], &maps.w[2], &maps.out, &prm};
+    e = launch_pdl(p->fn, dim3(p->grid), dim3(p->threads), args, static_cast<size_t>(p->smem_bytes),
+                   stream);
+  }
   if (e != cudaSuccess) {
     cudaGetLastError();
     return B2B_ERR_CUDA;
@@ -808,9 +836,49 @@ b2b_status_t run_f64(b2b_plan_s* p, const void* A, const void* B, const void* C,
   return B2B_OK;
 }
 
+// Argument checks shared by b2b_run and b2b_chain_run, then the launch.
+b2b_status_t run_checked(b2b_plan_s* p, const void* A, const void* const* W, void* D,
+                         b2b_stream_t stream) {
+  if (p->kind == kPlanEmpty) return B2B_OK;
+  const int S = p->stages;
+  if (!A || !D) return B2B_ERR_INVALID_ARG;
+  for (int s = 0; s < S; ++s)
+    if (!W[s]) return B2B_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(A) & 15u) return B2B_ERR_ALIGNMENT;
+  for (int s = 0; s < S; ++s)
+    if (reinterpret_cast<uintptr_t>(W[s]) & 15u) return B2B_ERR_ALIGNMENT;
+  if (reinterpret_cast<uintptr_t>(D) & 15u) return B2B_ERR_ALIGNMENT;
+  const size_t e = static_cast<size_t>(p->esz);
+  const size_t dbytes = static_cast<size_t>(p->batch * p->M * p->N[S - 1]) * p->osz;
+  if (overlaps(D, dbytes, A, static_cast<size_t>(p->batch * p->M * p->K) * e)) return B2B_ERR_ALIAS;
+  int64_t kin = p->K;
+  for (int s = 0; s < S; ++s) {
+    if (overlaps(D, dbytes, W[s], static_cast<size_t>(p->batch * kin * p->N[s]) * e)) return B2B_ERR_ALIAS;
+    kin = p->N[s];
+  }
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return B2B_ERR_CUDA;
+  }
+  if (dev != p->device) return B2B_ERR_DEVICE;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (p->kind == kPlanChainF64 || p->kind == kPlanGemmF64)
+    return run_f64(p, A, W[0], S >= 2 ? W[1] : nullptr, D, st);
+  return run_chain_tc(p, W, A, D, st);
+}
+
 }  // namespace
 
 extern "C" {
+
+b2b_status_t b2b_chain_plan_create(b2b_plan_t* out, b2b_dtype_t dtype, int64_t batch, int64_t M,
+                                   int64_t K, int n_stages, const int64_t* N) {
+  if (!out) return B2B_ERR_INVALID_ARG;
+  *out = nullptr;
+  if (!N || n_stages < 1 || n_stages > kMaxStages) return B2B_ERR_INVALID_ARG;
+  return create_common(out, dtype, n_stages, n_stages == 1, batch, M, K, N);
+}
 
 b2b_status_t b2b_plan_create(b2b_plan_t* out, b2b_dtype_t dtype, int64_t batch, int64_t M,
                              int64_t K, int64_t N1, int64_t N2, int64_t N3) {
@@ -830,34 +898,19 @@ b2b_status_t b2b_run(b2b_plan_t p, const void* A, const void* B, const void* C, 
   if (!p) return B2B_ERR_INVALID_ARG;
   if (p->kind == kPlanEmpty) return B2B_OK;
   const int S = p->stages;
-  if (!A || !B || !D) return B2B_ERR_INVALID_ARG;
+  if (S > 3) return B2B_ERR_INVALID_ARG;
   if ((S >= 2) != (C != nullptr)) return B2B_ERR_INVALID_ARG;
   if ((S >= 3) != (F != nullptr)) return B2B_ERR_INVALID_ARG;
-  const void* ins[4] = {A, B, C, F};
-  for (const void* q : ins)
-    if (q && (reinterpret_cast<uintptr_t>(q) & 15u)) return B2B_ERR_ALIGNMENT;
-  if (reinterpret_cast<uintptr_t>(D) & 15u) return B2B_ERR_ALIGNMENT;
-  const size_t e = static_cast<size_t>(p->esz);
-  size_t sizes[4];
-  sizes[0] = static_cast<size_t>(p->batch * p->M * p->K) * e;
-  int64_t kin = p->K;
-  for (int s = 0; s < 3; ++s) {
-    sizes[1 + s] = s < S ? static_cast<size_t>(p->batch * kin * p->N[s]) * e : 0;
-    if (s < S) kin = p->N[s];
-  }
-  const size_t dbytes = static_cast<size_t>(p->batch * p->M * p->N[S - 1]) * p->osz;
-  for (int i = 0; i < 4; ++i)
-    if (overlaps(D, dbytes, ins[i], sizes[i])) return B2B_ERR_ALIAS;
-  int dev = -1;
-  if (cudaGetDevice(&dev) != cudaSuccess) {
-    cudaGetLastError();
-    return B2B_ERR_CUDA;
-  }
-  if (dev != p->device) return B2B_ERR_DEVICE;
-  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  if (p->kind == kPlanChainF64 || p->kind == kPlanGemmF64) return run_f64(p, A, B, C, D, s);
   const void* W[3] = {B, C, F};
-  return run_chain_tc(p, W, A, D, s);
+  return run_checked(p, A, W, D, stream);
+}
+
+b2b_status_t b2b_chain_run(b2b_plan_t p, const void* A, const void* const* W, void* D,
+                           b2b_stream_t stream) {
+  if (!p || !W) return B2B_ERR_INVALID_ARG;
+  for (int s = 0; s < p->stages; ++s)
+    if (!W[s]) return B2B_ERR_INVALID_ARG;
+  return run_checked(p, A, W, D, stream);
 }
 
 b2b_status_t b2b_plan_destroy(b2b_plan_t p) {
@@ -905,9 +958,9 @@ b2b_status_t b2b_plan_info(b2b_plan_t p, int* launches, int* grid, int* threads,
   if (grid) *grid = p->grid;
   if (threads) *threads = p->threads;
   if (smem) *smem = p->smem_bytes;
-  if (tmem_cols) *tmem_cols = !tc ? 0 : (p->s3 ? 512 : static_cast<int>(p->prm.tmem_cols));
-  if (ring_stages) *ring_stages = !tc ? 0 : (p->s3 ? p->p3.nslot : p->prm.nst);
-  if (passes) *passes = !tc ? 1 : (p->s3 ? p->p3.npass : p->prm.npass);
+  if (tmem_cols) *tmem_cols = !tc ? 0 : (p->sn ? 512 : static_cast<int>(p->prm.tmem_cols));
+  if (ring_stages) *ring_stages = !tc ? 0 : (p->sn ? p->pn.nslot : p->prm.nst);
+  if (passes) *passes = !tc ? 1 : (p->sn ? p->pn.npass : p->prm.npass);
   return B2B_OK;
 }
 
@@ -1029,7 +1082,7 @@ b2b_status_t noalloc_scratch(int dev, void** out) {
 extern "C" b2b_status_t b2b_run_tf32_noalloc(int64_t batch, int64_t M, int64_t K, int64_t N1,
                                              int64_t N2, const void* A, const void* B,
                                              const void* C, void* D, b2b_stream_t stream) {
-  const int64_t N[3] = {N1, N2, 0};
+  const int64_t N[2] = {N1, N2};
   b2b_status_t st = validate_sizes(B2B_TF32, 2, batch, M, K, N);
   if (st != B2B_OK) return st;
   if (batch == 0 || M == 0) return B2B_OK;
@@ -1053,9 +1106,9 @@ extern "C" b2b_status_t b2b_run_tf32_noalloc(int64_t batch, int64_t M, int64_t K
   pl.batch = batch;
   pl.M = M;
   pl.K = K;
+  for (int s = 0; s < kMaxStages; ++s) pl.N[s] = 0;
   pl.N[0] = N1;
   pl.N[1] = N2;
-  pl.N[2] = 0;
   pl.budget_ns = kDefaultBudgetNs;
   pl.debug = 0;
   pl.d_status = nullptr;

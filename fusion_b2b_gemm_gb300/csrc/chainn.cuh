@@ -1,0 +1,545 @@
+// A cascade of S GEMMs (2 <= S <= 8) with 16-bit operands on pairs of SMs
+// (tcgen05, cta_group::2, sm_103a):
+//
+//   P_1 = A.W_0 -> round -> P_2 = P_1.W_1 -> round -> ... -> E = P_{S-1}.W_{S-1}
+//
+// Source of the method: patent "数据处理方法、装置、设备及介质" (Alibaba, 2023),
+// Detailed description para. 41 (several cascaded operators, each one's
+// output the next one's input), para. 54-60 (the result of one operator is
+// rearranged and handed to the next without going through memory) and
+// para. 103-110 (rearrangement through shared memory).
+//
+// Every weight is streamed through the SMs once per 256-row tile, so the
+// weights, not A, dominate the bytes an SM must load.  Two CTAs of a cluster
+// share each MMA (M = 256): each holds its own 128 rows of A, of the
+// intermediates and of every accumulator, and half of the columns of every
+// weight panel, which halves the weight traffic and the shared memory a
+// weight slot needs per SM.  The converters turn an accumulator row into the
+// K-major 128-byte-swizzled operand image of the next GEMM in shared memory
+// (one image, overwritten stage after stage).
+//
+// Every GEMM runs in passes of at most 256 output columns.  Tensor memory
+// (512 columns) holds two 256-column regions, X and Y.  An intermediate of
+// at most 256 columns takes the region not used last, so a GEMM writes one
+// region while the converters still read the other, and starts on the first
+// 128-column chunk of its operand image as soon as that chunk is written.
+// A wider intermediate (up to 512 columns) takes both regions; the next GEMM
+// then starts once the converters have freed X.  The passes of the last GEMM
+// alternate between the regions, so the epilogue of one pass overlaps the
+// MMAs of the next.  Whether a region is free is counted by one barrier per
+// region that its reader (the converters or the epilogue) releases.
+//
+// Roles (384 threads, one CTA per SM, persistent over 256-row tiles):
+//   warp 0     producer: one ring of 16 KB slots in the order the MMAs read
+//              them (the first GEMM: an A panel and this CTA's half of a
+//              weight panel; every later GEMM: a weight half panel)
+//   warp 1     TMEM allocation (both CTAs); the even CTA's lane 0 issues MMAs
+//   warps 2-9  converters (accumulator -> operand image), half of each
+//              128-column chunk for each of the two warps that share a TMEM
+//              lane quadrant
+//   warps 6-9  also the epilogue (accumulator -> output type -> staging ->
+//              TMA store, each warp its own 32 rows)
+//   warp 11    slot watcher (even CTA): waits for every slot's copies in
+//              the MMAs' order and publishes the count in shared memory,
+//              which the MMA thread polls at a fraction of the cost of an
+//              mbarrier wait (the tensor pipe queues only about two MMAs, so
+//              the MMA thread's own waits would leave it idle)
+// Every wait is bounded; after an abort the converter and epilogue loops are
+// still walked to the end with the work skipped, so that named barriers stay
+// matched, and the two CTAs meet at a cluster barrier before exit.
+#pragma once
+
+#include "chain_tc.cuh"
+
+namespace b2b {
+
+constexpr int kMaxStages = 8;
+
+// Barrier slots (8 bytes each) at ChainNParams::off_bar.
+enum : int {
+  knFull = 0,        // [16] ring slot filled (even CTA's: armed by it for both CTAs' copies)
+  knEmpty = 16,      // [16] ring slot consumed
+  knCFull = 32,      // an intermediate GEMM complete (all its passes): converters
+  knPChunk = 33,     // [2][4] 128-column chunk c of intermediate k's operand image
+                     //        (set k & 1) written in both CTAs (even CTA's)
+  knRFull = 41,      // [2] X / Y holds a pass of the last GEMM (epilogue)
+  knREmpty = 43,     // [2] X / Y read in both CTAs, by the converters or the
+                     //     epilogue (even CTA's)
+  knDrain = 45,      // every MMA complete (exit)
+  knSlotTmem = 46,   // uint32 TMEM base, then the int abort flag
+  knSlotReady = 47,  // uint32: ring slots whose copies have landed (even CTA)
+};
+
+constexpr int kChainNThreads = 384;
+
+struct ChainNParams {
+  int batch, M, K;
+  int S;                     // GEMMs in the cascade
+  int m_tiles, total_tiles;  // 256-row tiles per batch, in all
+  int wpad[kMaxStages];      // intermediate s < S-1: padded width (128, 256, 384 or 512)
+  int pw[kMaxStages];        // pass width: 128 or 256 (intermediates), NF (last GEMM)
+  int kpan[kMaxStages];      // 64-element K panels GEMM s reads
+  int npass;                 // NF-column passes of the last GEMM
+  int slots0;                // ring slots of the intermediate GEMMs of one tile
+  int nslot, nstg;           // ring slots (16 KB each) and staging buffers per warp
+  uint32_t off_ring, off_p, off_stg, off_bar;
+  int w_merged;              // bit s: weight s is read as one 4-D box per half panel
+  int split;                 // leftover tiles whose passes are split between two clusters
+  uint32_t debug;            // test support: bit 0 = the first ring slot is never filled
+  int* status;
+  unsigned long long budget_ns;
+};
+
+// Tensor maps of one run: A, the output, and every weight.
+struct ChainNMaps {
+  CUtensorMap a, out;
+  CUtensorMap w[kMaxStages];
+};
+
+// Work units of a cluster.  Tiles are dealt to the clusters in strides; when
+// they do not divide evenly, the `split` leftover tiles are each shared by two
+// clusters, one taking the first half of the last GEMM's passes and the other
+// the rest (both compute the intermediates), and these half units come first.
+// That shortens the longest cluster's work and starts half of the clusters
+// out of step with the others, which spreads their HBM-bound first GEMMs.
+struct ChainNUnit {
+  int b, mt, p0, p1;  // batch, 256-row tile, passes [p0, p1) of the last GEMM
+};
+__device__ __forceinline__ int chainn_units(const ChainNParams& p, int cid, int ncl) {
+  if (p.split > 0) return p.total_tiles / ncl + (cid < 2 * p.split ? 1 : 0);
+  return cid < p.total_tiles ? (p.total_tiles - cid + ncl - 1) / ncl : 0;
+}
+__device__ __forceinline__ ChainNUnit chainn_unit(const ChainNParams& p, int cid, int ncl, int i) {
+  int tile, p0 = 0, p1 = p.npass;
+  if (p.split > 0 && cid < 2 * p.split) {
+    if (i == 0) {
+      tile = (p.total_tiles / ncl) * ncl + (cid >> 1);
+      const int h = (p.npass + 1) / 2;
+      p0 = (cid & 1) ? h : 0;
+      p1 = (cid & 1) ? p.npass : h;
+    } else {
+      tile = cid + (i - 1) * ncl;
+    }
+  } else {
+    tile = cid + i * ncl;
+  }
+  ChainNUnit u;
+  u.b = tile / p.m_tiles;
+  u.mt = tile - u.b * p.m_tiles;
+  u.p0 = p0;
+  u.p1 = p1;
+  return u;
+}
+
+// Tensor-memory placement, walked identically by the MMA thread, the
+// converters and the epilogue: an accumulator of at most 256 columns takes
+// the region not used last; a wider one starts at column 0 and covers both,
+// and the region after it is X (freed first).
+struct RegionCursor {
+  int last = 1;
+  __device__ __forceinline__ uint32_t take(int width) {
+    if (width <= 256) {
+      last ^= 1;
+      return static_cast<uint32_t>(last) * 256u;
+    }
+    last = 1;
+    return 0u;
+  }
+};
+
+template <int IN, int OUT, int NF>
+__global__ void __launch_bounds__(kChainNThreads, 1)
+    chainn_kernel(const __grid_constant__ ChainNMaps maps, const __grid_constant__ ChainNParams p) {
+  using namespace ptx;
+  static_assert(IN == kInF16 || IN == kInBF16, "16-bit operands");
+  static_assert(NF == 128 || NF == 256, "pass width of the last GEMM");
+  constexpr int CG = 2;
+  constexpr int CK = 64;           // K elements per 128-byte panel
+  constexpr int KSTEP = 16;        // K of one MMA
+  constexpr int WBOX_N = 64;       // weight columns per 128-byte block
+  constexpr int WBOX_BYTES = CK * 128;
+  constexpr int OSZ = (OUT == kOutF32) ? 4 : 2;
+  constexpr int OBOX_N = 128 / OSZ;
+  constexpr uint32_t FMT = (IN == kInF16) ? 0u : 1u;
+  constexpr uint32_t kCols = 512;
+
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* gbase = smem_raw + (base - raw);
+  const uint32_t bar0 = base + p.off_bar;
+  auto bar = [&](int i) -> uint32_t { return bar0 + 8u * static_cast<uint32_t>(i); };
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + p.off_bar + 8 * knSlotTmem);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();
+  const bool leader = (rank == 0);
+  const int S = p.S;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < 16; ++i) {
+      mbar_init(bar(knFull + i), 1);
+      mbar_init(bar(knEmpty + i), 1);
+    }
+    mbar_init(bar(knCFull), 1);
+    for (int i = 0; i < 8; ++i) mbar_init(bar(knPChunk + i), 2);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(bar(knRFull + i), 1);
+      mbar_init(bar(knREmpty + i), 2);
+    }
+    mbar_init(bar(knDrain), 1);
+    *abort_flag = 0;
+    *reinterpret_cast<volatile uint32_t*>(gbase + p.off_bar + 8 * knSlotReady) = 0u;
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc<CG>(smem_u32(tmem_slot), kCols);
+    tmem_relinquish<CG>();
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();  // the peer's barriers exist before anything arrives on them
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  grid_launch_dependents();
+  grid_dependency_wait();
+
+  BoundedWait bw{abort_flag, p.status, p.budget_ns, kTimeoutCode};
+  // Waits on barriers that threads of the peer CTA arrive on (the same
+  // default-scope wait: the remote arrives are ordered by the barrier itself).
+  BoundedWait bwm = bw;
+  auto lbar = [&](int i) -> uint32_t { return mapa_shared(bar(i), 0); };
+
+  // Work units (256-row tiles, or halves of their last GEMM) of this
+  // cluster; this CTA's 128 rows of each.
+  const int cid = static_cast<int>(blockIdx.x >> 1);
+  const int ncl = static_cast<int>(gridDim.x >> 1);
+  const int t_count = chainn_units(p, cid, ncl);
+  auto row0 = [&](int mt) -> int { return mt * 256 + static_cast<int>(rank) * 128; };
+  const uint32_t p_img = base + p.off_p;
+  const int kpan_last = p.kpan[S - 1];
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      prefetch_tmap(&maps.a);
+      prefetch_tmap(&maps.out);
+      for (int s = 0; s < S; ++s) prefetch_tmap(&maps.w[s]);
+      uint32_t slot = 0, phase = 0;
+      uint64_t issued = 0;
+      bool ok = true;
+      // one ring slot: an A panel (s < 0) or this CTA's half of a weight panel
+      auto load = [&](int s, int b, int m0, int kb, int col0, int pw) -> bool {
+        if (!bw.wait(bar(knEmpty + slot), phase ^ 1u)) return false;
+        const uint32_t dst = base + p.off_ring + slot * static_cast<uint32_t>(kPanelBytes);
+        const uint32_t fb = lbar(knFull + slot);
+        const int wcols = pw / 2;
+        const uint32_t bytes = s < 0 ? static_cast<uint32_t>(kPanelBytes) : 128u * static_cast<uint32_t>(wcols);
+        // Only the even CTA arms its barrier, for both CTAs' copies; the odd
+        // CTA's copies may land first (the transaction count then dips
+        // below zero until the arming, which the barrier allows).
+        if (leader) mbar_arrive_expect_tx(bar(knFull + slot), 2u * bytes);
+        // test support: the very first slot is armed but never filled
+        if (!((p.debug & 1u) && issued == 0)) {
+          if (s < 0) {
+            tma_load_3d_pair(dst, &maps.a, fb, kb * CK, m0, b);
+          } else {
+            const CUtensorMap* wm = &maps.w[s];
+            const int n0 = col0 + static_cast<int>(rank) * wcols;
+            if ((p.w_merged >> s) & 1) {
+              tma_load_4d_pair(dst, wm, fb, 0, kb * CK, n0 / WBOX_N, b);
+            } else {
+              for (int j = 0; j < wcols / WBOX_N; ++j)
+                tma_load_3d_pair(dst + j * WBOX_BYTES, wm, fb, n0 + j * WBOX_N, kb * CK, b);
+            }
+          }
+        }
+        ++issued;
+        if (++slot == static_cast<uint32_t>(p.nslot)) {
+          slot = 0;
+          phase ^= 1u;
+        }
+        return true;
+      };
+      for (int it = 0; it < t_count && ok; ++it) {
+        const ChainNUnit c = chainn_unit(p, cid, ncl, it);
+        const int m0 = row0(c.mt);
+        // the ring reaches only a few panels into the next unit's first
+        // GEMM: pull the next unit's A into L2 now
+        if (it + 1 < t_count) {
+          const ChainNUnit n = chainn_unit(p, cid, ncl, it + 1);
+          for (int q = 0; q < p.kpan[0]; ++q) tma_prefetch_l2_3d(&maps.a, q * CK, row0(n.mt), n.b);
+        }
+        for (int s = 0; s < S - 1 && ok; ++s) {
+          const int pw = p.pw[s];
+          for (int col0 = 0; col0 < p.wpad[s] && ok; col0 += pw)
+            for (int kb = 0; kb < p.kpan[s] && ok; ++kb) {
+              if (s == 0) ok = load(-1, c.b, m0, kb, 0, 0);
+              if (ok) ok = load(s, c.b, m0, kb, col0, pw);
+            }
+        }
+        for (int j = c.p0; j < c.p1 && ok; ++j)
+          for (int kb = 0; kb < kpan_last && ok; ++kb) ok = load(S - 1, c.b, m0, kb, j * NF, NF);
+      }
+      // copies in flight land before exit (the even CTA's barriers count both
+      // CTAs' copies; the odd CTA waits at the cluster barrier before exit)
+      const uint64_t n = static_cast<uint64_t>(p.nslot);
+      const uint64_t tail = !leader ? 0 : (issued < n ? issued : n);
+      for (uint64_t j = 0; j < tail; ++j) {
+        const uint64_t idx = issued - 1 - j;
+        drain_wait(bar(knFull + static_cast<int>(idx % n)), static_cast<uint32_t>((idx / n) & 1u),
+                   p.budget_ns);
+      }
+    }
+  } else if (warp == 11) {
+    // ------------------------------------------- slot watcher (even CTA)
+    if (lane == 0 && leader) {
+      uint32_t slot = 0, phase = 0, n = 0;
+      const uint32_t ready = bar(knSlotReady);
+      bool ok = true;
+      for (int it = 0; it < t_count && ok; ++it) {
+        const ChainNUnit c = chainn_unit(p, cid, ncl, it);
+        const int per_unit = p.slots0 + (c.p1 - c.p0) * kpan_last;
+        for (int q = 0; q < per_unit && ok; ++q) {
+          ok = bw.wait(bar(knFull + slot), phase);
+          if (!ok) break;
+          if (++slot == static_cast<uint32_t>(p.nslot)) {
+            slot = 0;
+            phase ^= 1u;
+          }
+          st_release_shared(ready, ++n);
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------- MMA (even CTA, lane 0)
+    if (lane == 0 && leader) {
+      uint32_t slot = 0;
+      uint32_t ux = 0, uy = 0;  // products written to X / Y so far
+      bool ok = true;
+      // region r's previous product has been read in both CTAs
+      auto take_region = [&](int r) -> bool {
+        const uint32_t ur = r ? uy : ux;
+        const bool done = ur == 0 || bwm.wait(bar(knREmpty + r), (ur - 1u) & 1u);
+        if (r) ++uy; else ++ux;
+        return done;
+      };
+      // the next `need` slots have landed once the watcher's count reaches
+      // consumed + need
+      uint32_t consumed = 0, seen = 0;
+      const uint32_t ready = bar(knSlotReady);
+      auto stage_ready = [&](uint32_t need) -> bool {
+        if (seen >= consumed + need) return true;
+        seen = ld_acquire_shared(ready);
+        if (seen >= consumed + need) return true;
+        const uint64_t t0 = globaltimer_ns();
+        for (;;) {
+          for (int i = 0; i < 32; ++i) {
+            seen = ld_acquire_shared(ready);
+            if (seen >= consumed + need) return true;
+          }
+          if (*abort_flag) return false;
+          if (globaltimer_ns() - t0 > p.budget_ns) {
+            bw.raise();
+            return false;
+          }
+        }
+      };
+      // Four MMAs over one 64-element K panel.  First GEMM (a_smem): the A
+      // panel is in this slot and the weight half panel in the next; later
+      // GEMMs read K panel kb of the operand image, after waiting for the
+      // chunk barrier `chunk` (if >= 0) with parity cpar.
+      auto stage_mmas = [&](uint32_t d, uint32_t idesc, bool a_smem, int kb, int chunk,
+                            uint32_t cpar) -> bool {
+        const uint32_t need = a_smem ? 2u : 1u;
+        if (!stage_ready(need)) return false;
+        if (chunk >= 0 && !bwm.wait(bar(chunk), cpar)) return false;
+        consumed += need;
+        tc_fence_after();
+        const uint32_t s0 = slot;
+        const uint32_t s1 = a_smem ? (slot + 1u == static_cast<uint32_t>(p.nslot) ? 0u : slot + 1u) : slot;
+        const uint32_t wb = base + p.off_ring + s1 * static_cast<uint32_t>(kPanelBytes);
+        const uint32_t sa = a_smem ? base + p.off_ring + s0 * static_cast<uint32_t>(kPanelBytes)
+                                   : p_img + static_cast<uint32_t>(kb) * kPanelBytes;
+        const uint32_t acc0 = kb != 0 ? 1u : 0u;
+#pragma unroll
+        for (int kk = 0; kk < CK / KSTEP; ++kk)
+          mma_ss<false, CG>(d, desc_sw128(sa + kk * 32u, 16u, 1024u),
+                            desc_sw128(wb + kk * KSTEP * 128u, WBOX_BYTES, 1024u), idesc, kk ? 1u : acc0);
+        tc_commit<CG>(bar(knEmpty + s0));
+        if (a_smem) tc_commit<CG>(bar(knEmpty + s1));
+        slot = s1 + 1u == static_cast<uint32_t>(p.nslot) ? 0u : s1 + 1u;
+        return true;
+      };
+      // the K panels of GEMM s > 0 from kb on need chunk kb / 2 of the
+      // previous intermediate (global index k - 1), on its first pass only
+      RegionCursor rc;
+      uint32_t k = 0;  // intermediates started so far
+      auto chunk_of = [&](bool first_pass, int kb) -> int {
+        if (!first_pass || (kb & 1)) return -1;
+        return knPChunk + static_cast<int>(((k - 1u) & 1u) * 4u) + kb / 2;
+      };
+      for (int it = 0; it < t_count && ok; ++it) {
+        const ChainNUnit c = chainn_unit(p, cid, ncl, it);
+        for (int s = 0; s < S - 1 && ok; ++s) {
+          const int pw = p.pw[s];
+          const uint32_t cbase = rc.take(p.wpad[s]);
+          const uint32_t idesc = make_idesc(FMT, static_cast<uint32_t>(pw), 256u, true);
+          const uint32_t cpar = ((k - 1u) >> 1) & 1u;
+          int touched = 0;
+          for (int col0 = 0; col0 < p.wpad[s] && ok; col0 += pw) {
+            const uint32_t col = cbase + static_cast<uint32_t>(col0);
+            const int r = static_cast<int>(col >> 8);
+            if (!((touched >> r) & 1)) {
+              touched |= 1 << r;
+              ok = take_region(r);
+              if (!ok) break;
+              tc_fence_after();
+            }
+            for (int kb = 0; kb < p.kpan[s] && ok; ++kb)
+              ok = stage_mmas(tmem_base + col, idesc, s == 0, kb, s == 0 ? -1 : chunk_of(col0 == 0, kb), cpar);
+          }
+          if (!ok) break;
+          tc_commit<CG>(bar(knCFull));
+          ++k;
+        }
+        if (!ok) break;
+        // the unit's passes of the last GEMM, each in the next region
+        const uint32_t idesc = make_idesc(FMT, NF, 256u, true);
+        const uint32_t cpar = ((k - 1u) >> 1) & 1u;
+        for (int j = c.p0; j < c.p1 && ok; ++j) {
+          const uint32_t col = rc.take(NF);
+          const int r = static_cast<int>(col >> 8);
+          ok = take_region(r);
+          if (!ok) break;
+          tc_fence_after();
+          for (int kb = 0; kb < kpan_last && ok; ++kb)
+            ok = stage_mmas(tmem_base + col, idesc, false, kb, chunk_of(j == c.p0, kb), cpar);
+          if (!ok) break;
+          tc_commit<CG>(bar(knRFull + r));
+        }
+      }
+      tc_commit<CG>(bar(knDrain));
+      drain_wait(bar(knDrain), 0, p.budget_ns);
+    }
+  } else if (warp >= 2 && warp < 10) {
+    // ----------------------------------------- converters (warps 2-9) and
+    // ---------------------------------------------------- epilogue (6-9)
+    // Every tile: each intermediate accumulator into the operand image, in
+    // 128-column chunks, by all eight warps (warp w reads TMEM lanes
+    // 32 (w % 4) .. + 31; warps 2-5 take the low 64 columns of a chunk,
+    // warps 6-9 the high 64), then warps 6-9 store the passes of the last
+    // GEMM.  An intermediate's completion barrier also means that every
+    // earlier MMA, and so every read of the image it overwrites, is done.
+    const int q = warp & 3;
+    const int row = q * 32 + lane;
+    const int h = warp < 6 ? 0 : 1;
+    const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
+    const bool epi = (warp >= 6);
+    // epilogue: each warp converts and stores its own 32 rows (boxes of 32
+    // rows x 128 bytes) through two staging buffers of its own, so the warps
+    // never wait for each other except once per pass, when the region has
+    // been read
+    const uint32_t wstg = base + p.off_stg + static_cast<uint32_t>(q) * 2u * 4096u;
+    const bool elected = (warp == 6 && lane == 0);
+    constexpr int NBOX = NF / OBOX_N;
+    constexpr int LDS = OBOX_N / 32;
+    RegionCursor rc;
+    uint32_t k = 0;          // intermediates converted so far
+    uint32_t krx = 0, kry = 0;  // last-GEMM passes read from X / Y so far
+    uint32_t nbox = 0;
+    bool ok = true;
+    for (int it = 0; it < t_count; ++it) {
+      const ChainNUnit c = chainn_unit(p, cid, ncl, it);
+      for (int s = 0; s < S - 1; ++s) {
+        const uint32_t cbase = rc.take(p.wpad[s]);
+        if (ok) ok = warp_wait(bw, bar(knCFull), k & 1u);
+        if (ok) tc_fence_after();
+        const int nch = p.wpad[s] / 128;
+        for (int ch = 0; ch < nch; ++ch) {
+          const int pcol = ch * 128 + h * 64;
+          if (ok) {
+            rearrange_accumulator<IN>(tmem_base + lane_off + cbase + static_cast<uint32_t>(pcol), 64, row,
+                                      p_img + static_cast<uint32_t>(pcol / 64) * kPanelBytes);
+            tc_fence_before();
+          }
+          named_bar_sync(2, 256);
+          if (warp == 2 && lane == 0 && ok) {
+            // every chunk barrier of the set completes once per intermediate
+            // (the MMA thread derives its parities from that): after the last
+            // chunk, the ones this width does not use complete too
+            const int set = knPChunk + static_cast<int>((k & 1u) * 4u);
+            mbar_arrive_cluster(lbar(set + ch));
+            if (ch + 1 == nch)
+              for (int c2 = nch; c2 < 4; ++c2) mbar_arrive_cluster(lbar(set + c2));
+            // the chunk was the last one in its region: the region is free
+            const uint32_t r = (cbase + static_cast<uint32_t>(ch * 128)) >> 8;
+            if (ch + 1 == nch || ((cbase + static_cast<uint32_t>(ch * 128 + 128)) >> 8) != r)
+              mbar_arrive_cluster(lbar(knREmpty + static_cast<int>(r)));
+          }
+        }
+        ++k;
+      }
+      const int mw = row0(c.mt) + q * 32;  // this warp's first row
+      for (int j = c.p0; j < c.p1; ++j) {
+        const uint32_t col = rc.take(NF);
+        if (!epi) continue;
+        const int r = static_cast<int>(col >> 8);
+        if (ok) ok = warp_wait(bw, bar(knRFull + r), (r ? kry : krx) & 1u);
+        if (r) ++kry; else ++krx;
+        tc_fence_after();
+        const uint32_t tsrc = tmem_base + lane_off + col;
+        uint32_t v[LDS][32];
+        if (ok) {
+#pragma unroll
+          for (int l = 0; l < LDS; ++l) tmem_ld32(tsrc + static_cast<uint32_t>(l * 32), v[l]);
+        }
+#pragma unroll 1
+        for (int x = 0; x < NBOX; ++x) {
+          const uint32_t stg = wstg + (nbox & 1u) * 4096u;
+          // the store issued two boxes ago (same buffer) has read it
+          if (lane == 0 && ok) bulk_wait_read<1>();
+          __syncwarp();
+          if (ok) {
+            tmem_wait_ld();
+#pragma unroll
+            for (int l = 0; l < LDS; ++l) store_output_row<OUT>(stg, lane, l * 32, v[l]);
+            fence_proxy_async_smem();
+            if (x + 1 < NBOX) {
+#pragma unroll
+              for (int l = 0; l < LDS; ++l)
+                tmem_ld32(tsrc + static_cast<uint32_t>((x + 1) * OBOX_N + l * 32), v[l]);
+            }
+          }
+          if (x == NBOX - 1) {
+            // every warp has read the region: one arrival per CTA on the even CTA
+            if (ok) tc_fence_before();
+            named_bar_sync(1, 128);
+            if (elected && ok) mbar_arrive_cluster(lbar(knREmpty + r));
+          }
+          __syncwarp();
+          // (the odd CTA's rows of the last tile may lie past M)
+          if (lane == 0 && ok && mw < p.M) {
+            tma_store_3d(&maps.out, stg, j * NF + x * OBOX_N, mw, c.b);
+            bulk_commit();
+          }
+          ++nbox;
+        }
+      }
+    }
+    if (epi && lane == 0) bulk_wait_all();
+  }
+
+  __syncthreads();
+  // neither CTA leaves (or frees tensor memory) while the other may still
+  // arrive on its barriers or the even CTA's MMAs may still write it
+  cluster_sync();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc<CG>(tmem_base, kCols);
+  }
+}
+
+}  // namespace b2b

@@ -3,7 +3,7 @@
 // table; the plan picks the entry that matches the padded widths it chose.
 #pragma once
 
-#include "chain3.cuh"
+#include "chainn.cuh"
 #include "chain_tc.cuh"
 
 namespace b2b {
@@ -23,21 +23,22 @@ ChainTable chain_table_f16();
 ChainTable chain_table_bf16();
 ChainTable chain_table_tf32();
 
-// Three-stage 16-bit chains (chain3_kernel, CTA pairs).
-struct Chain3Entry {
-  int in, out, n1p, n2p, nf;
+// Cascades of 16-bit GEMMs on CTA pairs (chainn_kernel): three or more
+// stages, or two with an intermediate wider than 256 columns.
+struct ChainNEntry {
+  int in, out, nf;
   const void* fn;
 };
-struct Chain3Table {
-  const Chain3Entry* entries;
+struct ChainNTable {
+  const ChainNEntry* entries;
   int count;
 };
-Chain3Table chain3_table_f16();
-Chain3Table chain3_table_bf16();
+ChainNTable chainn_table_f16();
+ChainNTable chainn_table_bf16();
 
 }  // namespace b2b
 
 #define B2B_CHAIN_ENTRY(IN, OUT, S, A, B, F, R) \
   { IN, OUT, S, A, B, F, R, reinterpret_cast<const void*>(&::b2b::chain_tc_kernel<IN, OUT, S, A, B, F, R>) }
-#define B2B_CHAIN3_ENTRY(IN, OUT, A, B, F) \
-  { IN, OUT, A, B, F, reinterpret_cast<const void*>(&::b2b::chain3_kernel<IN, OUT, A, B, F>) }
+#define B2B_CHAINN_ENTRY(IN, OUT, F) \
+  { IN, OUT, F, reinterpret_cast<const void*>(&::b2b::chainn_kernel<IN, OUT, F>) }

@@ -3,6 +3,7 @@
  *
  *   D = (A.B).C              (two cascaded GEMMs)
  *   E = ((A.B).C).F          (three cascaded GEMMs)
+ *   E = (..((A.W0).W1)..).W[S-1]   (S cascaded GEMMs, S <= B2B_MAX_STAGES)
  *
  * The method is the one of patent "数据处理方法、装置、设备及介质"
  * (Alibaba, 2023): two (or three) cascaded operators are fused so that the
@@ -10,7 +11,8 @@
  * held in the layout of the accumulator ("first data processing rule"), is
  * rearranged on chip into the operand layout operator 2 reads ("second data
  * processing rule") and handed straight to operator 2 (Detailed description
- * para. 35-37, steps 101-103; para. 54-60; three operators: para. 41).
+ * para. 35-37, steps 101-103; para. 54-60; more than two operators, each
+ * one's output the next one's input: para. 41).
  * The apparatus splits this into an operator-determination module, a
  * relation-determination module and a rearrangement module (para. 140-143,
  * Fig. 5); here b2b_plan_create plays the first two (the caller names the
@@ -43,6 +45,8 @@ extern "C" {
 #endif
 
 typedef struct b2b_plan_s* b2b_plan_t;
+/* Most GEMMs one plan chains (b2b_chain_plan_create). */
+#define B2B_MAX_STAGES 8
 /* A cudaStream_t (NULL = the legacy default stream). */
 typedef struct CUstream_st* b2b_stream_t;
 
@@ -78,8 +82,10 @@ typedef enum {
  *   N1, N2   output widths of GEMM1 and GEMM2.
  *   N3       output width of GEMM3, or 0 for a two-stage chain.
  * Sizes this build supports (otherwise B2B_ERR_UNSUPPORTED):
- *   16-bit types: K % 8 == 0; N1, N2 (and N3) % 8 == 0; N1, N2 <= 256;
- *                 N3 <= 4096 (the last GEMM runs in passes of up to 256).
+ *   16-bit types: K % 8 == 0; N1, N2 (and N3) % 8 == 0; intermediate
+ *                 widths (N1, and N2 of a three-stage chain) <= 512; the
+ *                 last width <= 4096 (the last GEMM runs in passes of up to
+ *                 256 columns).
  *   B2B_TF32:     two stages; K % 4 == 0; N1 <= 256; N1, N2 % 4 == 0.
  *   B2B_F64:      two stages; K % 4 == 0; N1, N2 in {16, 32, 64}.
  * Binds to the current CUDA device, which must be an sm_103 GPU
@@ -88,6 +94,23 @@ typedef enum {
  */
 b2b_status_t b2b_plan_create(b2b_plan_t* out, b2b_dtype_t dtype, int64_t batch, int64_t M,
                              int64_t K, int64_t N1, int64_t N2, int64_t N3);
+
+/*
+ * Create a plan for a cascade of n_stages GEMMs, 1 <= n_stages <= B2B_MAX_STAGES
+ * (patent para. 41: the output of each operator is the input of the next):
+ *   E = (..((A.W[0]).W[1])..).W[n_stages-1],
+ * with A[batch][M][K], W[s][batch][N[s-1]][N[s]] (N[-1] = K) and the output
+ * E[batch][M][N[n_stages-1]], rounded as described above between GEMMs.
+ *   N        n_stages output widths (host array, read during the call).
+ * Supported sizes are those of b2b_plan_create, for every intermediate
+ * width N[0..n_stages-2] (16-bit types: any n_stages; B2B_TF32 and B2B_F64:
+ * n_stages <= 2).  n_stages == 1 gives the single-GEMM plan of
+ * b2b_gemm_plan_create; 2 or 3 give the plans of b2b_plan_create.  Run the
+ * plan with b2b_chain_run (or, for at most three stages, b2b_run).
+ * Returns B2B_ERR_INVALID_ARG for a null `out` or `N`, or n_stages out of range.
+ */
+b2b_status_t b2b_chain_plan_create(b2b_plan_t* out, b2b_dtype_t dtype, int64_t batch, int64_t M,
+                                   int64_t K, int n_stages, const int64_t* N);
 
 /*
  * A single GEMM D = A.B (one operator, no fusion), used to build the unfused
@@ -109,10 +132,20 @@ b2b_status_t b2b_gemm_plan_create(b2b_plan_t* out, b2b_dtype_t dtype, int64_t ba
  * Returns B2B_ERR_CUDA if the launch fails.  A kernel that gives up a
  * bounded wait records B2B_ERR_TIMEOUT in the plan's status word, which
  * b2b_plan_device_status reports.  Runs on one plan from several streams
- * may overlap: the plan is not modified by b2b_run.
+ * may overlap: the plan is not modified by b2b_run.  A plan of more than
+ * three stages is rejected (B2B_ERR_INVALID_ARG): use b2b_chain_run.
  */
 b2b_status_t b2b_run(b2b_plan_t plan, const void* A, const void* B, const void* C, const void* F,
                      void* D, b2b_stream_t stream);
+
+/*
+ * Run any plan asynchronously on `stream`: W is a host array of the plan's
+ * n_stages device weight pointers (read during the call), `out` the device
+ * output [batch][M][N_last].  Pointer rules, errors and the status word are
+ * those of b2b_run; a null W or a null entry in it is B2B_ERR_INVALID_ARG.
+ */
+b2b_status_t b2b_chain_run(b2b_plan_t plan, const void* A, const void* const* W, void* out,
+                           b2b_stream_t stream);
 
 /* Destroy a plan (NULL is accepted).  No run on it may still be in flight. */
 b2b_status_t b2b_plan_destroy(b2b_plan_t plan);

@@ -52,7 +52,9 @@ def _create(dtype, batch, M, K, N1, N2, N3=0):
     ((1, 1, 64, 0, 64, 64), 1),           # K = 0
     ((1, 1, 64, 64, 0, 64), 1),           # N1 = 0
     ((1, 1, 64, 60, 64, 64), 2),          # K not a multiple of 8 for fp16
-    ((1, 1, 64, 64, 300, 64), 2),         # N1 > 256
+    ((1, 1, 64, 64, 520, 64), 2),         # N1 > 512
+    ((1, 1, 64, 64, 264, 64), 0),         # 256 < N1 <= 512: the paired kernel
+    ((3, 1, 64, 64, 264, 64), 2),         # tf32 N1 > 256
     ((3, 1, 64, 64, 64, 64, 64), 2),      # tf32 three-stage
     ((4, 1, 64, 64, 48, 64), 2),          # fp64 N1 not in {16, 32, 64}
     ((9, 1, 64, 64, 64, 64), 1),          # unknown dtype
@@ -70,8 +72,43 @@ def test_plan_create_validates_before_device(args, code):
     assert not h.value
 
 
+def _create_chain(dtype, batch, M, K, widths, n=None):
+    h = ctypes.c_void_p()
+    arr = (ctypes.c_int64 * max(1, len(widths)))(*widths)
+    code = b2b.b2b_chain_plan_create(ctypes.byref(h), dtype, batch, M, K,
+                                     len(widths) if n is None else n, arr)
+    return code, h
+
+
+@pytest.mark.parametrize("args,code", [
+    ((1, 1, 64, 64, (64, 64, 64, 64, 64)), 0),       # five stages
+    ((2, 1, 64, 64, (512,) * 7 + (4096,)), 0),       # eight stages at the width limits
+    ((1, 1, 64, 64, (64,) * 9), 1),                  # more than eight stages
+    ((1, 1, 64, 64, ()), 1),                         # no stage
+    ((1, 1, 64, 64, (64, 64, 520, 64)), 2),          # an intermediate wider than 512
+    ((1, 1, 64, 64, (64, 64, 64, 4104)), 2),         # last width above 4096
+    ((1, 1, 64, 64, (64, 60, 64, 64)), 2),           # width not a multiple of 8
+    ((3, 1, 64, 64, (64, 64, 64)), 2),               # tf32 three stages
+    ((4, 1, 64, 64, (16, 16, 16)), 2),               # fp64 three stages
+])
+def test_chain_plan_create_validates_before_device(args, code):
+    got, h = _create_chain(*args)
+    if code == 0:
+        import torch
+        if torch.cuda.is_available():
+            pytest.skip("a GPU is present")
+        assert got in (5, 6)
+    else:
+        assert got == code
+    assert not h.value
+
+
 def test_null_arguments():
     assert b2b.b2b_run(None, None, None, None, None, None, None) == 1
+    assert b2b.b2b_chain_run(None, None, None, None, None) == 1
+    assert b2b.b2b_chain_plan_create(None, 1, 1, 64, 64, 2, None) == 1
+    h = ctypes.c_void_p()
+    assert b2b.b2b_chain_plan_create(ctypes.byref(h), 1, 1, 64, 64, 2, None) == 1
     assert b2b.b2b_plan_destroy(None) == 0
     assert b2b.b2b_plan_device_status(None, None) == 1
     assert b2b.b2b_plan_info(None, None, None, None, None, None, None, None) == 1

@@ -37,6 +37,7 @@ CASES = [
     wl.Workload("fail_res_f16", "f16", 2, 512, 128, (128, 128), "normal_fanin", 1.0, 51),
     wl.Workload("fail_stream_bf16_3", "bf16", 1, 384, 512, (256, 256, 512), "normal_fanin", 1.0, 52),
     wl.Workload("fail_tf32", "tf32", 1, 384, 256, (256, 256), "normal", 1.0 / 16, 53),
+    wl.Workload("fail_deep5_f16", "f16", 1, 600, 128, (256, 512, 128, 256, 384), "normal_fanin", 1.0, 54),
 ]
 
 
@@ -44,13 +45,13 @@ CASES = [
 def test_timeout_is_reported_and_the_plan_recovers(w):
     host = wl.make_inputs(w)
     dev = [t.cuda() for t in host]
-    plan = b2b.Plan(w.dtype, w.batch, w.M, w.K, *w.N)
+    plan = b2b.ChainPlan(w.dtype, w.batch, w.M, w.K, w.N)
     out = plan.empty_out()
     out.fill_(0)
     plan.set_wait_budget(20_000_000)          # 20 ms
     plan.set_debug(1)
     t0 = time.perf_counter()
-    plan.run(*dev, D=out)
+    plan.run(dev[0], dev[1:], D=out)
     status = plan.status()                    # synchronises
     elapsed = time.perf_counter() - t0
     assert status == TIMEOUT
@@ -60,7 +61,7 @@ def test_timeout_is_reported_and_the_plan_recovers(w):
     # the context and the plan are healthy: a normal run is correct
     plan.set_debug(0)
     plan.set_wait_budget(0)
-    plan.run(*dev, D=out)
+    plan.run(dev[0], dev[1:], D=out)
     assert plan.status() == 0
     acc, mid, fin = KINDS[w.dtype]
     want = oracle.chain(oracle.widen(host[0]), [oracle.widen(t) for t in host[1:]], acc, mid, fin)

@@ -39,9 +39,13 @@ def _cuda():
 
 
 def run_gpu(w, host):
-    plan = b2b.Plan(w.dtype, w.batch, w.M, w.K, *w.N)
     dev = [t.cuda() for t in host]
-    out = plan.run(*dev)
+    if w.stages <= 3:
+        plan = b2b.Plan(w.dtype, w.batch, w.M, w.K, *w.N)
+        out = plan.run(*dev)
+    else:
+        plan = b2b.ChainPlan(w.dtype, w.batch, w.M, w.K, w.N)
+        out = plan.run(dev[0], dev[1:])
     torch.cuda.synchronize()
     assert plan.status() == 0
     return out.cpu()
@@ -86,6 +90,12 @@ EXACT = [
     wl.Workload("x_f16_3_narrow", "f16", 3, 384, 64, (64, 64, 64), "int", 1, 16),
     wl.Workload("x_bf16_f32out_3", "bf16_f32out", 2, 200, 128, (128, 128, 256), "int", 1, 17),
     wl.Workload("x_f16_f32out_3", "f16_f32out", 1, 700, 192, (96, 160, 384), "int", 1, 18),
+    # longer cascades and intermediates wider than 256 columns (every
+    # partial sum stays below 2^24: |value| <= K * N1 * N2 ...)
+    wl.Workload("x_f16_4", "f16", 2, 300, 32, (32, 32, 32, 64), "int", 1, 19),
+    wl.Workload("x_f16_f32out_5", "f16_f32out", 1, 520, 16, (16, 16, 16, 16, 128), "int", 1, 20),
+    wl.Workload("x_bf16_wide384", "bf16", 1, 300, 32, (384, 64), "int", 1, 41),
+    wl.Workload("x_bf16_wide512_3", "bf16", 1, 260, 16, (512, 16, 256), "int", 1, 42),
 ]
 
 
@@ -140,6 +150,14 @@ EDGES = [
     wl.Workload("streamed_many_f16", "f16", 1, 40000, 512, (128, 128), "normal_fanin", 1.0, 36),
     wl.Workload("streamed_many_tf32", "tf32", 2, 10000, 96, (64, 64), "normal", 1.0 / 16, 37),
     wl.Workload("streamed_many_bf16_npass", "bf16", 1, 20000, 64, (128, 384), "normal_fanin", 1.0, 38),
+    # longer cascades (one kernel for every stage) and wide intermediates
+    wl.Workload("deep6_bf16", "bf16", 1, 520, 256, (256, 128, 256, 192, 256, 320), "normal_fanin", 1.0, 43),
+    wl.Workload("eight_f16", "f16", 1, 260, 64, (128,) * 7 + (64,), "normal_fanin", 1.0, 44),
+    wl.Workload("wide512_f16_3", "f16", 1, 700, 128, (512, 512, 256), "normal_fanin", 1.0, 45),
+    wl.Workload("wide384_bf16_3", "bf16_f32out", 2, 300, 64, (384, 200, 136), "normal_fanin", 1.0, 46),
+    wl.Workload("wide512_bf16_2", "bf16", 1, 300, 96, (512, 1000), "normal_fanin", 1.0, 47),
+    wl.Workload("wide_tail_f16_4", "f16", 1, 129, 72, (264, 40, 392, 8), "normal_fanin", 1.0, 48),
+    wl.Workload("streamed_many_bf16_4", "bf16", 1, 40000, 128, (128, 128, 128, 512), "normal_fanin", 1.0, 49),
 ]
 
 
@@ -159,6 +177,46 @@ def test_empty_chain_is_a_no_op():
     plan.run(a, a, a, None, d)
     torch.cuda.synchronize()
     assert torch.all(d == 7.0)
+
+
+def test_chain_plan_matches_plan_bitwise():
+    """The S-stage interface and the three-argument one run the same kernel."""
+    w = wl.small(wl.WORKLOADS["three_stage_bf16"], M=300)
+    host = wl.make_inputs(w)
+    dev = [t.cuda() for t in host]
+    a = b2b.Plan(w.dtype, w.batch, w.M, w.K, *w.N).run(*dev)
+    b = b2b.ChainPlan(w.dtype, w.batch, w.M, w.K, w.N).run(dev[0], dev[1:])
+    torch.cuda.synchronize()
+    assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+
+
+def test_chain_plan_of_one_and_two_stages():
+    """ChainPlan with one or two widths runs the single-GEMM and two-stage plans."""
+    for N in ((128,), (128, 64)):
+        w = wl.Workload("short", "f16_f32out", 2, 200, 64, N, "normal_fanin", 1.0, 61)
+        host = wl.make_inputs(w)
+        plan = b2b.ChainPlan(w.dtype, w.batch, w.M, w.K, w.N)
+        out = plan.run(host[0].cuda(), [t.cuda() for t in host[1:]])
+        torch.cuda.synchronize()
+        assert plan.status() == 0
+        want = oracle.chain(oracle.widen(host[0]), [oracle.widen(t) for t in host[1:]],
+                            oracle.F32, oracle.F16, oracle.F32)
+        assert rel_err(out.cpu(), want) <= 1e-2
+
+
+def test_more_than_three_stages_need_chain_run():
+    plan = b2b.ChainPlan("f16", 1, 128, 64, (64, 64, 64, 64))
+    A = torch.zeros((1, 128, 64), dtype=torch.float16, device="cuda")
+    W = torch.zeros((1, 64, 64), dtype=torch.float16, device="cuda")
+    D = torch.zeros((1, 128, 64), dtype=torch.float16, device="cuda")
+    assert b2b.b2b_run(plan._h, A.data_ptr(), W.data_ptr(), W.data_ptr(), W.data_ptr(),
+                       D.data_ptr(), None) == 1
+    with pytest.raises(b2b.B2BError) as e:       # a weight missing
+        plan.run(A, [W, W, W, None], D)
+    assert e.value.code == 1
+    plan.run(A, [W, W, W, W], D)
+    torch.cuda.synchronize()
+    assert plan.status() == 0 and torch.all(D == 0)
 
 
 def test_runs_are_deterministic():

@@ -213,7 +213,7 @@ class Case:
         import torch
         import fusion_b2b_gemm_gb300 as b2b
         self.w = w
-        self.plan = b2b.Plan(w.dtype, w.batch, w.M, w.K, *w.N)
+        self.plan = b2b.ChainPlan(w.dtype, w.batch, w.M, w.K, w.N)
         host = wl.make_inputs(w)
         self.host = host
         per_copy = w.unique_bytes()
@@ -225,7 +225,7 @@ class Case:
 
     def fused(self, i):
         k = i % self.copies
-        self.plan.run(*self.inputs[k], D=self.outs[k])
+        self.plan.run(self.inputs[k][0], self.inputs[k][1:], D=self.outs[k])
 
     # -- unfused: torch / cuBLAS per GEMM, intermediate in HBM in the operand type
     def make_unfused_torch(self):
@@ -351,7 +351,7 @@ def run_reference(args):
     if rank != 0:
         return 0
     import oracle
-    w = wl.WORKLOADS[args.workload]
+    w = wl.ALL_WORKLOADS[args.workload]
     rows = args.ref_rows
     sw = w.with_(batch=1, M=min(rows, w.M))
     host = wl.make_inputs(sw)
@@ -389,7 +389,7 @@ def run_ours(args):
     import fusion_b2b_gemm_gb300  # noqa: F401  (fails loudly if the library is missing)
 
     peaks = load_peaks()
-    w = wl.WORKLOADS[args.workload]
+    w = wl.ALL_WORKLOADS[args.workload]
     case = Case(w, device)
     stream = torch.cuda.current_stream()
 
@@ -486,7 +486,7 @@ def per_config(args, peaks_all, device, stream):
     import torch
     out = []
     steps = args.cfg_steps
-    for name, w in wl.WORKLOADS.items():
+    for name, w in wl.ALL_WORKLOADS.items():
         case = Case(w, device)
         for i in range(3):
             case.fused(i)
@@ -510,7 +510,7 @@ def per_config(args, peaks_all, device, stream):
         go.replay()
         o_ms = graph_time_ms(go, torch.cuda.current_stream(), reps=3) / (3 * steps)
         entry = {
-            "workload": name, "dtype": w.dtype, "gflop": w.flops() / 1e9, "unique_mb": w.unique_bytes() / 2**20,
+            "workload": name, "extra": name in wl.EXTRA_WORKLOADS, "dtype": w.dtype, "gflop": w.flops() / 1e9, "unique_mb": w.unique_bytes() / 2**20,
             "fused_ms": fused_ms, "fused_tflops": w.flops() / (fused_ms * 1e-3) / 1e12,
             "fused_eager_median_ms": float(np.median(per)),
             "roofline": roofline_for(w, fused_ms, peaks_all, recorded_traffic(name)),
@@ -533,7 +533,7 @@ def main():
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default=wl.BENCH_WORKLOAD, choices=list(wl.WORKLOADS))
+    ap.add_argument("--workload", default=wl.BENCH_WORKLOAD, choices=list(wl.ALL_WORKLOADS))
     ap.add_argument("--soak-s", type=float, default=1.5, dest="soak_s")
     ap.add_argument("--cfg-steps", type=int, default=50, dest="cfg_steps")
     ap.add_argument("--cpu-s", type=float, default=10.0, dest="cpu_s")

@@ -220,7 +220,10 @@ b2b_status_t setup_chainn(b2b_plan_s* p) {
     // passes of 256 columns where they tile the width, else of 128
     c.pw[s] = (w % 256 == 0) ? 256 : 128;
     c.kpan[s + 1] = w / 64;
-    c.slots0 += (w / c.pw[s]) * c.kpan[s] * (s == 0 ? 2 : 1);
+    // the first GEMM: an A slot and a weight slot per K panel; later GEMMs:
+    // one weight slot per K panel, or per two with 128-column passes
+    const int kps = (s > 0 && c.pw[s] == 128) ? 2 : 1;
+    c.slots0 += (w / c.pw[s]) * (s == 0 ? 2 * c.kpan[s] : c.kpan[s] / kps);
     wmax = std::max(wmax, w);
   }
   c.pw[S - 1] = p->nf;
@@ -228,11 +231,16 @@ b2b_status_t setup_chainn(b2b_plan_s* p) {
   p->n1p = c.wpad[0];
   p->n2p = S >= 3 ? c.wpad[1] : 0;
   const uint32_t p_bytes = 256u * static_cast<uint32_t>(wmax);
-  c.nstg = 2;  // two 4 KB buffers per epilogue warp
-  const int64_t room = kSmemBudget - kBarBytes - int64_t(p_bytes) - int64_t(c.nstg) * kPanelBytes;
   // the rest of shared memory: ring slots of 16 KB (an A panel or a weight
-  // half panel each), at most sixteen
-  c.nslot = static_cast<int>(std::min<int64_t>(16, room / kPanelBytes));
+  // half panel each), at most sixteen, after one or two 4 KB staging buffers
+  // per epilogue warp (two, unless one buffer buys a ring slot in a ring of
+  // fewer than six)
+  auto slots_with = [&](int nstg) -> int {
+    const int64_t room = kSmemBudget - kBarBytes - int64_t(p_bytes) - int64_t(nstg) * kPanelBytes;
+    return static_cast<int>(std::min<int64_t>(16, room / kPanelBytes));
+  };
+  c.nstg = (slots_with(2) < 6 && slots_with(1) > slots_with(2)) ? 1 : 2;
+  c.nslot = slots_with(c.nstg);
   if (c.nslot < 4) return B2B_ERR_UNSUPPORTED;
   c.off_ring = 0;
   c.off_p = static_cast<uint32_t>(c.nslot) * kPanelBytes;
@@ -240,7 +248,7 @@ b2b_status_t setup_chainn(b2b_plan_s* p) {
   c.off_bar = c.off_stg + static_cast<uint32_t>(c.nstg) * kPanelBytes;
   p->smem_bytes = static_cast<int>(c.off_bar + kBarBytes + 1024);
   if (p->smem_bytes > kSmemOptin) return B2B_ERR_UNSUPPORTED;
-  // a weight whose width is a multiple of 64 is read one 4-D box per half panel
+  // a weight whose width is a multiple of 64 is read in 4-D boxes
   c.w_merged = 0;
   for (int s = 0; s < S; ++s)
     if (p->N[s] % 64 == 0) c.w_merged |= 1 << s;
@@ -712,7 +720,10 @@ b2b_status_t encode_chain_maps(b2b_plan_s* p, const void* const* W, const void* 
     // CTA pairs: each CTA loads half of a pass's 64-column blocks
     for (int s = 0; s < S && st == B2B_OK; ++s) {
       if ((p->pn.w_merged >> s) & 1) {
-        st = encode_w4d(&maps->w[s], in_dt, p->esz, W[s], p->N[s], kin, p->batch, CK,
+        // a box of this CTA's column blocks of a pass, over one K panel, or
+        // two for 128-column passes after the first GEMM
+        const uint32_t kps = (s > 0 && p->pn.pw[s] == 128) ? 2u : 1u;
+        st = encode_w4d(&maps->w[s], in_dt, p->esz, W[s], p->N[s], kin, p->batch, CK * kps,
                         static_cast<uint32_t>(p->pn.pw[s] / 128));
       } else {
         st = encode_3d(&maps->w[s], in_dt, p->esz, W[s], p->N[s], kin, p->batch, CK, CK);

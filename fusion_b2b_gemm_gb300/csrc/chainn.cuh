@@ -23,11 +23,15 @@
 // at most 256 columns takes the region not used last, so a GEMM writes one
 // region while the converters still read the other, and starts on the first
 // 128-column chunk of its operand image as soon as that chunk is written.
-// A wider intermediate (up to 512 columns) takes both regions; the next GEMM
-// then starts once the converters have freed X.  The passes of the last GEMM
-// alternate between the regions, so the epilogue of one pass overlaps the
-// MMAs of the next.  Whether a region is free is counted by one barrier per
-// region that its reader (the converters or the epilogue) releases.
+// A wider intermediate (up to 512 columns) starts in the region not used
+// last and continues in the other; the next GEMM writes the first one again
+// once its converters have freed it.  The passes of the first GEMM are
+// converted one by one as they complete (it reads no operand image); a later
+// GEMM's result only once the whole GEMM, which reads the image, is done.
+// The passes of the last GEMM alternate between the regions, so the
+// epilogue of one pass overlaps the MMAs of the next.  Whether a region is
+// free is counted by one barrier per region that its reader (the converters
+// or the epilogue) releases.
 //
 // Roles (384 threads, one CTA per SM, persistent over 256-row tiles):
 //   warp 0     producer: one ring of 16 KB slots in the order the MMAs read
@@ -59,7 +63,8 @@ constexpr int kMaxStages = 8;
 enum : int {
   knFull = 0,        // [16] ring slot filled (even CTA's: armed by it for both CTAs' copies)
   knEmpty = 16,      // [16] ring slot consumed
-  knCFull = 32,      // an intermediate GEMM complete (all its passes): converters
+  knCFull = 32,      // an intermediate GEMM after the first complete (all its
+                     // passes): converters
   knPChunk = 33,     // [2][4] 128-column chunk c of intermediate k's operand image
                      //        (set k & 1) written in both CTAs (even CTA's)
   knRFull = 41,      // [2] X / Y holds a pass of the last GEMM (epilogue)
@@ -68,6 +73,7 @@ enum : int {
   knDrain = 45,      // every MMA complete (exit)
   knSlotTmem = 46,   // uint32 TMEM base, then the int abort flag
   knSlotReady = 47,  // uint32: ring slots whose copies have landed (even CTA)
+  knCFull0 = 48,     // [4] pass j of the first GEMM complete: converters
 };
 
 constexpr int kChainNThreads = 384;
@@ -132,20 +138,26 @@ __device__ __forceinline__ ChainNUnit chainn_unit(const ChainNParams& p, int cid
 }
 
 // Tensor-memory placement, walked identically by the MMA thread, the
-// converters and the epilogue: an accumulator of at most 256 columns takes
-// the region not used last; a wider one starts at column 0 and covers both,
-// and the region after it is X (freed first).
+// converters and the epilogue.  Every accumulator starts in the region not
+// used last (r0); a wider one continues in the other region, and the next
+// accumulator then starts in r0 again, which its converters free first.
+// Column c of an accumulator that starts in r0 lives at tmem_col(r0, c).
+template <int V>
+struct integral_constant_int {
+  static constexpr int value = V;
+};
+
 struct RegionCursor {
-  int last = 1;
+  uint32_t last = 1;
   __device__ __forceinline__ uint32_t take(int width) {
-    if (width <= 256) {
-      last ^= 1;
-      return static_cast<uint32_t>(last) * 256u;
-    }
-    last = 1;
-    return 0u;
+    const uint32_t r0 = last ^ 1u;
+    last = width <= 256 ? r0 : r0 ^ 1u;
+    return r0;
   }
 };
+__device__ __forceinline__ uint32_t tmem_col(uint32_t r0, int c) {
+  return ((((static_cast<uint32_t>(c) >> 8) ^ r0) & 1u) << 8) | (static_cast<uint32_t>(c) & 255u);
+}
 
 template <int IN, int OUT, int NF>
 __global__ void __launch_bounds__(kChainNThreads, 1)
@@ -184,6 +196,7 @@ __global__ void __launch_bounds__(kChainNThreads, 1)
       mbar_init(bar(knEmpty + i), 1);
     }
     mbar_init(bar(knCFull), 1);
+    for (int i = 0; i < 4; ++i) mbar_init(bar(knCFull0 + i), 1);
     for (int i = 0; i < 8; ++i) mbar_init(bar(knPChunk + i), 2);
     for (int i = 0; i < 2; ++i) {
       mbar_init(bar(knRFull + i), 1);
@@ -220,6 +233,11 @@ __global__ void __launch_bounds__(kChainNThreads, 1)
   auto row0 = [&](int mt) -> int { return mt * 256 + static_cast<int>(rank) * 128; };
   const uint32_t p_img = base + p.off_p;
   const int kpan_last = p.kpan[S - 1];
+  // K panels per ring slot: a weight half panel of 64 columns (pass width
+  // 128) takes 8 KB, so a slot holds two K panels of it; GEMM s > 0 only
+  // (its K panel count, a multiple of 128 / 64, is even)
+  auto kps_of = [&](int s) -> int { return (s > 0 && p.pw[s] == 128) ? 2 : 1; };
+  const int kps_last = kps_of(S - 1);
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -230,13 +248,15 @@ __global__ void __launch_bounds__(kChainNThreads, 1)
       uint32_t slot = 0, phase = 0;
       uint64_t issued = 0;
       bool ok = true;
-      // one ring slot: an A panel (s < 0) or this CTA's half of a weight panel
-      auto load = [&](int s, int b, int m0, int kb, int col0, int pw) -> bool {
+      // one ring slot: an A panel (s < 0), or this CTA's half of `npan`
+      // weight K panels (kb, kb + 1, ...)
+      auto load = [&](int s, int b, int m0, int kb, int col0, int pw, int npan) -> bool {
         if (!bw.wait(bar(knEmpty + slot), phase ^ 1u)) return false;
         const uint32_t dst = base + p.off_ring + slot * static_cast<uint32_t>(kPanelBytes);
         const uint32_t fb = lbar(knFull + slot);
         const int wcols = pw / 2;
-        const uint32_t bytes = s < 0 ? static_cast<uint32_t>(kPanelBytes) : 128u * static_cast<uint32_t>(wcols);
+        const uint32_t bytes =
+            s < 0 ? static_cast<uint32_t>(kPanelBytes) : 128u * static_cast<uint32_t>(wcols * npan);
         // Only the even CTA arms its barrier, for both CTAs' copies; the odd
         // CTA's copies may land first (the transaction count then dips
         // below zero until the arming, which the barrier allows).
@@ -249,10 +269,13 @@ __global__ void __launch_bounds__(kChainNThreads, 1)
             const CUtensorMap* wm = &maps.w[s];
             const int n0 = col0 + static_cast<int>(rank) * wcols;
             if ((p.w_merged >> s) & 1) {
+              // one box of npan * 64 K rows and wcols / 64 column blocks
               tma_load_4d_pair(dst, wm, fb, 0, kb * CK, n0 / WBOX_N, b);
             } else {
-              for (int j = 0; j < wcols / WBOX_N; ++j)
-                tma_load_3d_pair(dst + j * WBOX_BYTES, wm, fb, n0 + j * WBOX_N, kb * CK, b);
+              for (int i = 0; i < npan; ++i)
+                for (int j = 0; j < wcols / WBOX_N; ++j)
+                  tma_load_3d_pair(dst + (i * (wcols / WBOX_N) + j) * WBOX_BYTES, wm, fb, n0 + j * WBOX_N,
+                                   (kb + i) * CK, b);
             }
           }
         }
@@ -273,15 +296,16 @@ __global__ void __launch_bounds__(kChainNThreads, 1)
           for (int q = 0; q < p.kpan[0]; ++q) tma_prefetch_l2_3d(&maps.a, q * CK, row0(n.mt), n.b);
         }
         for (int s = 0; s < S - 1 && ok; ++s) {
-          const int pw = p.pw[s];
+          const int pw = p.pw[s], kps = kps_of(s);
           for (int col0 = 0; col0 < p.wpad[s] && ok; col0 += pw)
-            for (int kb = 0; kb < p.kpan[s] && ok; ++kb) {
-              if (s == 0) ok = load(-1, c.b, m0, kb, 0, 0);
-              if (ok) ok = load(s, c.b, m0, kb, col0, pw);
+            for (int kb = 0; kb < p.kpan[s] && ok; kb += kps) {
+              if (s == 0) ok = load(-1, c.b, m0, kb, 0, 0, 1);
+              if (ok) ok = load(s, c.b, m0, kb, col0, pw, kps);
             }
         }
         for (int j = c.p0; j < c.p1 && ok; ++j)
-          for (int kb = 0; kb < kpan_last && ok; ++kb) ok = load(S - 1, c.b, m0, kb, j * NF, NF);
+          for (int kb = 0; kb < kpan_last && ok; kb += kps_last)
+            ok = load(S - 1, c.b, m0, kb, j * NF, NF, kps_last);
       }
       // copies in flight land before exit (the even CTA's barriers count both
       // CTAs' copies; the odd CTA waits at the cluster barrier before exit)
@@ -301,7 +325,7 @@ __global__ void __launch_bounds__(kChainNThreads, 1)
       bool ok = true;
       for (int it = 0; it < t_count && ok; ++it) {
         const ChainNUnit c = chainn_unit(p, cid, ncl, it);
-        const int per_unit = p.slots0 + (c.p1 - c.p0) * kpan_last;
+        const int per_unit = p.slots0 + (c.p1 - c.p0) * (kpan_last / kps_last);
         for (int q = 0; q < per_unit && ok; ++q) {
           ok = bw.wait(bar(knFull + slot), phase);
           if (!ok) break;
@@ -347,12 +371,14 @@ __global__ void __launch_bounds__(kChainNThreads, 1)
           }
         }
       };
-      // Four MMAs over one 64-element K panel.  First GEMM (a_smem): the A
-      // panel is in this slot and the weight half panel in the next; later
-      // GEMMs read K panel kb of the operand image, after waiting for the
-      // chunk barrier `chunk` (if >= 0) with parity cpar.
-      auto stage_mmas = [&](uint32_t d, uint32_t idesc, bool a_smem, int kb, int chunk,
+      // Four MMAs per 64-element K panel.  First GEMM (a_smem): the A panel
+      // is in this slot and the weight half panel in the next; later GEMMs
+      // read K panels kb .. kb + npan - 1 of the operand image (their weight
+      // half panels share one slot), after waiting for the chunk barrier
+      // `chunk` (if >= 0) with parity cpar.
+      auto stage_mmas = [&](auto npan_c, uint32_t d, uint32_t idesc, bool a_smem, int kb, int chunk,
                             uint32_t cpar) -> bool {
+        constexpr int npan = decltype(npan_c)::value;
         const uint32_t need = a_smem ? 2u : 1u;
         if (!stage_ready(need)) return false;
         if (chunk >= 0 && !bwm.wait(bar(chunk), cpar)) return false;
@@ -364,10 +390,22 @@ __global__ void __launch_bounds__(kChainNThreads, 1)
         const uint32_t sa = a_smem ? base + p.off_ring + s0 * static_cast<uint32_t>(kPanelBytes)
                                    : p_img + static_cast<uint32_t>(kb) * kPanelBytes;
         const uint32_t acc0 = kb != 0 ? 1u : 0u;
+        // (straight-line MMAs: a branch between two of them costs more than
+        // the tensor pipe's queue hides)
+        if constexpr (npan == 2) {
 #pragma unroll
-        for (int kk = 0; kk < CK / KSTEP; ++kk)
-          mma_ss<false, CG>(d, desc_sw128(sa + kk * 32u, 16u, 1024u),
-                            desc_sw128(wb + kk * KSTEP * 128u, WBOX_BYTES, 1024u), idesc, kk ? 1u : acc0);
+          for (int kk = 0; kk < 2 * (CK / KSTEP); ++kk) {
+            const uint32_t pa = static_cast<uint32_t>(kk >> 2), ks = static_cast<uint32_t>(kk & 3);
+            mma_ss<false, CG>(d, desc_sw128(sa + pa * kPanelBytes + ks * 32u, 16u, 1024u),
+                              desc_sw128(wb + pa * WBOX_BYTES + ks * KSTEP * 128u, WBOX_BYTES, 1024u), idesc,
+                              kk ? 1u : acc0);
+          }
+        } else {
+#pragma unroll
+          for (int kk = 0; kk < CK / KSTEP; ++kk)
+            mma_ss<false, CG>(d, desc_sw128(sa + kk * 32u, 16u, 1024u),
+                              desc_sw128(wb + kk * KSTEP * 128u, WBOX_BYTES, 1024u), idesc, kk ? 1u : acc0);
+        }
         tc_commit<CG>(bar(knEmpty + s0));
         if (a_smem) tc_commit<CG>(bar(knEmpty + s1));
         slot = s1 + 1u == static_cast<uint32_t>(p.nslot) ? 0u : s1 + 1u;
@@ -381,16 +419,26 @@ __global__ void __launch_bounds__(kChainNThreads, 1)
         if (!first_pass || (kb & 1)) return -1;
         return knPChunk + static_cast<int>(((k - 1u) & 1u) * 4u) + kb / 2;
       };
+      // one pass: kpan K panels, npan of them per ring slot
+      auto run_pass = [&](auto npan_c, uint32_t d, uint32_t idesc, bool a_smem, int kpan, bool first,
+                          uint32_t cpar) -> bool {
+        constexpr int npan = decltype(npan_c)::value;
+        for (int kb = 0; kb < kpan; kb += npan)
+          if (!stage_mmas(npan_c, d, idesc, a_smem, kb, a_smem ? -1 : chunk_of(first, kb), cpar)) return false;
+        return true;
+      };
+      using One = integral_constant_int<1>;
+      using Two = integral_constant_int<2>;
       for (int it = 0; it < t_count && ok; ++it) {
         const ChainNUnit c = chainn_unit(p, cid, ncl, it);
         for (int s = 0; s < S - 1 && ok; ++s) {
           const int pw = p.pw[s];
-          const uint32_t cbase = rc.take(p.wpad[s]);
+          const uint32_t r0 = rc.take(p.wpad[s]);
           const uint32_t idesc = make_idesc(FMT, static_cast<uint32_t>(pw), 256u, true);
           const uint32_t cpar = ((k - 1u) >> 1) & 1u;
           int touched = 0;
           for (int col0 = 0; col0 < p.wpad[s] && ok; col0 += pw) {
-            const uint32_t col = cbase + static_cast<uint32_t>(col0);
+            const uint32_t col = tmem_col(r0, col0);
             const int r = static_cast<int>(col >> 8);
             if (!((touched >> r) & 1)) {
               touched |= 1 << r;
@@ -398,11 +446,15 @@ __global__ void __launch_bounds__(kChainNThreads, 1)
               if (!ok) break;
               tc_fence_after();
             }
-            for (int kb = 0; kb < p.kpan[s] && ok; ++kb)
-              ok = stage_mmas(tmem_base + col, idesc, s == 0, kb, s == 0 ? -1 : chunk_of(col0 == 0, kb), cpar);
+            ok = kps_of(s) == 2 ? run_pass(Two{}, tmem_base + col, idesc, s == 0, p.kpan[s], col0 == 0, cpar)
+                                : run_pass(One{}, tmem_base + col, idesc, s == 0, p.kpan[s], col0 == 0, cpar);
+            // the first GEMM reads no operand image, so each of its passes
+            // can be converted as soon as it completes (every MMA that read
+            // the image, the previous tile's last GEMM, completed before it)
+            if (ok && s == 0) tc_commit<CG>(bar(knCFull0 + (col0 >> (pw == 256 ? 8 : 7))));
           }
           if (!ok) break;
-          tc_commit<CG>(bar(knCFull));
+          if (s > 0) tc_commit<CG>(bar(knCFull));
           ++k;
         }
         if (!ok) break;
@@ -410,13 +462,13 @@ __global__ void __launch_bounds__(kChainNThreads, 1)
         const uint32_t idesc = make_idesc(FMT, NF, 256u, true);
         const uint32_t cpar = ((k - 1u) >> 1) & 1u;
         for (int j = c.p0; j < c.p1 && ok; ++j) {
-          const uint32_t col = rc.take(NF);
-          const int r = static_cast<int>(col >> 8);
+          const int r = static_cast<int>(rc.take(NF));
+          const uint32_t col = static_cast<uint32_t>(r) * 256u;
           ok = take_region(r);
           if (!ok) break;
           tc_fence_after();
-          for (int kb = 0; kb < kpan_last && ok; ++kb)
-            ok = stage_mmas(tmem_base + col, idesc, false, kb, chunk_of(j == c.p0, kb), cpar);
+          ok = kps_last == 2 ? run_pass(Two{}, tmem_base + col, idesc, false, kpan_last, j == c.p0, cpar)
+                             : run_pass(One{}, tmem_base + col, idesc, false, kpan_last, j == c.p0, cpar);
           if (!ok) break;
           tc_commit<CG>(bar(knRFull + r));
         }
@@ -442,26 +494,37 @@ __global__ void __launch_bounds__(kChainNThreads, 1)
     // rows x 128 bytes) through two staging buffers of its own, so the warps
     // never wait for each other except once per pass, when the region has
     // been read
-    const uint32_t wstg = base + p.off_stg + static_cast<uint32_t>(q) * 2u * 4096u;
+    const bool two_stg = p.nstg == 2;
+    const uint32_t wstg = base + p.off_stg + static_cast<uint32_t>(q * p.nstg) * 4096u;
     const bool elected = (warp == 6 && lane == 0);
     constexpr int NBOX = NF / OBOX_N;
     constexpr int LDS = OBOX_N / 32;
     RegionCursor rc;
-    uint32_t k = 0;          // intermediates converted so far
+    uint32_t k = 0;             // intermediates converted so far
+    uint32_t kl = 0;            // of them, intermediates after the first
     uint32_t krx = 0, kry = 0;  // last-GEMM passes read from X / Y so far
     uint32_t nbox = 0;
     bool ok = true;
     for (int it = 0; it < t_count; ++it) {
       const ChainNUnit c = chainn_unit(p, cid, ncl, it);
       for (int s = 0; s < S - 1; ++s) {
-        const uint32_t cbase = rc.take(p.wpad[s]);
-        if (ok) ok = warp_wait(bw, bar(knCFull), k & 1u);
-        if (ok) tc_fence_after();
+        const uint32_t r0 = rc.take(p.wpad[s]);
+        // the first GEMM: one completion barrier per pass; later GEMMs: one
+        if (s > 0) {
+          if (ok) ok = warp_wait(bw, bar(knCFull), kl & 1u);
+          ++kl;
+          if (ok) tc_fence_after();
+        }
         const int nch = p.wpad[s] / 128;
+        const int cpp = p.pw[s] / 128;  // chunks per pass
         for (int ch = 0; ch < nch; ++ch) {
           const int pcol = ch * 128 + h * 64;
+          if (s == 0 && (cpp == 1 || !(ch & 1))) {
+            if (ok) ok = warp_wait(bw, bar(knCFull0 + (cpp == 1 ? ch : ch >> 1)), static_cast<uint32_t>(it) & 1u);
+            if (ok) tc_fence_after();
+          }
           if (ok) {
-            rearrange_accumulator<IN>(tmem_base + lane_off + cbase + static_cast<uint32_t>(pcol), 64, row,
+            rearrange_accumulator<IN>(tmem_base + lane_off + tmem_col(r0, pcol), 64, row,
                                       p_img + static_cast<uint32_t>(pcol / 64) * kPanelBytes);
             tc_fence_before();
           }
@@ -475,8 +538,8 @@ __global__ void __launch_bounds__(kChainNThreads, 1)
             if (ch + 1 == nch)
               for (int c2 = nch; c2 < 4; ++c2) mbar_arrive_cluster(lbar(set + c2));
             // the chunk was the last one in its region: the region is free
-            const uint32_t r = (cbase + static_cast<uint32_t>(ch * 128)) >> 8;
-            if (ch + 1 == nch || ((cbase + static_cast<uint32_t>(ch * 128 + 128)) >> 8) != r)
+            const uint32_t r = tmem_col(r0, ch * 128) >> 8;
+            if (ch + 1 == nch || (tmem_col(r0, ch * 128 + 128) >> 8) != r)
               mbar_arrive_cluster(lbar(knREmpty + static_cast<int>(r)));
           }
         }
@@ -484,9 +547,9 @@ __global__ void __launch_bounds__(kChainNThreads, 1)
       }
       const int mw = row0(c.mt) + q * 32;  // this warp's first row
       for (int j = c.p0; j < c.p1; ++j) {
-        const uint32_t col = rc.take(NF);
+        const int r = static_cast<int>(rc.take(NF));
         if (!epi) continue;
-        const int r = static_cast<int>(col >> 8);
+        const uint32_t col = static_cast<uint32_t>(r) * 256u;
         if (ok) ok = warp_wait(bw, bar(knRFull + r), (r ? kry : krx) & 1u);
         if (r) ++kry; else ++krx;
         tc_fence_after();
@@ -498,9 +561,11 @@ __global__ void __launch_bounds__(kChainNThreads, 1)
         }
 #pragma unroll 1
         for (int x = 0; x < NBOX; ++x) {
-          const uint32_t stg = wstg + (nbox & 1u) * 4096u;
+          const uint32_t stg = wstg + (two_stg ? (nbox & 1u) * 4096u : 0u);
           // the store issued two boxes ago (same buffer) has read it
-          if (lane == 0 && ok) bulk_wait_read<1>();
+          if (lane == 0 && ok) {
+            if (two_stg) bulk_wait_read<1>(); else bulk_wait_read<0>();
+          }
           __syncwarp();
           if (ok) {
             tmem_wait_ld();

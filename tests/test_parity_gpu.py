@@ -116,6 +116,8 @@ REDUCED = [
     wl.small(wl.WORKLOADS["tf32"], M=640),
     wl.small(wl.WORKLOADS["f64"], M=200, batch=3),
     wl.small(wl.WORKLOADS["three_stage_bf16"], M=520),
+    wl.small(wl.EXTRA_WORKLOADS["four_stage_bf16"], M=777),
+    wl.small(wl.EXTRA_WORKLOADS["wide_f16"], M=600, batch=2),
 ]
 
 
@@ -272,9 +274,9 @@ def test_single_gemm_plan(dtype, K, N):
 
 # ------------------------------------------------ full-size, sampled rows --
 
-@pytest.mark.parametrize("name", list(wl.WORKLOADS))
+@pytest.mark.parametrize("name", list(wl.ALL_WORKLOADS))
 def test_full_size_sampled_rows(name):
-    w = wl.WORKLOADS[name]
+    w = wl.ALL_WORKLOADS[name]
     host = wl.make_inputs(w)
     got = run_gpu(w, host)
     rng = np.random.default_rng(99)

@@ -106,6 +106,18 @@ WORKLOADS: Dict[str, Workload] = {
                                  "normal_fanin", 1.0, 4, "bf16 in/out, two bf16 intermediates"),
 }
 
+# Longer cascades and wider intermediates than the five workloads above (the
+# general form of the method: each operator's output is the next one's
+# input).  Measured beside them; not part of the published comparison.
+EXTRA_WORKLOADS: Dict[str, Workload] = {
+    "four_stage_bf16": Workload("four_stage_bf16", "bf16", 1, 65536, 256, (256, 256, 256, 256),
+                                "normal_fanin", 1.0, 5, "bf16 in/out, three bf16 intermediates"),
+    "wide_f16": Workload("wide_f16", "f16", 8, 8192, 128, (512, 128), "normal_fanin", 1.0, 6,
+                         "fp16 in/out, one 512-column fp16 intermediate"),
+}
+
+ALL_WORKLOADS: Dict[str, Workload] = {**WORKLOADS, **EXTRA_WORKLOADS}
+
 BENCH_WORKLOAD = "batched_f16"
 
 

@@ -173,7 +173,8 @@ def oracle_kinds(dtype):
     import oracle
     return {"f16_f32out": (oracle.F32, oracle.F16, oracle.F32), "f16": (oracle.F32, oracle.F16, oracle.F16),
             "bf16": (oracle.F32, oracle.BF16, oracle.BF16), "bf16_f32out": (oracle.F32, oracle.BF16, oracle.F32),
-            "tf32": (oracle.F32, oracle.TF32, oracle.F32), "f64": (oracle.NONE, oracle.NONE, oracle.NONE)}[dtype]
+            "tf32": (oracle.F32, oracle.TF32, oracle.F32), "f64": (oracle.NONE, oracle.NONE, oracle.NONE),
+            "tf32_f16": (oracle.F32, oracle.F16, oracle.F32), "tf32_bf16": (oracle.F32, oracle.BF16, oracle.F32)}[dtype]
 
 
 def oracle_sample(w: wl.Workload, rows: int, batches: int = 1):
@@ -237,6 +238,8 @@ class Case:
             k = i % self.copies
             x = self.inputs[k][0]
             for s, W in enumerate(self.inputs[k][1:]):
+                if x.dtype != W.dtype:  # mixed types: the intermediate takes the next weight's type
+                    x = x.to(W.dtype)
                 x = torch.bmm(x, W)
                 if s == w.stages - 1 and x.dtype != out_dt:
                     x = x.to(out_dt)
@@ -250,15 +253,19 @@ class Case:
         w = self.w
         in_dt, out_dt = wl.io_dtypes(w.dtype)
         single_dt = {"f16_f32out": "f16", "f16": "f16", "bf16": "bf16", "bf16_f32out": "bf16",
-                     "tf32": "tf32", "f64": "f64"}[w.dtype]
-        last_dt = w.dtype
+                     "tf32": "tf32", "f64": "f64", "tf32_f16": "f16", "tf32_bf16": "bf16"}[w.dtype]
+        last_dt = {"tf32_f16": "f16_f32out", "tf32_bf16": "bf16_f32out"}.get(w.dtype, w.dtype)
+        mixed = w.dtype in ("tf32_f16", "tf32_bf16")
+        mid_dt = wl.input_dtypes(w.dtype, w.stages)[-1]
         plans, mids = [], []
         kin = w.K
         for s, n in enumerate(w.N):
-            dt = last_dt if s == w.stages - 1 else single_dt
+            dt = "tf32" if (mixed and s == 0) else (last_dt if s == w.stages - 1 else single_dt)
             plans.append(b2b.GemmPlan(dt, w.batch, w.M, kin, n))
             if s < w.stages - 1:
-                mids.append(torch.empty((w.batch, w.M, n), dtype=in_dt, device=self.outs[0].device))
+                # (mixed: the tf32 GEMM writes fp32, cast to the 16-bit type below)
+                mids.append(torch.empty((w.batch, w.M, n), dtype=torch.float32 if (mixed and s == 0) else mid_dt,
+                                        device=self.outs[0].device))
             kin = n
         self._own = (plans, mids)
 
@@ -266,10 +273,13 @@ class Case:
             k = i % self.copies
             x = self.inputs[k][0]
             for s, W in enumerate(self.inputs[k][1:]):
+                if x.dtype != W.dtype:
+                    x = x.to(W.dtype)
                 dst = mids[s] if s < w.stages - 1 else self.outs[k]
                 plans[s].run(x, W, D=dst)
                 x = dst
-        return run, sum(p.info()["launches_per_run"] for p in plans)
+        launches = sum(p.info()["launches_per_run"] for p in plans) + (1 if mixed else 0)
+        return run, launches
 
 
 def measure_peak_matmul(dtype_name: str, n: int, reps: int = 5):
@@ -298,7 +308,13 @@ def roofline_for(w: wl.Workload, kernel_ms: float, peaks: dict, traffic=None):
     """Bound, achieved and peak for the fused kernel of workload w."""
     flops = w.flops()
     byts = w.unique_bytes()
-    tflops_peak = peaks["tensor"][w.dtype]
+    if w.dtype in ("tf32_f16", "tf32_bf16"):
+        # mixed types: the first GEMM at the tf32 rate, the rest at the 16-bit
+        # rate; the peak is the blend for this workload's split of the work
+        f0 = 2 * w.batch * w.M * w.K * w.N[0]
+        tflops_peak = flops / (f0 / peaks["tensor"]["tf32"] + (flops - f0) / peaks["tensor"]["bf16"])
+    else:
+        tflops_peak = peaks["tensor"][w.dtype]
     t_compute = flops / (tflops_peak * 1e12)
     t_mem = byts / (peaks["hbm_gbs"] * 1e9)
     if t_mem >= t_compute:
@@ -419,6 +435,8 @@ def run_ours(args):
     barrier()
     clocks = sampler.stop()
     total_ms = max_over_ranks(total_ms, device)
+    if case.plan.status() != 0:
+        raise RuntimeError("a bounded wait of the fused kernel gave up during the timed region")
 
     ms_per_step = total_ms / args.steps
     kernel_ms = ms_per_step      # one kernel launch per step, back to back in the graph
@@ -493,6 +511,8 @@ def per_config(args, peaks_all, device, stream):
         g = graph_of(case.fused, steps, stream)
         g.replay()
         fused_ms = graph_time_ms(g, torch.cuda.current_stream(), reps=3) / (3 * steps)
+        if case.plan.status() != 0:
+            raise RuntimeError(f"{name}: a bounded wait of the fused kernel gave up")
         per, _ = event_time_ms(case.fused, steps, stream)
         torch_fn = case.make_unfused_torch()
         old = torch.backends.cuda.matmul.allow_tf32
@@ -509,13 +529,15 @@ def per_config(args, peaks_all, device, stream):
         go = graph_of(own_fn, steps, stream)
         go.replay()
         o_ms = graph_time_ms(go, torch.cuda.current_stream(), reps=3) / (3 * steps)
+        if any(p.status() != 0 for p in case._own[0]):
+            o_ms = None  # a single-GEMM kernel gave up a wait: no valid time
         entry = {
             "workload": name, "extra": name in wl.EXTRA_WORKLOADS, "dtype": w.dtype, "gflop": w.flops() / 1e9, "unique_mb": w.unique_bytes() / 2**20,
             "fused_ms": fused_ms, "fused_tflops": w.flops() / (fused_ms * 1e-3) / 1e12,
             "fused_eager_median_ms": float(np.median(per)),
             "roofline": roofline_for(w, fused_ms, peaks_all, recorded_traffic(name)),
             "unfused_torch_ms": t_ms, "unfused_own_ms": o_ms, "unfused_own_launches": own_launches,
-            "speedup_vs_best_unfused": min(t_ms, o_ms) / fused_ms,
+            "speedup_vs_best_unfused": min(t_ms, o_ms if o_ms is not None else t_ms) / fused_ms,
             "launches_per_run": case.info["launches_per_run"], "plan": case.info,
             "timing": f"{steps} calls per CUDA graph, 3 replays",
         }

@@ -28,7 +28,8 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 _LIB_PATH = os.path.join(_HERE, "_lib", "libb2b.so")
 
 # b2b_dtype_t
-DTYPES = {"f16_f32out": 0, "f16": 1, "bf16": 2, "tf32": 3, "f64": 4, "bf16_f32out": 5}
+DTYPES = {"f16_f32out": 0, "f16": 1, "bf16": 2, "tf32": 3, "f64": 4, "bf16_f32out": 5,
+          "tf32_f16": 6, "tf32_bf16": 7}
 MAX_STAGES = 8  # B2B_MAX_STAGES
 STATUS = {0: "B2B_OK", 1: "B2B_ERR_INVALID_ARG", 2: "B2B_ERR_UNSUPPORTED", 3: "B2B_ERR_ALIGNMENT",
           4: "B2B_ERR_ALIAS", 5: "B2B_ERR_DEVICE", 6: "B2B_ERR_CUDA", 7: "B2B_ERR_TIMEOUT"}
@@ -143,9 +144,12 @@ class Plan:
     # -- torch helpers ---------------------------------------------------
     def io_dtypes(self):
         import torch
+        # (type of A, type of the output); the mixed types' later weights are
+        # 16-bit (weight_dtypes)
         table = {"f16_f32out": (torch.float16, torch.float32), "f16": (torch.float16, torch.float16),
                  "bf16": (torch.bfloat16, torch.bfloat16), "bf16_f32out": (torch.bfloat16, torch.float32),
-                 "tf32": (torch.float32, torch.float32), "f64": (torch.float64, torch.float64)}
+                 "tf32": (torch.float32, torch.float32), "f64": (torch.float64, torch.float64),
+                 "tf32_f16": (torch.float32, torch.float32), "tf32_bf16": (torch.float32, torch.float32)}
         return table[self.dtype]
 
     def out_shape(self) -> Tuple[int, int, int]:

@@ -84,12 +84,12 @@ const ChainKernelEntry* find_chain_kernel(int in, int out, int S, int n1p, int n
   return nullptr;
 }
 
-const ChainNEntry* find_chainn_kernel(int in, int out, int nf) {
+const ChainNEntry* find_chainn_kernel(int in, int out, int nf, bool tf0) {
   const ChainNTable tables[] = {chainn_table_f16(), chainn_table_bf16()};
   for (const ChainNTable& t : tables)
     for (int i = 0; i < t.count; ++i) {
       const ChainNEntry& e = t.entries[i];
-      if (e.in == in && e.out == out && e.nf == nf) return &e;
+      if (e.in == in && e.out == out && e.nf == nf && e.tf0 == tf0) return &e;
     }
   return nullptr;
 }
@@ -160,6 +160,7 @@ struct b2b_plan_s {
   int stages;
   int64_t batch, M, K, N[kMaxStages];
   int in_kind, out_kind, esz, osz;
+  bool tf0;  // mixed-type cascade: the first GEMM on tf32 operands (fp32 A, W0)
   int n1p, n2p, nf;
   bool res;
   ChainParams prm;
@@ -212,7 +213,8 @@ b2b_status_t setup_chainn(b2b_plan_s* p) {
   c.total_tiles = static_cast<int>(tiles);
   p->nf = p->N[S - 1] > 128 ? 256 : 128;
   int wmax = 0;
-  c.kpan[0] = static_cast<int>((p->K + 63) / 64);
+  // 128-byte K panels of the first GEMM: 64 16-bit or 32 tf32 elements
+  c.kpan[0] = static_cast<int>(p->tf0 ? (p->K + 31) / 32 : (p->K + 63) / 64);
   for (int s = 0; s < S - 1; ++s) {
     const int w = static_cast<int>((p->N[s] + 127) / 128 * 128);
     if (w > 512) return B2B_ERR_UNSUPPORTED;
@@ -250,9 +252,9 @@ b2b_status_t setup_chainn(b2b_plan_s* p) {
   if (p->smem_bytes > kSmemOptin) return B2B_ERR_UNSUPPORTED;
   // a weight whose width is a multiple of 64 is read in 4-D boxes
   c.w_merged = 0;
-  for (int s = 0; s < S; ++s)
+  for (int s = p->tf0 ? 1 : 0; s < S; ++s)
     if (p->N[s] % 64 == 0) c.w_merged |= 1 << s;
-  const ChainNEntry* e = find_chainn_kernel(p->in_kind, p->out_kind, p->nf);
+  const ChainNEntry* e = find_chainn_kernel(p->in_kind, p->out_kind, p->nf, p->tf0);
   if (!e) return B2B_ERR_UNSUPPORTED;
   p->fn = e->fn;
   p->threads = kChainNThreads;
@@ -266,7 +268,7 @@ b2b_status_t setup_chainn(b2b_plan_s* p) {
 // regions, shared-memory carve-up, and whether the weights stay resident.
 b2b_status_t setup_chain_tc(b2b_plan_s* p) {
   const int S = p->stages;
-  if (p->in_kind != kInTF32 && (S >= 3 || (S == 2 && p->N[0] > 256))) return setup_chainn(p);
+  if (p->tf0 || (p->in_kind != kInTF32 && (S >= 3 || (S == 2 && p->N[0] > 256)))) return setup_chainn(p);
   p->sn = false;
   const int CK = 128 / p->esz;
   const int64_t wmin = 64;
@@ -524,6 +526,16 @@ b2b_status_t validate_sizes(b2b_dtype_t dt, int stages, int64_t batch, int64_t M
         if (N[s] > 4096) return B2B_ERR_UNSUPPORTED;
       }
       return B2B_OK;
+    case B2B_TF32_F16:
+    case B2B_TF32_BF16:
+      if (stages < 2 || batch > 32767) return B2B_ERR_UNSUPPORTED;
+      if (K % 4) return B2B_ERR_UNSUPPORTED;
+      for (int s = 0; s < stages; ++s) {
+        if (N[s] % 8) return B2B_ERR_UNSUPPORTED;
+        if (s < stages - 1 && N[s] > 512) return B2B_ERR_UNSUPPORTED;
+        if (N[s] > 4096) return B2B_ERR_UNSUPPORTED;
+      }
+      return B2B_OK;
     case B2B_TF32:
       if (stages > 2 || batch > 32767) return B2B_ERR_UNSUPPORTED;
       if (K % 4) return B2B_ERR_UNSUPPORTED;
@@ -551,6 +563,10 @@ void type_info(b2b_dtype_t dt, int* in_kind, int* out_kind, int* esz, int* osz) 
     case B2B_BF16: *in_kind = kInBF16; *out_kind = kOutBF16; *esz = 2; *osz = 2; break;
     case B2B_BF16_F32OUT: *in_kind = kInBF16; *out_kind = kOutF32; *esz = 2; *osz = 4; break;
     case B2B_TF32: *in_kind = kInTF32; *out_kind = kOutF32; *esz = 4; *osz = 4; break;
+    // mixed: the type of the intermediates and of the later weights (the
+    // first GEMM's fp32 operands are described by the plan's tf0 flag)
+    case B2B_TF32_F16: *in_kind = kInF16; *out_kind = kOutF32; *esz = 2; *osz = 4; break;
+    case B2B_TF32_BF16: *in_kind = kInBF16; *out_kind = kOutF32; *esz = 2; *osz = 4; break;
     default: *in_kind = -1; *out_kind = -1; *esz = 8; *osz = 8; break;
   }
 }
@@ -559,7 +575,7 @@ b2b_status_t create_common(b2b_plan_t* out, b2b_dtype_t dt, int stages, bool sin
                            int64_t batch, int64_t M, int64_t K, const int64_t* N) {
   if (!out) return B2B_ERR_INVALID_ARG;
   *out = nullptr;
-  if (dt < B2B_F16_F32OUT || dt > B2B_BF16_F32OUT) return B2B_ERR_INVALID_ARG;
+  if (dt < B2B_F16_F32OUT || dt > B2B_TF32_BF16) return B2B_ERR_INVALID_ARG;
   b2b_status_t st = validate_sizes(dt, stages, batch, M, K, N);
   if (st != B2B_OK) return st;
   int dev = 0, sms = 0;
@@ -578,6 +594,7 @@ b2b_status_t create_common(b2b_plan_t* out, b2b_dtype_t dt, int stages, bool sin
   for (int s = 0; s < kMaxStages; ++s) p->N[s] = s < stages ? N[s] : 0;
   p->budget_ns = kDefaultBudgetNs;
   type_info(dt, &p->in_kind, &p->out_kind, &p->esz, &p->osz);
+  p->tf0 = dt == B2B_TF32_F16 || dt == B2B_TF32_BF16;
   if (batch == 0 || M == 0) {
     // An empty chain: valid, and every run is a no-op.
     p->kind = kPlanEmpty;
@@ -605,9 +622,11 @@ b2b_status_t create_common(b2b_plan_t* out, b2b_dtype_t dt, int stages, bool sin
       st = B2B_ERR_CUDA;
     }
   }
-  if (st == B2B_OK && dt == B2B_TF32 && p->kind != kPlanEmpty) {
+  if (st == B2B_OK && (dt == B2B_TF32 || p->tf0) && p->kind != kPlanEmpty) {
+    // workspace for the weights transposed to [N][K] (tf32: every weight;
+    // mixed: the first)
     int64_t words = 0, kin = K;
-    for (int s = 0; s < stages; ++s) {
+    for (int s = 0; s < (p->tf0 ? 1 : stages); ++s) {
       words += batch * kin * N[s];
       kin = N[s];
     }
@@ -717,8 +736,17 @@ b2b_status_t encode_chain_maps(b2b_plan_s* p, const void* const* W, const void* 
       kin = p->N[s];
     }
   } else if (p->sn) {
+    if (p->tf0 && st == B2B_OK) {
+      // mixed: fp32 A in panels of 32 elements; W0 as transposed into the
+      // workspace ([N1][K] per batch), boxes of this CTA's rows of a pass
+      st = encode_3d(&maps->a, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, A, p->K, p->M, p->batch, 32, 128);
+      if (st == B2B_OK)
+        st = encode_3d(&maps->w[0], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, p->d_wt, p->K, p->N[0], p->batch, 32,
+                       static_cast<uint32_t>(p->pn.pw[0] / 2));
+      kin = p->N[0];
+    }
     // CTA pairs: each CTA loads half of a pass's 64-column blocks
-    for (int s = 0; s < S && st == B2B_OK; ++s) {
+    for (int s = p->tf0 ? 1 : 0; s < S && st == B2B_OK; ++s) {
       if ((p->pn.w_merged >> s) & 1) {
         // a box of this CTA's column blocks of a pass, over one K panel, or
         // two for 128-column passes after the first GEMM
@@ -754,16 +782,17 @@ b2b_status_t encode_chain_maps(b2b_plan_s* p, const void* const* W, const void* 
 b2b_status_t run_chain_tc(b2b_plan_s* p, const void* const* W, const void* A, void* D,
                           cudaStream_t stream) {
   const int S = p->stages;
-  if (p->in_kind == kInTF32) {
-    // The tf32 MMA reads B K-major: transpose every weight to [N][K] first.
+  if (p->in_kind == kInTF32 || p->tf0) {
+    // The tf32 MMA reads B K-major: transpose every tf32 weight to [N][K]
+    // first (mixed cascades: W0 only).
     TransposeJob job;
     std::memset(&job, 0, sizeof(job));
     job.batch = static_cast<int>(p->batch);
-    job.count = S;
+    job.count = p->tf0 ? 1 : S;
     uint32_t* dst = static_cast<uint32_t*>(p->d_wt);
     int64_t kin = p->K;
     int max_r = 0, max_c = 0;
-    for (int s = 0; s < S; ++s) {
+    for (int s = 0; s < job.count; ++s) {
       job.in[s] = static_cast<const uint32_t*>(W[s]);
       job.out[s] = dst;
       job.rows[s] = static_cast<int>(kin);
@@ -773,7 +802,7 @@ b2b_status_t run_chain_tc(b2b_plan_s* p, const void* const* W, const void* A, vo
       dst += p->batch * kin * p->N[s];
       kin = p->N[s];
     }
-    const dim3 grid((max_c + 31) / 32, (max_r + 31) / 32, static_cast<unsigned>(S * p->batch));
+    const dim3 grid((max_c + 31) / 32, (max_r + 31) / 32, static_cast<unsigned>(job.count * p->batch));
     void* targs[1] = {&job};
     if (launch_pdl(reinterpret_cast<const void*>(&transpose32_kernel), grid, dim3(256), targs, 0,
                    stream) != cudaSuccess) {
@@ -859,12 +888,14 @@ b2b_status_t run_checked(b2b_plan_s* p, const void* A, const void* const* W, voi
   for (int s = 0; s < S; ++s)
     if (reinterpret_cast<uintptr_t>(W[s]) & 15u) return B2B_ERR_ALIGNMENT;
   if (reinterpret_cast<uintptr_t>(D) & 15u) return B2B_ERR_ALIGNMENT;
-  const size_t e = static_cast<size_t>(p->esz);
+  // element sizes: A and W[0] are fp32 in a mixed-type cascade
+  const size_t e = static_cast<size_t>(p->esz), e0 = p->tf0 ? 4u : e;
   const size_t dbytes = static_cast<size_t>(p->batch * p->M * p->N[S - 1]) * p->osz;
-  if (overlaps(D, dbytes, A, static_cast<size_t>(p->batch * p->M * p->K) * e)) return B2B_ERR_ALIAS;
+  if (overlaps(D, dbytes, A, static_cast<size_t>(p->batch * p->M * p->K) * e0)) return B2B_ERR_ALIAS;
   int64_t kin = p->K;
   for (int s = 0; s < S; ++s) {
-    if (overlaps(D, dbytes, W[s], static_cast<size_t>(p->batch * kin * p->N[s]) * e)) return B2B_ERR_ALIAS;
+    if (overlaps(D, dbytes, W[s], static_cast<size_t>(p->batch * kin * p->N[s]) * (s == 0 ? e0 : e)))
+      return B2B_ERR_ALIAS;
     kin = p->N[s];
   }
   int dev = -1;
@@ -1122,6 +1153,7 @@ extern "C" b2b_status_t b2b_run_tf32_noalloc(int64_t batch, int64_t M, int64_t K
   pl.N[1] = N2;
   pl.budget_ns = kDefaultBudgetNs;
   pl.debug = 0;
+  pl.tf0 = false;
   pl.d_status = nullptr;
   pl.d_wt = scratch;
   pl.wt_bytes = kNoAllocScratchWords * sizeof(uint32_t);

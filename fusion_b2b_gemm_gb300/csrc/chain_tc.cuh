@@ -643,9 +643,10 @@ __global__ void __launch_bounds__(kChainThreads, 1)
               tc_fence_after();
             }
           }
-          if constexpr (P_TMEM) {
+          if constexpr (P_TMEM && S >= 2) {
             // The intermediate of the previous tile (in region X) must be fully
-            // read by GEMM2 before GEMM1 of this tile overwrites X.
+            // read by GEMM2 before GEMM1 of this tile overwrites X.  (A single
+            // GEMM has no intermediate, and nothing completes this barrier.)
             if (it > 0 && !bw.wait(bar(kBarPEmpty), static_cast<uint32_t>(it - 1) & 1u)) return false;
           }
         }

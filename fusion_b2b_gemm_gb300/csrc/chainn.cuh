@@ -159,7 +159,12 @@ __device__ __forceinline__ uint32_t tmem_col(uint32_t r0, int c) {
   return ((((static_cast<uint32_t>(c) >> 8) ^ r0) & 1u) << 8) | (static_cast<uint32_t>(c) & 255u);
 }
 
-template <int IN, int OUT, int NF>
+// TF0: the first GEMM takes fp32 A and W0 as tf32 operands (W0 transposed to
+// [N][K], K-major, which the tf32 MMA reads), and its result is rounded to
+// the 16-bit type IN of every later GEMM: a mixed-type cascade, where the
+// accumulator and operand layouts of the first hand-over differ in element
+// size as well as in order.
+template <int IN, int OUT, int NF, bool TF0 = false>
 __global__ void __launch_bounds__(kChainNThreads, 1)
     chainn_kernel(const __grid_constant__ ChainNMaps maps, const __grid_constant__ ChainNParams p) {
   using namespace ptx;
@@ -167,6 +172,7 @@ __global__ void __launch_bounds__(kChainNThreads, 1)
   static_assert(NF == 128 || NF == 256, "pass width of the last GEMM");
   constexpr int CG = 2;
   constexpr int CK = 64;           // K elements per 128-byte panel
+  constexpr int CK0 = TF0 ? 32 : CK;  // of the first GEMM's operands
   constexpr int KSTEP = 16;        // K of one MMA
   constexpr int WBOX_N = 64;       // weight columns per 128-byte block
   constexpr int WBOX_BYTES = CK * 128;
@@ -264,11 +270,14 @@ __global__ void __launch_bounds__(kChainNThreads, 1)
         // test support: the very first slot is armed but never filled
         if (!((p.debug & 1u) && issued == 0)) {
           if (s < 0) {
-            tma_load_3d_pair(dst, &maps.a, fb, kb * CK, m0, b);
+            tma_load_3d_pair(dst, &maps.a, fb, kb * CK0, m0, b);
           } else {
             const CUtensorMap* wm = &maps.w[s];
             const int n0 = col0 + static_cast<int>(rank) * wcols;
-            if ((p.w_merged >> s) & 1) {
+            if (TF0 && s == 0) {
+              // W0 transposed: this CTA's wcols rows of 32 K elements
+              tma_load_3d_pair(dst, wm, fb, kb * CK0, n0, b);
+            } else if ((p.w_merged >> s) & 1) {
               // one box of npan * 64 K rows and wcols / 64 column blocks
               tma_load_4d_pair(dst, wm, fb, 0, kb * CK, n0 / WBOX_N, b);
             } else {
@@ -293,7 +302,7 @@ __global__ void __launch_bounds__(kChainNThreads, 1)
         // GEMM: pull the next unit's A into L2 now
         if (it + 1 < t_count) {
           const ChainNUnit n = chainn_unit(p, cid, ncl, it + 1);
-          for (int q = 0; q < p.kpan[0]; ++q) tma_prefetch_l2_3d(&maps.a, q * CK, row0(n.mt), n.b);
+          for (int q = 0; q < p.kpan[0]; ++q) tma_prefetch_l2_3d(&maps.a, q * CK0, row0(n.mt), n.b);
         }
         for (int s = 0; s < S - 1 && ok; ++s) {
           const int pw = p.pw[s], kps = kps_of(s);
@@ -371,14 +380,14 @@ __global__ void __launch_bounds__(kChainNThreads, 1)
           }
         }
       };
-      // Four MMAs per 64-element K panel.  First GEMM (a_smem): the A panel
-      // is in this slot and the weight half panel in the next; later GEMMs
-      // read K panels kb .. kb + npan - 1 of the operand image (their weight
-      // half panels share one slot), after waiting for the chunk barrier
-      // `chunk` (if >= 0) with parity cpar.
-      auto stage_mmas = [&](auto npan_c, uint32_t d, uint32_t idesc, bool a_smem, int kb, int chunk,
-                            uint32_t cpar) -> bool {
+      // Four MMAs per 128-byte K panel.  First GEMM (npan == 0): the A
+      // panel is in this slot and the weight half panel in the next; later
+      // GEMMs read K panels kb .. kb + npan - 1 of the operand image (their
+      // weight half panels share one slot), after waiting for the chunk
+      // barrier `chunk` (if >= 0) with parity cpar.
+      auto stage_mmas = [&](auto npan_c, uint32_t d, uint32_t idesc, int kb, int chunk, uint32_t cpar) -> bool {
         constexpr int npan = decltype(npan_c)::value;
+        constexpr bool a_smem = npan == 0;
         const uint32_t need = a_smem ? 2u : 1u;
         if (!stage_ready(need)) return false;
         if (chunk >= 0 && !bwm.wait(bar(chunk), cpar)) return false;
@@ -392,7 +401,13 @@ __global__ void __launch_bounds__(kChainNThreads, 1)
         const uint32_t acc0 = kb != 0 ? 1u : 0u;
         // (straight-line MMAs: a branch between two of them costs more than
         // the tensor pipe's queue hides)
-        if constexpr (npan == 2) {
+        if constexpr (a_smem && TF0) {
+          // tf32: 8 K elements (32 bytes) per MMA, B K-major like A
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            mma_ss<true, CG>(d, desc_sw128(sa + kk * 32u, 16u, 1024u), desc_sw128(wb + kk * 32u, 16u, 1024u), idesc,
+                             kk ? 1u : acc0);
+        } else if constexpr (npan == 2) {
 #pragma unroll
           for (int kk = 0; kk < 2 * (CK / KSTEP); ++kk) {
             const uint32_t pa = static_cast<uint32_t>(kk >> 2), ks = static_cast<uint32_t>(kk & 3);
@@ -419,14 +434,16 @@ __global__ void __launch_bounds__(kChainNThreads, 1)
         if (!first_pass || (kb & 1)) return -1;
         return knPChunk + static_cast<int>(((k - 1u) & 1u) * 4u) + kb / 2;
       };
-      // one pass: kpan K panels, npan of them per ring slot
-      auto run_pass = [&](auto npan_c, uint32_t d, uint32_t idesc, bool a_smem, int kpan, bool first,
-                          uint32_t cpar) -> bool {
+      // one pass: kpan K panels, npan of them per ring slot (0: the first
+      // GEMM, one K panel and two slots)
+      auto run_pass = [&](auto npan_c, uint32_t d, uint32_t idesc, int kpan, bool first, uint32_t cpar) -> bool {
         constexpr int npan = decltype(npan_c)::value;
-        for (int kb = 0; kb < kpan; kb += npan)
-          if (!stage_mmas(npan_c, d, idesc, a_smem, kb, a_smem ? -1 : chunk_of(first, kb), cpar)) return false;
+        constexpr int step = npan == 0 ? 1 : npan;
+        for (int kb = 0; kb < kpan; kb += step)
+          if (!stage_mmas(npan_c, d, idesc, kb, npan == 0 ? -1 : chunk_of(first, kb), cpar)) return false;
         return true;
       };
+      using First = integral_constant_int<0>;
       using One = integral_constant_int<1>;
       using Two = integral_constant_int<2>;
       for (int it = 0; it < t_count && ok; ++it) {
@@ -434,7 +451,8 @@ __global__ void __launch_bounds__(kChainNThreads, 1)
         for (int s = 0; s < S - 1 && ok; ++s) {
           const int pw = p.pw[s];
           const uint32_t r0 = rc.take(p.wpad[s]);
-          const uint32_t idesc = make_idesc(FMT, static_cast<uint32_t>(pw), 256u, true);
+          const uint32_t idesc = (TF0 && s == 0) ? make_idesc(2u, static_cast<uint32_t>(pw), 256u, false)
+                                                 : make_idesc(FMT, static_cast<uint32_t>(pw), 256u, true);
           const uint32_t cpar = ((k - 1u) >> 1) & 1u;
           int touched = 0;
           for (int col0 = 0; col0 < p.wpad[s] && ok; col0 += pw) {
@@ -446,8 +464,12 @@ __global__ void __launch_bounds__(kChainNThreads, 1)
               if (!ok) break;
               tc_fence_after();
             }
-            ok = kps_of(s) == 2 ? run_pass(Two{}, tmem_base + col, idesc, s == 0, p.kpan[s], col0 == 0, cpar)
-                                : run_pass(One{}, tmem_base + col, idesc, s == 0, p.kpan[s], col0 == 0, cpar);
+            if (s == 0)
+              ok = run_pass(First{}, tmem_base + col, idesc, p.kpan[s], col0 == 0, cpar);
+            else if (kps_of(s) == 2)
+              ok = run_pass(Two{}, tmem_base + col, idesc, p.kpan[s], col0 == 0, cpar);
+            else
+              ok = run_pass(One{}, tmem_base + col, idesc, p.kpan[s], col0 == 0, cpar);
             // the first GEMM reads no operand image, so each of its passes
             // can be converted as soon as it completes (every MMA that read
             // the image, the previous tile's last GEMM, completed before it)
@@ -467,8 +489,8 @@ __global__ void __launch_bounds__(kChainNThreads, 1)
           ok = take_region(r);
           if (!ok) break;
           tc_fence_after();
-          ok = kps_last == 2 ? run_pass(Two{}, tmem_base + col, idesc, false, kpan_last, j == c.p0, cpar)
-                             : run_pass(One{}, tmem_base + col, idesc, false, kpan_last, j == c.p0, cpar);
+          ok = kps_last == 2 ? run_pass(Two{}, tmem_base + col, idesc, kpan_last, j == c.p0, cpar)
+                             : run_pass(One{}, tmem_base + col, idesc, kpan_last, j == c.p0, cpar);
           if (!ok) break;
           tc_commit<CG>(bar(knRFull + r));
         }

@@ -27,6 +27,7 @@ ChainTable chain_table_tf32();
 // stages, or two with an intermediate wider than 256 columns.
 struct ChainNEntry {
   int in, out, nf;
+  bool tf0;  // first GEMM on tf32 operands (mixed-type cascade)
   const void* fn;
 };
 struct ChainNTable {
@@ -40,5 +41,5 @@ ChainNTable chainn_table_bf16();
 
 #define B2B_CHAIN_ENTRY(IN, OUT, S, A, B, F, R) \
   { IN, OUT, S, A, B, F, R, reinterpret_cast<const void*>(&::b2b::chain_tc_kernel<IN, OUT, S, A, B, F, R>) }
-#define B2B_CHAINN_ENTRY(IN, OUT, F) \
-  { IN, OUT, F, reinterpret_cast<const void*>(&::b2b::chainn_kernel<IN, OUT, F>) }
+#define B2B_CHAINN_ENTRY(IN, OUT, F, T) \
+  { IN, OUT, F, T, reinterpret_cast<const void*>(&::b2b::chainn_kernel<IN, OUT, F, T>) }

@@ -68,7 +68,12 @@ typedef enum {
   B2B_BF16 = 2,        /* bf16 in, bf16 intermediates, bf16 out            */
   B2B_TF32 = 3,        /* fp32 storage, tf32 operands and intermediate, fp32 out */
   B2B_F64 = 4,         /* fp64 throughout                                   */
-  B2B_BF16_F32OUT = 5  /* bf16 in, bf16 intermediates, fp32 out            */
+  B2B_BF16_F32OUT = 5, /* bf16 in, bf16 intermediates, fp32 out           */
+  /* Mixed-type cascades (two or more stages): A and W[0] in fp32 storage,
+   * multiplied as tf32 operands; every intermediate and every later weight
+   * fp16 (B2B_TF32_F16) or bf16 (B2B_TF32_BF16); fp32 out. */
+  B2B_TF32_F16 = 6,
+  B2B_TF32_BF16 = 7
 } b2b_dtype_t;
 
 /*
@@ -87,6 +92,10 @@ typedef enum {
  *                 last width <= 4096 (the last GEMM runs in passes of up to
  *                 256 columns).
  *   B2B_TF32:     two stages; K % 4 == 0; N1 <= 256; N1, N2 % 4 == 0.
+ *   B2B_TF32_F16, B2B_TF32_BF16: two or more stages; K % 4 == 0; every
+ *                 width % 8 == 0; intermediate widths <= 512, the last
+ *                 <= 4096.  A plan allocates a workspace for W[0] transposed
+ *                 (batch * K * N1 * 4 bytes); a run launches two kernels.
  *   B2B_F64:      two stages; K % 4 == 0; N1, N2 in {16, 32, 64}.
  * Binds to the current CUDA device, which must be an sm_103 GPU
  * (B2B_ERR_DEVICE otherwise).  Allocates one 4-byte device status word.

@@ -90,6 +90,12 @@ def _create_chain(dtype, batch, M, K, widths, n=None):
     ((1, 1, 64, 64, (64, 60, 64, 64)), 2),           # width not a multiple of 8
     ((3, 1, 64, 64, (64, 64, 64)), 2),               # tf32 three stages
     ((4, 1, 64, 64, (16, 16, 16)), 2),               # fp64 three stages
+    ((6, 1, 64, 64, (64, 64, 64)), 0),               # tf32 first GEMM, fp16 after it
+    ((7, 2, 64, 96, (512, 64)), 0),                  # tf32 then bf16, wide intermediate
+    ((6, 1, 64, 64, (64,)), 2),                      # a mixed cascade needs two stages
+    ((7, 1, 64, 66, (64, 64)), 2),                   # fp32 rows not 16-byte aligned
+    ((6, 1, 64, 64, (68, 64)), 2),                   # 16-bit width not a multiple of 8
+    ((8, 1, 64, 64, (64, 64)), 1),                   # unknown dtype
 ])
 def test_chain_plan_create_validates_before_device(args, code):
     got, h = _create_chain(*args)

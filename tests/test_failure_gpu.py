@@ -22,8 +22,8 @@ b2b = pytest.importorskip("fusion_b2b_gemm_gb300")
 
 TIMEOUT = 7
 KINDS = {"f16": (oracle.F32, oracle.F16, oracle.F16), "bf16": (oracle.F32, oracle.BF16, oracle.BF16),
-         "tf32": (oracle.F32, oracle.TF32, oracle.F32)}
-TOL = {"f16": 1e-2, "bf16": 1e-2, "tf32": 5e-3}
+         "tf32": (oracle.F32, oracle.TF32, oracle.F32), "tf32_bf16": (oracle.F32, oracle.BF16, oracle.F32)}
+TOL = {"f16": 1e-2, "bf16": 1e-2, "tf32": 5e-3, "tf32_bf16": 1e-2}
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -38,6 +38,7 @@ CASES = [
     wl.Workload("fail_stream_bf16_3", "bf16", 1, 384, 512, (256, 256, 512), "normal_fanin", 1.0, 52),
     wl.Workload("fail_tf32", "tf32", 1, 384, 256, (256, 256), "normal", 1.0 / 16, 53),
     wl.Workload("fail_deep5_f16", "f16", 1, 600, 128, (256, 512, 128, 256, 384), "normal_fanin", 1.0, 54),
+    wl.Workload("fail_mixed_bf16", "tf32_bf16", 1, 400, 64, (256, 128, 256), "normal_fanin", 1.0, 55),
 ]
 
 

@@ -27,8 +27,12 @@ KINDS = {
     "bf16_f32out": (oracle.F32, oracle.BF16, oracle.F32),
     "tf32": (oracle.F32, oracle.TF32, oracle.F32),
     "f64": (oracle.NONE, oracle.NONE, oracle.NONE),
+    # mixed: tf32 first GEMM, 16-bit intermediates and later GEMMs, fp32 out
+    "tf32_f16": (oracle.F32, oracle.F16, oracle.F32),
+    "tf32_bf16": (oracle.F32, oracle.BF16, oracle.F32),
 }
-TOL = {"f16_f32out": 1e-2, "f16": 1e-2, "bf16": 1e-2, "bf16_f32out": 1e-2, "tf32": 5e-3, "f64": 1e-12}
+TOL = {"f16_f32out": 1e-2, "f16": 1e-2, "bf16": 1e-2, "bf16_f32out": 1e-2, "tf32": 5e-3, "f64": 1e-12,
+       "tf32_f16": 1e-2, "tf32_bf16": 1e-2}
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -96,6 +100,10 @@ EXACT = [
     wl.Workload("x_f16_f32out_5", "f16_f32out", 1, 520, 16, (16, 16, 16, 16, 128), "int", 1, 20),
     wl.Workload("x_bf16_wide384", "bf16", 1, 300, 32, (384, 64), "int", 1, 41),
     wl.Workload("x_bf16_wide512_3", "bf16", 1, 260, 16, (512, 16, 256), "int", 1, 42),
+    # mixed types: tf32 first GEMM (integers below 2^10 are exact in tf32),
+    # then fp16 / bf16
+    wl.Workload("x_tf32_f16_2", "tf32_f16", 2, 300, 64, (128, 64), "int", 2, 71),
+    wl.Workload("x_tf32_bf16_4", "tf32_bf16", 1, 520, 32, (256, 32, 32, 256), "int", 1, 72),
 ]
 
 
@@ -160,6 +168,12 @@ EDGES = [
     wl.Workload("wide512_bf16_2", "bf16", 1, 300, 96, (512, 1000), "normal_fanin", 1.0, 47),
     wl.Workload("wide_tail_f16_4", "f16", 1, 129, 72, (264, 40, 392, 8), "normal_fanin", 1.0, 48),
     wl.Workload("streamed_many_bf16_4", "bf16", 1, 40000, 128, (128, 128, 128, 512), "normal_fanin", 1.0, 49),
+    # mixed types: ragged K (a partial 32-element tf32 panel), wide first
+    # intermediate, several stages, more tiles than clusters
+    wl.Workload("mixed_f16_ktail", "tf32_f16", 2, 333, 200, (256, 136), "normal_fanin", 1.0, 73),
+    wl.Workload("mixed_bf16_wide", "tf32_bf16", 1, 300, 128, (512, 128, 384), "normal_fanin", 1.0, 74),
+    wl.Workload("mixed_f16_5", "tf32_f16", 1, 700, 96, (128, 256, 128, 256, 72), "normal_fanin", 1.0, 75),
+    wl.Workload("mixed_bf16_many", "tf32_bf16", 1, 30000, 256, (256, 256), "normal_fanin", 1.0, 76),
 ]
 
 
@@ -254,10 +268,14 @@ def test_argument_errors_on_device():
 
 # ------------------------------------------ unfused reference building block --
 
-@pytest.mark.parametrize("dtype,K,N", [("f16", 128, 128), ("f16_f32out", 64, 64), ("bf16", 256, 512),
-                                       ("tf32", 256, 256), ("f64", 64, 64)])
-def test_single_gemm_plan(dtype, K, N):
-    w = wl.Workload("gemm", dtype, 2, 300, K, (N,), "normal", 0.2, 31)
+@pytest.mark.parametrize("dtype,K,N,M", [("f16", 128, 128, 300), ("f16_f32out", 64, 64, 300),
+                                         ("bf16", 256, 512, 300), ("tf32", 256, 256, 300), ("f64", 64, 64, 300),
+                                         # more tiles than SMs: A through its own ring, several
+                                         # tiles per CTA
+                                         ("tf32", 256, 256, 20000), ("tf32", 128, 512, 20000),
+                                         ("bf16_f32out", 256, 256, 20000), ("f16", 64, 384, 20000)])
+def test_single_gemm_plan(dtype, K, N, M):
+    w = wl.Workload("gemm", dtype, 2, M, K, (N,), "normal", 0.2, 31)
     host = wl.make_inputs(w)
     plan = b2b.GemmPlan(dtype, w.batch, w.M, K, N)
     dev = [t.cuda() for t in host]

@@ -17,7 +17,7 @@ from typing import Dict, List, Optional, Tuple
 import numpy as np
 
 # Storage / compute types of a chain.  The names match the C enum b2b_dtype_t.
-DTYPES = ("f16_f32out", "f16", "bf16", "tf32", "f64", "bf16_f32out")
+DTYPES = ("f16_f32out", "f16", "bf16", "tf32", "f64", "bf16_f32out", "tf32_f16", "tf32_bf16")
 
 # torch dtypes for (inputs, output); resolved lazily so that this module
 # imports without torch.
@@ -28,13 +28,26 @@ _IO = {
     "bf16_f32out": ("bfloat16", "float32"),
     "tf32": ("float32", "float32"),
     "f64": ("float64", "float64"),
+    # mixed: fp32 A and first weight (tf32 operands), 16-bit later weights
+    "tf32_f16": ("float32", "float32"),
+    "tf32_bf16": ("float32", "float32"),
 }
+# storage type of the weights after the first, where it differs from A's
+_LATER = {"tf32_f16": "float16", "tf32_bf16": "bfloat16"}
 
 
 def io_dtypes(dtype: str):
     import torch
     a, b = _IO[dtype]
     return getattr(torch, a), getattr(torch, b)
+
+
+def input_dtypes(dtype: str, stages: int):
+    """torch storage types of [A, W1, ..., W_stages]."""
+    import torch
+    a, _ = _IO[dtype]
+    later = _LATER.get(dtype, a)
+    return [getattr(torch, a), getattr(torch, a)] + [getattr(torch, later)] * (stages - 1)
 
 
 @dataclasses.dataclass(frozen=True)
@@ -77,15 +90,19 @@ class Workload:
         i, o = io_dtypes(self.dtype)
         return (torch.empty((), dtype=i).element_size(), torch.empty((), dtype=o).element_size())
 
+    def input_elem_bytes(self) -> List[int]:
+        import torch
+        return [torch.empty((), dtype=t).element_size() for t in input_dtypes(self.dtype, self.stages)]
+
     def unique_bytes(self) -> int:
         """Inputs and output, each once; the intermediates are not counted."""
-        ei, eo = self.elem_bytes()
-        n_in = sum(int(np.prod(s)) for s in self.shapes())
-        return n_in * ei + int(np.prod(self.out_shape())) * eo
+        _, eo = self.elem_bytes()
+        n_in = sum(int(np.prod(s)) * e for s, e in zip(self.shapes(), self.input_elem_bytes()))
+        return n_in + int(np.prod(self.out_shape())) * eo
 
     def intermediate_bytes(self) -> int:
         """Bytes an unfused chain writes and reads back for its intermediates."""
-        ei, _ = self.elem_bytes()
+        ei = self.input_elem_bytes()[-1]
         return sum(2 * self.batch * self.M * n * ei for n in self.N[:-1])
 
     def with_(self, **kw) -> "Workload":
@@ -114,6 +131,10 @@ EXTRA_WORKLOADS: Dict[str, Workload] = {
                                 "normal_fanin", 1.0, 5, "bf16 in/out, three bf16 intermediates"),
     "wide_f16": Workload("wide_f16", "f16", 8, 8192, 128, (512, 128), "normal_fanin", 1.0, 6,
                          "fp16 in/out, one 512-column fp16 intermediate"),
+    "mixed_tf32_bf16": Workload("mixed_tf32_bf16", "tf32_bf16", 1, 65536, 256, (256, 256, 256),
+                                "normal_fanin", 1.0, 7,
+                                "fp32 A and first weight (tf32 GEMM), bf16 intermediates and later "
+                                "weights, fp32 out"),
 }
 
 ALL_WORKLOADS: Dict[str, Workload] = {**WORKLOADS, **EXTRA_WORKLOADS}
@@ -139,10 +160,11 @@ def make_inputs(w: Workload, seed: Optional[int] = None):
     """Seeded CPU tensors [A, W1, W2(, W3)] in the workload's storage type."""
     import torch
     rng = np.random.default_rng(w.seed if seed is None else seed)
-    in_dt, _ = io_dtypes(w.dtype)
+    dts = input_dtypes(w.dtype, w.stages)
     out = []
     fan = [w.K, w.K] + list(w.N[:-1])        # A, W1, W2, W3 consumers' K
     for idx, shp in enumerate(w.shapes()):
+        in_dt = dts[idx]
         x = _draw(rng, shp, w.dist, w.scale, fan[idx])
         if in_dt == torch.float64:
             t = torch.from_numpy(x)

@@ -177,6 +177,9 @@ struct b2b_plan_s {
   // tf32 only: the weights transposed to [N][K] before every run
   void* d_wt;
   size_t wt_bytes;
+  // resident weights: the tile schedule (host copy, then device copy)
+  std::vector<int> sched_host;
+  int* d_sched;
   // Encoded tensor maps of recent runs, keyed by the pointer set (encoding
   // costs host time on every call otherwise).  Guarded by `mu`.
   struct MapSet {
@@ -191,6 +194,8 @@ struct b2b_plan_s {
 };
 
 namespace {
+
+std::vector<int> res_schedule(int64_t batch, int64_t m_tiles, int G);
 
 // Cascades of 16-bit GEMMs on CTA pairs (chainn_kernel): 256-row tiles,
 // intermediates padded to a multiple of 128 columns (at most 512), every GEMM
@@ -429,7 +434,72 @@ b2b_status_t setup_chain_tc(b2b_plan_s* p) {
   p->fn = e->fn;
   p->threads = kChainThreads;
   p->grid = static_cast<int>(std::min<int64_t>(c.total_tiles, p->sms));
+  c.sched = nullptr;
+  p->sched_host.clear();
+  if (p->res) p->sched_host = res_schedule(p->batch, c.m_tiles, p->grid);
   return B2B_OK;
+}
+
+// Tile schedule for resident weights.  A CTA's weights change only where its
+// tiles cross into another batch, and a change drains the pipeline: the new
+// weights may replace the old ones only after the old batch's last GEMM2, and
+// their load then queues behind the A tiles in flight -- about kSwitchTiles
+// tiles' time on a GB300 (batched_f16: 3.3 us per change against 1.1 us per
+// tile, measured per CTA).  The default split (one contiguous range of
+// ceil(T / G) tiles per CTA) makes about a third of the CTAs change batch once.
+// Instead every batch is cut into pieces of L tiles, one CTA each, and the
+// shorter leftovers of consecutive batches are packed into shared CTAs while
+// their tiles plus kSwitchTiles per change stay within L; the smallest L that
+// fits in G CTAs is taken if it beats the default split's largest cost.
+// Returns the table (kSchedStride ints per CTA) or an empty vector.
+constexpr int kSwitchTiles = 3;
+
+std::vector<int> res_schedule(int64_t batch, int64_t m_tiles, int G) {
+  std::vector<int> none;
+  const int64_t T = batch * m_tiles;
+  if (batch < 2 || G < 1 || T <= G) return none;
+  int64_t c_contig = 0;
+  for (int64_t i = 0; i < G; ++i) {
+    const int64_t b0 = i * T / G, b1 = (i + 1) * T / G;
+    if (b1 <= b0) continue;
+    const int64_t changes = (b1 - 1) / m_tiles - b0 / m_tiles;
+    c_contig = std::max(c_contig, (b1 - b0) + kSwitchTiles * changes);
+  }
+  for (int64_t L = (T + G - 1) / G; L < c_contig; ++L) {
+    // pieces of L tiles per batch, then leftovers packed in batch order
+    struct Seg { int64_t first, count; };
+    std::vector<std::vector<Seg>> ctas;
+    std::vector<Seg> pack;
+    int64_t pack_cost = 0;
+    auto flush = [&]() {
+      if (!pack.empty()) ctas.push_back(pack);
+      pack.clear();
+      pack_cost = 0;
+    };
+    for (int64_t b = 0; b < batch && static_cast<int64_t>(ctas.size()) <= G; ++b) {
+      const int64_t full = m_tiles / L, rest = m_tiles - full * L;
+      for (int64_t j = 0; j < full; ++j) ctas.push_back({Seg{b * m_tiles + j * L, L}});
+      if (rest == 0) continue;
+      const Seg s{b * m_tiles + full * L, rest};
+      const int64_t cost = pack.empty() ? rest : pack_cost + kSwitchTiles + rest;
+      if (!pack.empty() && (cost > L || static_cast<int>(pack.size()) == kSchedSegs)) flush();
+      pack_cost = pack.empty() ? rest : pack_cost + kSwitchTiles + rest;
+      pack.push_back(s);
+    }
+    flush();
+    if (static_cast<int64_t>(ctas.size()) > G) continue;
+    std::vector<int> table(static_cast<size_t>(G) * kSchedStride, 0);
+    for (size_t i = 0; i < ctas.size(); ++i) {
+      int* row = table.data() + i * kSchedStride;
+      row[0] = static_cast<int>(ctas[i].size());
+      for (size_t k = 0; k < ctas[i].size(); ++k) {
+        row[1 + 2 * k] = static_cast<int>(ctas[i][k].first);
+        row[2 + 2 * k] = static_cast<int>(ctas[i][k].count);
+      }
+    }
+    return table;
+  }
+  return none;
 }
 
 // A paired chain runs one persistent cluster of two CTAs per tile slot: as
@@ -622,6 +692,16 @@ b2b_status_t create_common(b2b_plan_t* out, b2b_dtype_t dt, int stages, bool sin
       st = B2B_ERR_CUDA;
     }
   }
+  if (st == B2B_OK && !p->sched_host.empty()) {
+    const size_t bytes = p->sched_host.size() * sizeof(int);
+    if (cudaMalloc(&p->d_sched, bytes) != cudaSuccess ||
+        cudaMemcpy(p->d_sched, p->sched_host.data(), bytes, cudaMemcpyHostToDevice) != cudaSuccess) {
+      cudaGetLastError();
+      st = B2B_ERR_CUDA;
+    } else {
+      p->prm.sched = p->d_sched;
+    }
+  }
   if (st == B2B_OK && (dt == B2B_TF32 || p->tf0) && p->kind != kPlanEmpty) {
     // workspace for the weights transposed to [N][K] (tf32: every weight;
     // mixed: the first)
@@ -639,6 +719,7 @@ b2b_status_t create_common(b2b_plan_t* out, b2b_dtype_t dt, int stages, bool sin
   if (st != B2B_OK) {
     if (p->d_status) cudaFree(p->d_status);
     if (p->d_wt) cudaFree(p->d_wt);
+    if (p->d_sched) cudaFree(p->d_sched);
     delete p;
     return st;
   }
@@ -959,6 +1040,7 @@ b2b_status_t b2b_plan_destroy(b2b_plan_t p) {
   if (!p) return B2B_OK;
   if (p->d_status) cudaFree(p->d_status);
   if (p->d_wt) cudaFree(p->d_wt);
+  if (p->d_sched) cudaFree(p->d_sched);
   delete p;
   return B2B_OK;
 }
@@ -1156,6 +1238,7 @@ extern "C" b2b_status_t b2b_run_tf32_noalloc(int64_t batch, int64_t M, int64_t K
   pl.tf0 = false;
   pl.d_status = nullptr;
   pl.d_wt = scratch;
+  pl.d_sched = nullptr;
   pl.wt_bytes = kNoAllocScratchWords * sizeof(uint32_t);
   pl.cache_n = 0;
   pl.clock = 0;

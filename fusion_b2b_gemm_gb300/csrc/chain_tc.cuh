@@ -96,7 +96,13 @@ struct ChainParams {
   uint32_t debug;     // test support: bit 0 = arm the first ring stage but never fill it
   int* status;
   unsigned long long budget_ns;
+  // Resident weights: optional tile schedule, kSchedStride ints per CTA:
+  // the number of segments, then (first tile, tile count) of each, tiles
+  // numbered batch-major; null = one contiguous range per CTA.
+  const int* sched;
 };
+constexpr int kSchedSegs = 4;
+constexpr int kSchedStride = 1 + 2 * kSchedSegs;
 
 // Which tensor-memory region phase `ph` of local tile `it` writes, and how
 // many times that region has been written before (its use index, which the
@@ -275,16 +281,37 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, uint64
 }
 
 // Tiles of one CTA, walked without divisions: batch b and 128-row tile mt.
+// A scheduled CTA walks a list of contiguous segments instead (`segs`: tile
+// count of the current one in `left`, then (first, count) pairs).
 struct TileCursor {
   int b, mt, db, dmt, m_tiles;
+  int left, seg, nseg;
+  const int* segs;
   __device__ __forceinline__ void init(int tile, int step, int mtiles) {
     m_tiles = mtiles;
     b = tile / mtiles;
     mt = tile - b * mtiles;
     db = step / mtiles;
     dmt = step - db * mtiles;
+    segs = nullptr;
+  }
+  __device__ __forceinline__ void init_segments(const int* s, int n, int mtiles) {
+    init(n > 0 ? s[0] : 0, 1, mtiles);
+    segs = s;
+    nseg = n;
+    seg = 0;
+    left = n > 0 ? s[1] : 0;
   }
   __device__ __forceinline__ void next() {
+    if (segs != nullptr && --left == 0) {
+      if (++seg < nseg) {
+        const int t = segs[2 * seg];
+        b = t / m_tiles;
+        mt = t - b * m_tiles;
+        left = segs[2 * seg + 1];
+      }
+      return;
+    }
     mt += dmt;
     b += db;
     if (mt >= m_tiles) {
@@ -385,13 +412,25 @@ __global__ void __launch_bounds__(kChainThreads, 1)
   // (few batch changes), otherwise strided so that concurrent CTAs share the
   // same weights in L2.
   int t_begin, t_step, t_count;
+  const int* my_segs = nullptr;
+  int my_nseg = 0;
   if constexpr (RES) {
-    const long long T = p.total_tiles, G = gridDim.x;
-    const int b0 = static_cast<int>((blockIdx.x * T) / G);
-    const int b1 = static_cast<int>(((blockIdx.x + 1) * T) / G);
-    t_begin = b0;
-    t_step = 1;
-    t_count = b1 - b0;
+    if (p.sched != nullptr) {
+      // a schedule that keeps most CTAs within one batch (see the plan)
+      my_segs = p.sched + blockIdx.x * kSchedStride + 1;
+      my_nseg = p.sched[blockIdx.x * kSchedStride];
+      t_count = 0;
+      for (int i = 0; i < my_nseg; ++i) t_count += my_segs[2 * i + 1];
+      t_begin = my_nseg > 0 ? my_segs[0] : 0;
+      t_step = 1;
+    } else {
+      const long long T = p.total_tiles, G = gridDim.x;
+      const int b0 = static_cast<int>((blockIdx.x * T) / G);
+      const int b1 = static_cast<int>(((blockIdx.x + 1) * T) / G);
+      t_begin = b0;
+      t_step = 1;
+      t_count = b1 - b0;
+    }
   } else {
     t_begin = blockIdx.x;
     t_step = gridDim.x;
@@ -400,7 +439,10 @@ __global__ void __launch_bounds__(kChainThreads, 1)
                   : 0;
   }
   TileCursor first;
-  first.init(t_begin, t_step, p.m_tiles);
+  if (my_segs != nullptr)
+    first.init_segments(my_segs, my_nseg, p.m_tiles);
+  else
+    first.init(t_begin, t_step, p.m_tiles);
   const int nph = NPH_FIXED + p.npass;
   const bool lookahead = p.lookahead != 0;
   // streamed weights with CTAs that run several tiles: A panels come through

@@ -160,6 +160,10 @@ EDGES = [
     wl.Workload("streamed_many_f16", "f16", 1, 40000, 512, (128, 128), "normal_fanin", 1.0, 36),
     wl.Workload("streamed_many_tf32", "tf32", 2, 10000, 96, (64, 64), "normal", 1.0 / 16, 37),
     wl.Workload("streamed_many_bf16_npass", "bf16", 1, 20000, 64, (128, 384), "normal_fanin", 1.0, 38),
+    # resident weights over many batches: the batch-aware tile schedule, with
+    # CTAs that take the leftover tiles of two batches
+    wl.Workload("sched_res_f16", "f16", 40, 2000, 128, (128, 128), "normal_fanin", 1.0, 39),
+    wl.Workload("sched_res_bf16_f32out", "bf16_f32out", 33, 1100, 64, (64, 128), "normal_fanin", 1.0, 40),
     # longer cascades (one kernel for every stage) and wide intermediates
     wl.Workload("deep6_bf16", "bf16", 1, 520, 256, (256, 128, 256, 192, 256, 320), "normal_fanin", 1.0, 43),
     wl.Workload("eight_f16", "f16", 1, 260, 64, (128,) * 7 + (64,), "normal_fanin", 1.0, 44),

@@ -100,6 +100,9 @@ struct ChainParams {
   // the number of segments, then (first tile, tile count) of each, tiles
   // numbered batch-major; null = one contiguous range per CTA.
   const int* sched;
+  // A transpose kernel runs first and lets this kernel start only after the
+  // earlier kernels are complete: A may be read before this kernel's wait.
+  int a_early;
 };
 constexpr int kSchedSegs = 4;
 constexpr int kSchedStride = 1 + 2 * kSchedSegs;
@@ -401,8 +404,16 @@ __global__ void __launch_bounds__(kChainThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  // While the weight transpose in front of this kernel runs, pull this CTA's
+  // first A tile into L2 (only A: the weights are the transpose's output).
+  if (!RES && p.a_early && warp == 0 && lane == 0 && static_cast<int>(blockIdx.x) < p.total_tiles) {
+    const int b = static_cast<int>(blockIdx.x) / p.m_tiles;
+    const int mt = static_cast<int>(blockIdx.x) - b * p.m_tiles;
+    for (int kb = 0; kb < p.kpan0; ++kb) tma_prefetch_l2_3d(&tmA, kb * CK, mt * 128, b);
+  }
   // The prologue above may overlap the previous kernel in the stream; no
-  // global memory is touched before that kernel has completed.
+  // global memory is touched before that kernel has completed (except the
+  // prefetch of A above, see a_early).
   grid_launch_dependents();
   grid_dependency_wait();
 

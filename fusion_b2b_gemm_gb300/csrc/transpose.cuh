@@ -24,8 +24,11 @@ struct TransposeJob {
 
 __global__ void __launch_bounds__(256) transpose32_kernel(const __grid_constant__ TransposeJob job) {
   __shared__ uint32_t tile[32][33];
-  ptx::grid_launch_dependents();
+  // Wait for the earlier kernels first, then let the chain kernel start: its
+  // start then implies that they are complete, so it may read A (which this
+  // kernel does not write) before its own wait.
   ptx::grid_dependency_wait();
+  ptx::grid_launch_dependents();
   const int z = blockIdx.z;
   const int mat = z / job.batch;
   const int b = z % job.batch;

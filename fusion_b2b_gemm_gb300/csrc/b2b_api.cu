@@ -269,8 +269,10 @@ b2b_status_t setup_chainn(b2b_plan_s* p) {
   return B2B_OK;
 }
 
-// Tiling of a tcgen05 chain: padded widths, final-pass width, tensor-memory
-// regions, shared-memory carve-up, and whether the weights stay resident.
+// Tiling of a tcgen05 chain of one or two GEMMs (chain_tc_kernel): padded
+// widths, final-pass width, tensor-memory regions, shared-memory carve-up,
+// and whether the weights stay resident.  Longer cascades, intermediates
+// wider than 256 columns and mixed types go to setup_chainn.
 b2b_status_t setup_chain_tc(b2b_plan_s* p) {
   const int S = p->stages;
   if (p->tf0 || (p->in_kind != kInTF32 && (S >= 3 || (S == 2 && p->N[0] > 256)))) return setup_chainn(p);
@@ -305,9 +307,6 @@ b2b_status_t setup_chain_tc(b2b_plan_s* p) {
   if (nz < 0)
     for (int c : cands)
       if (c >= wmin && c <= nl && base_z + c <= 512) { nf = c; nz = 1; break; }
-  if (nz < 0 && S == 3)
-    for (int c : cands)
-      if (c >= wmin && c <= nl && c <= p->n1p && c <= p->n2p) { nf = c; nz = 0; break; }
   if (nz < 0) return B2B_ERR_UNSUPPORTED;
   if (nf == 0) return B2B_ERR_UNSUPPORTED;
   p->nf = nf;

@@ -167,23 +167,112 @@ class Plan:
         _check(code, "b2b_run")
         return D
 
-    def run_from_host(self, host_inputs: Sequence, host_out, dev_inputs: Sequence, dev_out, stream=None):
+    def run_from_host(self, host_inputs: Sequence, host_out, dev_inputs: Sequence, dev_out, stream=None,
+                      chunks: Optional[int] = None):
         """One end-to-end call from pinned host buffers.
 
         Copies the inputs host->device, runs the chain, copies the result
-        device->host, all on ``stream``; returns (h2d_bytes, d2h_bytes).
-        The device buffers are the caller's.
+        device->host; returns (h2d_bytes, d2h_bytes).  The device buffers are
+        the caller's.  The call starts and ends on ``stream``.
+
+        With ``chunks`` > 1 (default: 2 when the call moves more than 16 MB,
+        4 above 64 MB; on a GB300 more chunks cost more host time per call
+        than they overlap)
+        the work is cut along the batch, or along the rows of A when there is
+        one batch: the upload of chunk i+1, the chain on chunk i (on
+        ``stream``) and the download of chunk i-1 overlap, the copies on two
+        side streams of this plan.  Every row tile is computed as in one call,
+        so the result is the same.
         """
         import torch
         s = stream or torch.cuda.current_stream()
-        h2d = 0
-        with torch.cuda.stream(s):
-            for h, d in zip(host_inputs, dev_inputs):
-                d.copy_(h, non_blocking=True)
-                h2d += h.numel() * h.element_size()
-            self._run_inputs(list(dev_inputs), dev_out, s)
-            host_out.copy_(dev_out, non_blocking=True)
-        return h2d, host_out.numel() * host_out.element_size()
+        h2d = sum(h.numel() * h.element_size() for h in host_inputs)
+        d2h = host_out.numel() * host_out.element_size()
+        pieces = self._host_chunks(chunks, h2d + d2h)
+        if len(pieces) <= 1:
+            with torch.cuda.stream(s):
+                for h, d in zip(host_inputs, dev_inputs):
+                    d.copy_(h, non_blocking=True)
+                self._run_inputs(list(dev_inputs), dev_out, s)
+                host_out.copy_(dev_out, non_blocking=True)
+            return h2d, d2h
+        s_in, s_out = self._side_streams(s.device)
+        start = torch.cuda.Event()
+        start.record(s)
+        s_in.wait_event(start)
+        s_out.wait_event(start)
+        by_batch = self.batch > 1
+        loaded = []
+        with torch.cuda.stream(s_in):
+            if not by_batch:  # one batch: the weights go up once, before the first rows
+                for h, d in zip(host_inputs[1:], dev_inputs[1:]):
+                    d.copy_(h, non_blocking=True)
+            for lo, hi in pieces:
+                for i, (h, d) in enumerate(zip(host_inputs, dev_inputs)):
+                    if by_batch:
+                        d[lo:hi].copy_(h[lo:hi], non_blocking=True)
+                    elif i == 0:
+                        d[:, lo:hi].copy_(h[:, lo:hi], non_blocking=True)
+                ev = torch.cuda.Event()
+                ev.record(s_in)
+                loaded.append(ev)
+        for (lo, hi), ev in zip(pieces, loaded):
+            s.wait_event(ev)
+            if by_batch:
+                sub_in = [d[lo:hi] for d in dev_inputs]
+                sub_out = dev_out[lo:hi]
+                plan = self._sub_plan(hi - lo, self.M)
+            else:
+                sub_in = [dev_inputs[0][:, lo:hi]] + list(dev_inputs[1:])
+                sub_out = dev_out[:, lo:hi]
+                plan = self._sub_plan(1, hi - lo)
+            plan._run_inputs(sub_in, sub_out, s)
+            done = torch.cuda.Event()
+            done.record(s)
+            s_out.wait_event(done)
+            with torch.cuda.stream(s_out):
+                if by_batch:
+                    host_out[lo:hi].copy_(sub_out, non_blocking=True)
+                else:
+                    host_out[:, lo:hi].copy_(sub_out, non_blocking=True)
+        s.wait_stream(s_out)
+        return h2d, d2h
+
+    def _host_chunks(self, chunks, nbytes):
+        """[(lo, hi)] along the batch, or along the rows (multiples of 256) of one batch."""
+        if chunks is None:
+            chunks = 4 if nbytes > (64 << 20) else (2 if nbytes > (16 << 20) else 1)
+        n = chunks
+        if n <= 1 or self.batch == 0 or self.M == 0:
+            return [(0, self.batch)]
+        if self.batch > 1:
+            n = min(n, self.batch)
+            edges = [self.batch * i // n for i in range(n + 1)]
+        else:
+            units = (self.M + 255) // 256
+            n = min(n, units)
+            edges = [min(self.M, 256 * (units * i // n)) for i in range(n + 1)]
+        return [(lo, hi) for lo, hi in zip(edges, edges[1:]) if hi > lo]
+
+    def _side_streams(self, device):
+        import torch
+        st = getattr(self, "_streams", None)
+        if st is None or st[0] != device:
+            st = (device, torch.cuda.Stream(device=device), torch.cuda.Stream(device=device))
+            self._streams = st
+        return st[1], st[2]
+
+    def _sub_plan(self, batch: int, M: int):
+        cache = self.__dict__.setdefault("_subs", {})
+        key = (batch, M)
+        if key not in cache:
+            cache[key] = self._make_like(batch, M)
+        return cache[key]
+
+    def _make_like(self, batch: int, M: int):
+        if self._single:
+            return GemmPlan(self.dtype, batch, M, self.K, self.N[0])
+        return ChainPlan(self.dtype, batch, M, self.K, self.N)
 
     def _run_inputs(self, inputs, D, stream):
         args = inputs + [None] * (4 - len(inputs))

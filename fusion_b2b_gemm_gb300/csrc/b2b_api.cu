@@ -803,7 +803,10 @@ b2b_status_t encode_chain_maps(b2b_plan_s* p, const void* const* W, const void* 
                                                                : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
   const uint32_t CK = 128 / p->esz;
   std::memset(maps, 0, sizeof(*maps));
-  b2b_status_t st = encode_3d(&maps->a, in_dt, p->esz, A, p->K, p->M, p->batch, CK, 128);
+  // A in its own storage type: fp32 in panels of 32 elements for a mixed-type
+  // cascade, else the chain's input type
+  b2b_status_t st = p->tf0 ? encode_3d(&maps->a, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, A, p->K, p->M, p->batch, 32, 128)
+                           : encode_3d(&maps->a, in_dt, p->esz, A, p->K, p->M, p->batch, CK, 128);
   int64_t kin = p->K;
   if (p->in_kind == kInTF32) {
     // the weights as transposed into the workspace ([N][K] per batch)
@@ -817,12 +820,10 @@ b2b_status_t encode_chain_maps(b2b_plan_s* p, const void* const* W, const void* 
     }
   } else if (p->sn) {
     if (p->tf0 && st == B2B_OK) {
-      // mixed: fp32 A in panels of 32 elements; W0 as transposed into the
-      // workspace ([N1][K] per batch), boxes of this CTA's rows of a pass
-      st = encode_3d(&maps->a, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, A, p->K, p->M, p->batch, 32, 128);
-      if (st == B2B_OK)
-        st = encode_3d(&maps->w[0], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, p->d_wt, p->K, p->N[0], p->batch, 32,
-                       static_cast<uint32_t>(p->pn.pw[0] / 2));
+      // mixed: W0 as transposed into the workspace ([N1][K] per batch),
+      // boxes of this CTA's rows of a pass
+      st = encode_3d(&maps->w[0], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, p->d_wt, p->K, p->N[0], p->batch, 32,
+                     static_cast<uint32_t>(p->pn.pw[0] / 2));
       kin = p->N[0];
     }
     // CTA pairs: each CTA loads half of a pass's 64-column blocks

@@ -175,6 +175,9 @@ EDGES = [
     # mixed types: ragged K (a partial 32-element tf32 panel), wide first
     # intermediate, several stages, more tiles than clusters
     wl.Workload("mixed_f16_ktail", "tf32_f16", 2, 333, 200, (256, 136), "normal_fanin", 1.0, 73),
+    # K = 4 mod 8: fp32 rows of A are 16-byte aligned, 16-bit ones would not be
+    wl.Workload("mixed_bf16_k4mod8", "tf32_bf16", 2, 260, 92, (328, 216), "normal_fanin", 1.0, 77),
+    wl.Workload("tf32_k4mod8", "tf32", 2, 300, 68, (96, 200), "normal", 1.0 / 16, 78),
     wl.Workload("mixed_bf16_wide", "tf32_bf16", 1, 300, 128, (512, 128, 384), "normal_fanin", 1.0, 74),
     wl.Workload("mixed_f16_5", "tf32_f16", 1, 700, 96, (128, 256, 128, 256, 72), "normal_fanin", 1.0, 75),
     wl.Workload("mixed_bf16_many", "tf32_bf16", 1, 30000, 256, (256, 256), "normal_fanin", 1.0, 76),
@@ -308,3 +311,72 @@ def test_full_size_sampled_rows(name):
     sub = got[batches][:, rows]
     assert rel_err(sub, want) <= TOL[w.dtype]
     assert torch.isfinite(got.float()).all()
+
+
+# ------------------------------------------------ seeded random shapes --
+
+def _random_cases(n=16, seed=2026):
+    """Cascades with random stage counts, widths, types and sizes (fixed seed)."""
+    import random
+    rng = random.Random(seed)
+    cases = []
+    for i in range(n):
+        dtype = rng.choice(["f16", "bf16", "f16_f32out", "bf16_f32out", "tf32_f16", "tf32_bf16"])
+        S = rng.randint(2, 6)
+        widths = []
+        for s in range(S):
+            hi = 512 if s < S - 1 else 640
+            widths.append(8 * rng.randint(1, hi // 8))
+        K = (4 if dtype.startswith("tf32") else 8) * rng.randint(1, 48)
+        if not dtype.startswith("tf32"):
+            K = 8 * rng.randint(1, 40)
+        batch = rng.randint(1, 3)
+        M = rng.randint(1, 1200)
+        cases.append(wl.Workload(f"rand{i}_{dtype}_s{S}", dtype, batch, M, K, tuple(widths),
+                                 "normal_fanin", 1.0, 100 + i))
+    return cases
+
+
+@pytest.mark.parametrize("w", _random_cases(), ids=lambda w: w.name)
+def test_random_cascades(w):
+    host = wl.make_inputs(w)
+    dev = [t.cuda() for t in host]
+    plan = b2b.ChainPlan(w.dtype, w.batch, w.M, w.K, w.N)
+    out = plan.run(dev[0], dev[1:])
+    torch.cuda.synchronize()
+    assert plan.status() == 0
+    want = run_oracle(w, host)
+    assert rel_err(out.cpu(), want) <= TOL[w.dtype], (w.N, w.K, w.M)
+
+
+def _random_two_stage(n=16, seed=7):
+    """Two-stage chains of the one-CTA kernels (16-bit with N1 <= 256, tf32,
+    fp64) and single GEMMs, random sizes (fixed seed)."""
+    import random
+    rng = random.Random(seed)
+    cases = []
+    for i in range(n):
+        dtype = rng.choice(["f16", "bf16", "f16_f32out", "bf16_f32out", "tf32", "f64"])
+        if dtype == "f64":
+            N = (rng.choice([16, 32, 64]), rng.choice([16, 32, 64]))
+            K = 4 * rng.randint(1, 32)
+        elif dtype == "tf32":
+            N = (4 * rng.randint(1, 64), 4 * rng.randint(1, 160))
+            K = 4 * rng.randint(1, 96)
+        else:
+            N = (8 * rng.randint(1, 32), 8 * rng.randint(1, 80))
+            K = 8 * rng.randint(1, 64)
+        batch = rng.randint(1, 40)
+        M = rng.randint(1, 3000 // batch + 1)
+        dist = "uniform" if dtype == "f64" else ("normal" if dtype == "tf32" else "normal_fanin")
+        scale = 1.0 / 16 if dtype == "tf32" else 1.0
+        cases.append(wl.Workload(f"rand2s{i}_{dtype}", dtype, batch, M, K, N, dist, scale, 200 + i))
+    return cases
+
+
+@pytest.mark.parametrize("w", _random_two_stage(), ids=lambda w: w.name)
+def test_random_two_stage(w):
+    host = wl.make_inputs(w)
+    got = run_gpu(w, host)
+    want = run_oracle(w, host)
+    assert rel_err(got, want) <= TOL[w.dtype], (w.N, w.K, w.M, w.batch)

@@ -175,6 +175,11 @@ EDGES = [
     # mixed types: ragged K (a partial 32-element tf32 panel), wide first
     # intermediate, several stages, more tiles than clusters
     wl.Workload("mixed_f16_ktail", "tf32_f16", 2, 333, 200, (256, 136), "normal_fanin", 1.0, 73),
+    # the largest sizes a plan takes: eight GEMMs, 512-wide intermediates and
+    # a 4096-wide last GEMM; a long K; one row
+    wl.Workload("max_widths_f16_8", "f16", 1, 300, 2048, (512,) * 7 + (4096,), "normal_fanin", 1.0, 79),
+    wl.Workload("long_k_bf16", "bf16", 2, 257, 8192, (256, 256), "normal_fanin", 1.0, 80),
+    wl.Workload("one_row_bf16_8", "bf16_f32out", 2, 1, 64, (128, 512, 64, 256, 384, 8, 512, 72), "normal_fanin", 1.0, 86),
     # K = 4 mod 8: fp32 rows of A are 16-byte aligned, 16-bit ones would not be
     wl.Workload("mixed_bf16_k4mod8", "tf32_bf16", 2, 260, 92, (328, 216), "normal_fanin", 1.0, 77),
     wl.Workload("tf32_k4mod8", "tf32", 2, 300, 68, (96, 200), "normal", 1.0 / 16, 78),

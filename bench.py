@@ -333,6 +333,11 @@ def roofline_for(w: wl.Workload, kernel_ms: float, peaks: dict, traffic=None):
 
 PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "traffic.json")
 
+# the arithmetic type of a workload's GEMMs (operands; accumulation is fp32,
+# fp64 for f64)
+COMPUTE_DTYPE = {"f16_f32out": "f16", "f16": "f16", "bf16": "bf16", "bf16_f32out": "bf16", "tf32": "tf32",
+                 "f64": "f64", "tf32_f16": "tf32+f16", "tf32_bf16": "tf32+bf16"}
+
 
 def kernel_source_digest() -> str:
     import hashlib
@@ -475,7 +480,7 @@ def run_ours(args):
     line = {
         "metric": "fused B2B GEMM TFLOPS", "value": value, "unit": "TFLOP/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "f16", "data": "synthetic",
+        "scaling": "weak", "vs_baseline": None, "dtype": COMPUTE_DTYPE[w.dtype], "data": "synthetic",
         "config": {"workload": w.name, "batch": w.batch, "M": w.M, "K": w.K, "N": list(w.N),
                    "io": w.dtype, "l2": f"rotating {case.copies} input/output copies "
                                          f"({case.copies * w.unique_bytes() / 2**20:.0f} MiB > L2)",

@@ -177,7 +177,7 @@ def oracle_kinds(dtype):
             "tf32_f16": (oracle.F32, oracle.F16, oracle.F32), "tf32_bf16": (oracle.F32, oracle.BF16, oracle.F32)}[dtype]
 
 
-def oracle_sample(w: wl.Workload, rows: int, batches: int = 1):
+def oracle_sample(w: wl.Workload, rows: int, batches: int = 1, threads: int = 0):
     """Run the oracle on a sample (first `batches` batches, first `rows` rows)."""
     import oracle
     sw = w.with_(batch=min(batches, w.batch), M=min(rows, w.M))
@@ -186,22 +186,24 @@ def oracle_sample(w: wl.Workload, rows: int, batches: int = 1):
     A = oracle.widen(host[0])
     Ws = [oracle.widen(t) for t in host[1:]]
     t0 = time.perf_counter()
-    oracle.chain(A, Ws, acc, mid, fin)
+    oracle.chain(A, Ws, acc, mid, fin, n_threads=threads)
     dt = time.perf_counter() - t0
     return sw, dt
 
 
-def cpu_baseline(w: wl.Workload, target_s: float = 10.0):
-    """Oracle throughput on a bounded sample sized for about `target_s` of CPU work."""
+def cpu_baseline(w: wl.Workload, target_s: float = 10.0, threads: int = 0):
+    """Oracle throughput on a bounded sample sized for about `target_s` of CPU
+    work, on all host cores (threads = 0) or on `threads` of them."""
     import oracle
     rows = 256
-    sw, dt = oracle_sample(w, rows)
+    sw, dt = oracle_sample(w, rows, threads=threads)
     per_row = dt / (sw.batch * sw.M)
     want_rows = int(max(256, min(w.batch * w.M, target_s / max(per_row, 1e-9))))
     batches = max(1, min(w.batch, want_rows // w.M))
     rows = want_rows if batches == 1 else w.M
-    sw, dt = oracle_sample(w, rows, batches)
-    return {"value": sw.flops() / dt / 1e12, "unit": "TFLOP/s", "cores": oracle.max_threads(), "kind": "oracle",
+    sw, dt = oracle_sample(w, rows, batches, threads=threads)
+    cores = threads if threads > 0 else oracle.max_threads()
+    return {"value": sw.flops() / dt / 1e12, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
             "sample": f"{sw.batch} batch x {sw.M} rows of {w.name} ({sw.flops() / 1e9:.2f} GFLOP, {dt:.2f} s)"}
 
 
@@ -487,6 +489,7 @@ def run_ours(args):
                    "parallelism": f"replica x{world}" if world > 1 else "single GPU"},
         "kernel_ms": kernel_ms,
         "eager_ms_per_call": float(np.median(per_eager)),
+        "eager_ms_p10_p90": [float(np.percentile(per_eager, 10)), float(np.percentile(per_eager, 90))],
         "timing": "K steps captured in one CUDA graph, CUDA events around one replay",
         "roofline": roofline_for(w, kernel_ms, peaks_all, recorded_traffic(w.name)),
         "clocks": clocks,
@@ -540,6 +543,7 @@ def per_config(args, peaks_all, device, stream):
             "workload": name, "extra": name in wl.EXTRA_WORKLOADS, "dtype": w.dtype, "gflop": w.flops() / 1e9, "unique_mb": w.unique_bytes() / 2**20,
             "fused_ms": fused_ms, "fused_tflops": w.flops() / (fused_ms * 1e-3) / 1e12,
             "fused_eager_median_ms": float(np.median(per)),
+            "fused_eager_p10_p90_ms": [float(np.percentile(per, 10)), float(np.percentile(per, 90))],
             "roofline": roofline_for(w, fused_ms, peaks_all, recorded_traffic(name)),
             "unfused_torch_ms": t_ms, "unfused_own_ms": o_ms, "unfused_own_launches": own_launches,
             "speedup_vs_best_unfused": min(t_ms, o_ms if o_ms is not None else t_ms) / fused_ms,
@@ -548,6 +552,8 @@ def per_config(args, peaks_all, device, stream):
         }
         if not args.no_cpu_configs:
             entry["cpu_oracle"] = cpu_baseline(w, target_s=args.cpu_cfg_s)
+            if name in ("tiny_f16", "tf32"):
+                entry["cpu_oracle_1_thread"] = cpu_baseline(w, target_s=args.cpu_cfg_s, threads=1)
         out.append(entry)
         del case, g, gt, go
         torch.cuda.empty_cache()

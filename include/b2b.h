@@ -98,8 +98,11 @@ typedef enum {
  *                 (batch * K * N1 * 4 bytes); a run launches two kernels.
  *   B2B_F64:      two stages; K % 4 == 0; N1, N2 in {16, 32, 64}.
  * Binds to the current CUDA device, which must be an sm_103 GPU
- * (B2B_ERR_DEVICE otherwise).  Allocates one 4-byte device status word.
- * No kernel is launched.
+ * (B2B_ERR_DEVICE otherwise).  Allocates a 4-byte device status word; a
+ * two-stage 16-bit plan whose weights stay resident over several batches
+ * also a tile-schedule table (36 bytes per CTA, copied once); tf32 and
+ * mixed plans also the workspace of their transposed weights.  No kernel is
+ * launched.
  */
 b2b_status_t b2b_plan_create(b2b_plan_t* out, b2b_dtype_t dtype, int64_t batch, int64_t M,
                              int64_t K, int64_t N1, int64_t N2, int64_t N3);

@@ -385,3 +385,24 @@ def test_random_two_stage(w):
     got = run_gpu(w, host)
     want = run_oracle(w, host)
     assert rel_err(got, want) <= TOL[w.dtype], (w.N, w.K, w.M, w.batch)
+
+
+def test_one_plan_on_two_streams_at_once():
+    """Runs of one plan may overlap on different streams (the plan is not
+    modified by a run): both results must be the single-stream ones."""
+    cases = [wl.small(wl.WORKLOADS["batched_f16"], M=1000, batch=40),
+             wl.small(wl.WORKLOADS["three_stage_bf16"], M=3000)]
+    for w in cases:
+        plan = b2b.ChainPlan(w.dtype, w.batch, w.M, w.K, w.N)
+        ins = [[t.cuda() for t in wl.make_inputs(w, seed=s)] for s in (1, 2)]
+        want = [plan.run(x[0], x[1:]).clone() for x in ins]
+        torch.cuda.synchronize()
+        streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+        outs = [plan.empty_out(), plan.empty_out()]
+        for rep in range(5):
+            for x, o, s in zip(ins, outs, streams):
+                plan.run(x[0], x[1:], o, stream=s)
+        torch.cuda.synchronize()
+        assert plan.status() == 0
+        for o, ref in zip(outs, want):
+            assert torch.equal(o.view(torch.int16), ref.view(torch.int16))

@@ -191,10 +191,24 @@ def oracle_sample(w: wl.Workload, rows: int, batches: int = 1, threads: int = 0)
     return sw, dt
 
 
+_ALL_CORES = []
+
+
+def all_cores() -> int:
+    """The oracle's thread count before any run has set one (a run with an
+    explicit count leaves it set for the process)."""
+    import oracle
+    if not _ALL_CORES:
+        _ALL_CORES.append(oracle.max_threads())
+    return _ALL_CORES[0]
+
+
 def cpu_baseline(w: wl.Workload, target_s: float = 10.0, threads: int = 0):
     """Oracle throughput on a bounded sample sized for about `target_s` of CPU
     work, on all host cores (threads = 0) or on `threads` of them."""
     import oracle
+    cores = all_cores()  # (taken before this call may set a count)
+    threads = threads if threads > 0 else cores
     rows = 256
     sw, dt = oracle_sample(w, rows, threads=threads)
     per_row = dt / (sw.batch * sw.M)
@@ -202,8 +216,7 @@ def cpu_baseline(w: wl.Workload, target_s: float = 10.0, threads: int = 0):
     batches = max(1, min(w.batch, want_rows // w.M))
     rows = want_rows if batches == 1 else w.M
     sw, dt = oracle_sample(w, rows, batches, threads=threads)
-    cores = threads if threads > 0 else oracle.max_threads()
-    return {"value": sw.flops() / dt / 1e12, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+    return {"value": sw.flops() / dt / 1e12, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
             "sample": f"{sw.batch} batch x {sw.M} rows of {w.name} ({sw.flops() / 1e9:.2f} GFLOP, {dt:.2f} s)"}
 
 

@@ -168,7 +168,7 @@ class Plan:
         return D
 
     def run_from_host(self, host_inputs: Sequence, host_out, dev_inputs: Sequence, dev_out, stream=None,
-                      chunks: Optional[int] = None):
+                      chunks: Optional[int] = None, graph: bool = True):
         """One end-to-end call from pinned host buffers.
 
         Copies the inputs host->device, runs the chain, copies the result
@@ -182,7 +182,9 @@ class Plan:
         one batch: the upload of chunk i+1, the chain on chunk i (on
         ``stream``) and the download of chunk i-1 overlap, the copies on two
         side streams of this plan.  Every row tile is computed as in one call,
-        so the result is the same.
+        so the result is the same.  With ``graph`` (default) the chunked
+        pipeline is captured in a CUDA graph on its first call for a set of
+        buffers and replayed afterwards (host memory must be pinned).
         """
         import torch
         s = stream or torch.cuda.current_stream()
@@ -196,7 +198,37 @@ class Plan:
                 self._run_inputs(list(dev_inputs), dev_out, s)
                 host_out.copy_(dev_out, non_blocking=True)
             return h2d, d2h
+        for lo, hi in pieces:  # every chunk's plan exists before any capture
+            self._sub_plan(hi - lo, self.M) if self.batch > 1 else self._sub_plan(1, hi - lo)
         s_in, s_out = self._side_streams(s.device)
+        if not graph:
+            self._pipeline(pieces, host_inputs, host_out, dev_inputs, dev_out, s, s_in, s_out)
+            return h2d, d2h
+        # The chunked pipeline is captured once per set of buffers and
+        # replayed: a replay costs the host a few microseconds where the
+        # eager form spends tens per chunk.
+        key = (tuple(t.data_ptr() for t in host_inputs), host_out.data_ptr(),
+               tuple(t.data_ptr() for t in dev_inputs), dev_out.data_ptr(), tuple(pieces),
+               tuple(tuple(t.shape) for t in host_inputs), s.device.index)
+        graphs = self.__dict__.setdefault("_graphs", {})
+        g = graphs.get(key)
+        if g is None:
+            if len(graphs) >= 4:
+                graphs.pop(next(iter(graphs)))
+            g = torch.cuda.CUDAGraph()
+            cap = torch.cuda.Stream(device=s.device)
+            cap.wait_stream(s)
+            with torch.cuda.graph(g, stream=cap):
+                self._pipeline(pieces, host_inputs, host_out, dev_inputs, dev_out, cap, s_in, s_out)
+            s.wait_stream(cap)
+            graphs[key] = g
+        with torch.cuda.stream(s):
+            g.replay()
+        return h2d, d2h
+
+    def _pipeline(self, pieces, host_inputs, host_out, dev_inputs, dev_out, s, s_in, s_out):
+        """Upload chunk i+1 on s_in, run chunk i on s, download chunk i-1 on s_out."""
+        import torch
         start = torch.cuda.Event()
         start.record(s)
         s_in.wait_event(start)
@@ -236,7 +268,6 @@ class Plan:
                 else:
                     host_out[:, lo:hi].copy_(sub_out, non_blocking=True)
         s.wait_stream(s_out)
-        return h2d, d2h
 
     def _host_chunks(self, chunks, nbytes):
         """[(lo, hi)] along the batch, or along the rows (multiples of 256) of one batch."""

@@ -39,6 +39,10 @@ CASES = [
     wl.Workload("fail_tf32", "tf32", 1, 384, 256, (256, 256), "normal", 1.0 / 16, 53),
     wl.Workload("fail_deep5_f16", "f16", 1, 600, 128, (256, 512, 128, 256, 384), "normal_fanin", 1.0, 54),
     wl.Workload("fail_mixed_bf16", "tf32_bf16", 1, 400, 64, (256, 128, 256), "normal_fanin", 1.0, 55),
+    # resident weights over many batches: CTAs walk the batch-aware schedule
+    wl.Workload("fail_sched_f16", "f16", 40, 2000, 128, (128, 128), "normal_fanin", 1.0, 56),
+    # one tile per CTA, output staged in the ring
+    wl.Workload("fail_one_tile_tf32", "tf32", 1, 4096, 128, (128, 256), "normal", 1.0 / 16, 57),
 ]
 
 

@@ -85,7 +85,7 @@ const ChainKernelEntry* find_chain_kernel(int in, int out, int S, int n1p, int n
 }
 
 const ChainNEntry* find_chainn_kernel(int in, int out, int nf, bool tf0) {
-  const ChainNTable tables[] = {chainn_table_f16(), chainn_table_bf16()};
+  const ChainNTable tables[] = {chainn_table_f16(), chainn_table_bf16(), chainn_table_tf32()};
   for (const ChainNTable& t : tables)
     for (int i = 0; i < t.count; ++i) {
       const ChainNEntry& e = t.entries[i];
@@ -217,19 +217,25 @@ b2b_status_t setup_chainn(b2b_plan_s* p) {
   if (tiles > (1ll << 30)) return B2B_ERR_UNSUPPORTED;
   c.total_tiles = static_cast<int>(tiles);
   p->nf = p->N[S - 1] > 128 ? 256 : 128;
+  // a two-GEMM tf32 chain: the intermediate (at most 256 columns) stays in
+  // tensor memory and the second GEMM runs in one pass
+  const bool pt = p->in_kind == kInTF32;
+  if (pt && (S != 2 || p->N[0] > 256 || p->N[1] > 256)) return B2B_ERR_UNSUPPORTED;
   int wmax = 0;
-  // 128-byte K panels of the first GEMM: 64 16-bit or 32 tf32 elements
-  c.kpan[0] = static_cast<int>(p->tf0 ? (p->K + 31) / 32 : (p->K + 63) / 64);
+  // 128-byte K panels: 64 16-bit or 32 tf32 elements
+  const int ck = pt ? 32 : 64;
+  c.kpan[0] = static_cast<int>(p->tf0 || pt ? (p->K + 31) / 32 : (p->K + 63) / 64);
   for (int s = 0; s < S - 1; ++s) {
     const int w = static_cast<int>((p->N[s] + 127) / 128 * 128);
     if (w > 512) return B2B_ERR_UNSUPPORTED;
     c.wpad[s] = w;
     // passes of 256 columns where they tile the width, else of 128
     c.pw[s] = (w % 256 == 0) ? 256 : 128;
-    c.kpan[s + 1] = w / 64;
+    c.kpan[s + 1] = w / ck;
     // the first GEMM: an A slot and a weight slot per K panel; later GEMMs:
-    // one weight slot per K panel, or per two with 128-column passes
-    const int kps = (s > 0 && c.pw[s] == 128) ? 2 : 1;
+    // one weight slot per K panel, or per two 16-bit ones with 128-column
+    // passes
+    const int kps = (!pt && s > 0 && c.pw[s] == 128) ? 2 : 1;
     c.slots0 += (w / c.pw[s]) * (s == 0 ? 2 * c.kpan[s] : c.kpan[s] / kps);
     wmax = std::max(wmax, w);
   }
@@ -237,7 +243,7 @@ b2b_status_t setup_chainn(b2b_plan_s* p) {
   c.npass = static_cast<int>((p->N[S - 1] + p->nf - 1) / p->nf);
   p->n1p = c.wpad[0];
   p->n2p = S >= 3 ? c.wpad[1] : 0;
-  const uint32_t p_bytes = 256u * static_cast<uint32_t>(wmax);
+  const uint32_t p_bytes = pt ? 0u : 256u * static_cast<uint32_t>(wmax);
   // the rest of shared memory: ring slots of 16 KB (an A panel or a weight
   // half panel each), at most sixteen, after one or two 4 KB staging buffers
   // per epilogue warp (two, unless one buffer buys a ring slot in a ring of
@@ -257,9 +263,9 @@ b2b_status_t setup_chainn(b2b_plan_s* p) {
   if (p->smem_bytes > kSmemOptin) return B2B_ERR_UNSUPPORTED;
   // a weight whose width is a multiple of 64 is read in 4-D boxes
   c.w_merged = 0;
-  for (int s = p->tf0 ? 1 : 0; s < S; ++s)
+  for (int s = p->tf0 ? 1 : 0; s < S && !pt; ++s)
     if (p->N[s] % 64 == 0) c.w_merged |= 1 << s;
-  const ChainNEntry* e = find_chainn_kernel(p->in_kind, p->out_kind, p->nf, p->tf0);
+  const ChainNEntry* e = find_chainn_kernel(p->in_kind, p->out_kind, p->nf, p->tf0 || pt);
   if (!e) return B2B_ERR_UNSUPPORTED;
   p->fn = e->fn;
   p->threads = kChainNThreads;
@@ -269,13 +275,25 @@ b2b_status_t setup_chainn(b2b_plan_s* p) {
   return B2B_OK;
 }
 
+// A two-GEMM tf32 chain runs on CTA pairs when both widths fit one 256-column
+// pass and the 128-row tiles outnumber the SMs: each SM then loads half of
+// every weight panel (measured: 2 x 65536 rows 84.0 -> 60.6 us, 20480 rows
+// 27.3 -> 21.7 us).  With at most one tile per SM the time is the latency of
+// one tile's load -> GEMM -> round -> GEMM -> store chain, which pairs do not
+// shorten (16384 rows: 14.9 us either way), and the one-tile kernel stays.
+bool tf32_pairs(const b2b_plan_s* p) {
+  return p->in_kind == kInTF32 && p->stages == 2 && p->N[0] <= 256 && p->N[1] <= 256 &&
+         p->batch * ((p->M + 127) / 128) > p->sms;
+}
+
 // Tiling of a tcgen05 chain of one or two GEMMs (chain_tc_kernel): padded
 // widths, final-pass width, tensor-memory regions, shared-memory carve-up,
 // and whether the weights stay resident.  Longer cascades, intermediates
 // wider than 256 columns and mixed types go to setup_chainn.
 b2b_status_t setup_chain_tc(b2b_plan_s* p) {
   const int S = p->stages;
-  if (p->tf0 || (p->in_kind != kInTF32 && (S >= 3 || (S == 2 && p->N[0] > 256)))) return setup_chainn(p);
+  if (p->tf0 || (p->in_kind != kInTF32 && (S >= 3 || (S == 2 && p->N[0] > 256))) || tf32_pairs(p))
+    return setup_chainn(p);
   p->sn = false;
   const int CK = 128 / p->esz;
   const int64_t wmin = 64;
@@ -812,8 +830,10 @@ b2b_status_t encode_chain_maps(b2b_plan_s* p, const void* const* W, const void* 
     // the weights as transposed into the workspace ([N][K] per batch)
     const uint32_t* dst = static_cast<const uint32_t*>(p->d_wt);
     for (int s = 0; s < S && st == B2B_OK; ++s) {
-      const uint32_t rows = s < S - 1 ? static_cast<uint32_t>(s == 0 ? p->n1p : p->n2p)
-                                      : static_cast<uint32_t>(p->nf);
+      // boxes of a pass's rows (CTA pairs: of this CTA's half of them)
+      const uint32_t rows = p->sn            ? static_cast<uint32_t>(p->pn.pw[s] / 2)
+                            : s < S - 1      ? static_cast<uint32_t>(s == 0 ? p->n1p : p->n2p)
+                                             : static_cast<uint32_t>(p->nf);
       st = encode_3d(&maps->w[s], in_dt, p->esz, dst, kin, p->N[s], p->batch, CK, rows);
       dst += p->batch * kin * p->N[s];
       kin = p->N[s];
@@ -919,7 +939,7 @@ b2b_status_t run_chain_tc(b2b_plan_s* p, const void* const* W, const void* A, vo
   cudaError_t e;
   if (p->sn) {
     ChainNParams prm = p->pn;
-    prm.a_early = p->tf0 ? 1 : 0;
+    prm.a_early = (p->tf0 || p->in_kind == kInTF32) ? 1 : 0;
     prm.status = p->d_status;
     prm.budget_ns = p->budget_ns;
     prm.debug = p->debug;
@@ -1251,6 +1271,10 @@ extern "C" b2b_status_t b2b_run_tf32_noalloc(int64_t batch, int64_t M, int64_t K
       cudaSuccess) {
     cudaGetLastError();
     return B2B_ERR_CUDA;
+  }
+  if (pl.sn) {
+    st = pair_grid(&pl);
+    if (st != B2B_OK) return st;
   }
   const void* ins[3] = {A, B, C};
   for (const void* q : ins)

@@ -166,12 +166,20 @@ __device__ __forceinline__ uint32_t tmem_col(uint32_t r0, int c) {
 // the 16-bit type IN of every later GEMM: a mixed-type cascade, where the
 // accumulator and operand layouts of the first hand-over differ in element
 // size as well as in order.
+//
+// IN = tf32 (with TF0): a two-GEMM tf32 chain.  The intermediate (at most
+// 256 columns) is rounded to tf32 in place in tensor memory, one K element
+// per 32-bit column, and the second GEMM (one pass, its weight transposed
+// like W0) reads it from there as its A operand, so no operand image is
+// kept.  The next GEMM to write that region is the next unit's first GEMM,
+// which the tensor pipe runs after every MMA that reads it.
 template <int IN, int OUT, int NF, bool TF0 = false>
 __global__ void __launch_bounds__(kChainNThreads, 1)
     chainn_kernel(const __grid_constant__ ChainNMaps maps, const __grid_constant__ ChainNParams p) {
   using namespace ptx;
-  static_assert(IN == kInF16 || IN == kInBF16, "16-bit operands");
+  static_assert(IN == kInF16 || IN == kInBF16 || (IN == kInTF32 && TF0), "16-bit or tf32 operands");
   static_assert(NF == 128 || NF == 256, "pass width of the last GEMM");
+  constexpr bool PT = IN == kInTF32;  // tf32 intermediate, kept in tensor memory
   constexpr int CG = 2;
   constexpr int CK = 64;           // K elements per 128-byte panel
   constexpr int CK0 = TF0 ? 32 : CK;  // of the first GEMM's operands
@@ -180,7 +188,7 @@ __global__ void __launch_bounds__(kChainNThreads, 1)
   constexpr int WBOX_BYTES = CK * 128;
   constexpr int OSZ = (OUT == kOutF32) ? 4 : 2;
   constexpr int OBOX_N = 128 / OSZ;
-  constexpr uint32_t FMT = (IN == kInF16) ? 0u : 1u;
+  constexpr uint32_t FMT = (IN == kInF16) ? 0u : (IN == kInBF16 ? 1u : 2u);
   constexpr uint32_t kCols = 512;
 
   extern __shared__ uint8_t smem_raw[];
@@ -250,8 +258,8 @@ __global__ void __launch_bounds__(kChainNThreads, 1)
   const int kpan_last = p.kpan[S - 1];
   // K panels per ring slot: a weight half panel of 64 columns (pass width
   // 128) takes 8 KB, so a slot holds two K panels of it; GEMM s > 0 only
-  // (its K panel count, a multiple of 128 / 64, is even)
-  auto kps_of = [&](int s) -> int { return (s > 0 && p.pw[s] == 128) ? 2 : 1; };
+  // (its K panel count, a multiple of 128 / 64, is even); tf32 weights: one
+  auto kps_of = [&](int s) -> int { return (!PT && s > 0 && p.pw[s] == 128) ? 2 : 1; };
   const int kps_last = kps_of(S - 1);
 
   if (warp == 0) {
@@ -283,8 +291,8 @@ __global__ void __launch_bounds__(kChainNThreads, 1)
           } else {
             const CUtensorMap* wm = &maps.w[s];
             const int n0 = col0 + static_cast<int>(rank) * wcols;
-            if (TF0 && s == 0) {
-              // W0 transposed: this CTA's wcols rows of 32 K elements
+            if ((TF0 && s == 0) || PT) {
+              // a tf32 weight transposed: this CTA's wcols rows of 32 K elements
               tma_load_3d_pair(dst, wm, fb, kb * CK0, n0, b);
             } else if ((p.w_merged >> s) & 1) {
               // one box of npan * 64 K rows and wcols / 64 column blocks
@@ -372,6 +380,9 @@ __global__ void __launch_bounds__(kChainNThreads, 1)
       // consumed + need
       uint32_t consumed = 0, seen = 0;
       const uint32_t ready = bar(knSlotReady);
+      // tf32 chains: the tensor-memory column of the intermediate the next
+      // GEMM reads
+      uint32_t p_tmem = 0;
       auto stage_ready = [&](uint32_t need) -> bool {
         if (seen >= consumed + need) return true;
         seen = ld_acquire_shared(ready);
@@ -416,6 +427,13 @@ __global__ void __launch_bounds__(kChainNThreads, 1)
           for (int kk = 0; kk < 4; ++kk)
             mma_ss<true, CG>(d, desc_sw128(sa + kk * 32u, 16u, 1024u), desc_sw128(wb + kk * 32u, 16u, 1024u), idesc,
                              kk ? 1u : acc0);
+        } else if constexpr (PT) {
+          // tf32 intermediate in tensor memory: K panel kb is its columns
+          // [32 kb, 32 kb + 32), 8 per MMA; B K-major as in the first GEMM
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            mma_ts<true, CG>(d, p_tmem + static_cast<uint32_t>(kb * 32 + kk * 8), desc_sw128(wb + kk * 32u, 16u, 1024u),
+                             idesc, kk ? 1u : acc0);
         } else if constexpr (npan == 2) {
 #pragma unroll
           for (int kk = 0; kk < 2 * (CK / KSTEP); ++kk) {
@@ -435,13 +453,15 @@ __global__ void __launch_bounds__(kChainNThreads, 1)
         slot = s1 + 1u == static_cast<uint32_t>(p.nslot) ? 0u : s1 + 1u;
         return true;
       };
-      // the K panels of GEMM s > 0 from kb on need chunk kb / 2 of the
-      // previous intermediate (global index k - 1), on its first pass only
+      // the K panels of GEMM s > 0 from kb on need chunk kb / 2 (tf32:
+      // kb / 4) of the previous intermediate (global index k - 1), on its
+      // first pass only
       RegionCursor rc;
       uint32_t k = 0;  // intermediates started so far
+      constexpr int kpc = PT ? 4 : 2;  // K panels per 128-column chunk
       auto chunk_of = [&](bool first_pass, int kb) -> int {
-        if (!first_pass || (kb & 1)) return -1;
-        return knPChunk + static_cast<int>(((k - 1u) & 1u) * 4u) + kb / 2;
+        if (!first_pass || (kb % kpc)) return -1;
+        return knPChunk + static_cast<int>(((k - 1u) & 1u) * 4u) + kb / kpc;
       };
       // one pass: kpan K panels, npan of them per ring slot (0: the first
       // GEMM, one K panel and two slots)
@@ -460,8 +480,8 @@ __global__ void __launch_bounds__(kChainNThreads, 1)
         for (int s = 0; s < S - 1 && ok; ++s) {
           const int pw = p.pw[s];
           const uint32_t r0 = rc.take(p.wpad[s]);
-          const uint32_t idesc = (TF0 && s == 0) ? make_idesc(2u, static_cast<uint32_t>(pw), 256u, false)
-                                                 : make_idesc(FMT, static_cast<uint32_t>(pw), 256u, true);
+          const uint32_t idesc = ((TF0 && s == 0) || PT) ? make_idesc(2u, static_cast<uint32_t>(pw), 256u, false)
+                                                         : make_idesc(FMT, static_cast<uint32_t>(pw), 256u, true);
           const uint32_t cpar = ((k - 1u) >> 1) & 1u;
           int touched = 0;
           for (int col0 = 0; col0 < p.wpad[s] && ok; col0 += pw) {
@@ -486,11 +506,12 @@ __global__ void __launch_bounds__(kChainNThreads, 1)
           }
           if (!ok) break;
           if (s > 0) tc_commit<CG>(bar(knCFull));
+          p_tmem = tmem_base + (r0 << 8);
           ++k;
         }
         if (!ok) break;
         // the unit's passes of the last GEMM, each in the next region
-        const uint32_t idesc = make_idesc(FMT, NF, 256u, true);
+        const uint32_t idesc = make_idesc(FMT, NF, 256u, !PT);
         const uint32_t cpar = ((k - 1u) >> 1) & 1u;
         for (int j = c.p0; j < c.p1 && ok; ++j) {
           const int r = static_cast<int>(rc.take(NF));

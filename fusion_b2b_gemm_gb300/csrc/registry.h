@@ -23,8 +23,9 @@ ChainTable chain_table_f16();
 ChainTable chain_table_bf16();
 ChainTable chain_table_tf32();
 
-// Cascades of 16-bit GEMMs on CTA pairs (chainn_kernel): three or more
-// stages, or two with an intermediate wider than 256 columns.
+// Cascades on CTA pairs (chainn_kernel): 16-bit GEMMs in three or more
+// stages, or two with an intermediate wider than 256 columns; mixed-type
+// cascades; two-GEMM tf32 chains.
 struct ChainNEntry {
   int in, out, nf;
   bool tf0;  // first GEMM on tf32 operands (mixed-type cascade)
@@ -36,6 +37,7 @@ struct ChainNTable {
 };
 ChainNTable chainn_table_f16();
 ChainNTable chainn_table_bf16();
+ChainNTable chainn_table_tf32();
 
 }  // namespace b2b
 

@@ -43,6 +43,8 @@ CASES = [
     wl.Workload("fail_sched_f16", "f16", 40, 2000, 128, (128, 128), "normal_fanin", 1.0, 56),
     # one tile per CTA, output staged in the ring
     wl.Workload("fail_one_tile_tf32", "tf32", 1, 4096, 128, (128, 256), "normal", 1.0 / 16, 57),
+    # a tf32 chain on CTA pairs (more 128-row tiles than SMs)
+    wl.Workload("fail_tf32_pairs", "tf32", 2, 10000, 64, (128, 128), "normal", 1.0 / 16, 58),
 ]
 
 

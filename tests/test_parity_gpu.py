@@ -104,6 +104,9 @@ EXACT = [
     # then fp16 / bf16
     wl.Workload("x_tf32_f16_2", "tf32_f16", 2, 300, 64, (128, 64), "int", 2, 71),
     wl.Workload("x_tf32_bf16_4", "tf32_bf16", 1, 520, 32, (256, 32, 32, 256), "int", 1, 72),
+    # a tf32 chain with more 128-row tiles than SMs runs on CTA pairs, its
+    # intermediate kept in tensor memory (ragged widths)
+    wl.Workload("x_tf32_pairs", "tf32", 4, 5000, 96, (200, 136), "int", 2, 87),
 ]
 
 
@@ -186,6 +189,12 @@ EDGES = [
     wl.Workload("mixed_bf16_wide", "tf32_bf16", 1, 300, 128, (512, 128, 384), "normal_fanin", 1.0, 74),
     wl.Workload("mixed_f16_5", "tf32_f16", 1, 700, 96, (128, 256, 128, 256, 72), "normal_fanin", 1.0, 75),
     wl.Workload("mixed_bf16_many", "tf32_bf16", 1, 30000, 256, (256, 256), "normal_fanin", 1.0, 76),
+    # tf32 chains on CTA pairs (more 128-row tiles than SMs): a partial K
+    # panel, a 128-column last pass, a last pair tile whose odd half lies
+    # wholly past M
+    wl.Workload("tf32_pairs_ktail", "tf32", 2, 10000, 68, (256, 256), "normal", 1.0 / 16, 88),
+    wl.Workload("tf32_pairs_n128", "tf32", 1, 20000, 256, (128, 96), "normal", 1.0 / 16, 89),
+    wl.Workload("tf32_pairs_mtail", "tf32", 3, 7000, 32, (72, 256), "normal", 1.0 / 16, 90),
 ]
 
 
@@ -195,6 +204,16 @@ def test_edge_shapes(w):
     got = run_gpu(w, host)
     want = run_oracle(w, host)
     assert rel_err(got, want) <= TOL[w.dtype]
+
+
+def test_tf32_chains_take_pairs_only_past_one_tile_per_sm():
+    # one 128-row tile per SM or fewer: the one-CTA kernel; more: CTA pairs
+    # (384 threads, an even grid)
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    one = b2b.Plan("tf32", 1, 128 * sms, 256, 256, 256).info()
+    many = b2b.Plan("tf32", 1, 128 * sms + 1, 256, 256, 256).info()
+    assert one["threads"] != 384
+    assert many["threads"] == 384 and many["grid"] % 2 == 0
 
 
 def test_empty_chain_is_a_no_op():

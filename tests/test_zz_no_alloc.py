@@ -45,7 +45,9 @@ def _rel(got, want):
 
 def test_two_calls_in_a_row_match_the_plan_path():
     shapes = [wl.Workload("na1", "tf32", 1, 640, 256, (256, 256), "normal", 1.0 / 16, 41),
-              wl.Workload("na2", "tf32", 2, 300, 128, (192, 136), "normal", 1.0 / 16, 42)]
+              wl.Workload("na2", "tf32", 2, 300, 128, (192, 136), "normal", 1.0 / 16, 42),
+              # more 128-row tiles than SMs: the CTA-pair kernel
+              wl.Workload("na_pairs", "tf32", 2, 10000, 64, (96, 128), "normal", 1.0 / 16, 44)]
     for w in shapes:
         host = wl.make_inputs(w)
         dev = [t.cuda() for t in host]

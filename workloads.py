@@ -135,6 +135,9 @@ EXTRA_WORKLOADS: Dict[str, Workload] = {
                                 "normal_fanin", 1.0, 7,
                                 "fp32 A and first weight (tf32 GEMM), bf16 intermediates and later "
                                 "weights, fp32 out"),
+    "tf32_batched": Workload("tf32_batched", "tf32", 4, 16384, 256, (256, 256), "normal", 1.0 / 16, 8,
+                             "the tf32 workload over four batches, weights distinct per batch "
+                             "(more 128-row tiles than SMs)"),
 }
 
 ALL_WORKLOADS: Dict[str, Workload] = {**WORKLOADS, **EXTRA_WORKLOADS}

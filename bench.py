@@ -222,6 +222,19 @@ def cpu_baseline(w: wl.Workload, target_s: float = 10.0, threads: int = 0):
 
 # ------------------------------------------------------------ GPU workloads --
 
+def rotated_copies(w: wl.Workload) -> int:
+    """Input/output copies rotated between timed calls so that their set exceeds L2."""
+    return max(1, min(8, -(-ROTATE_TARGET // w.unique_bytes())))
+
+
+def workload_config(w: wl.Workload, world: int) -> dict:
+    """The `config` object of the JSON line (the same for both arms)."""
+    copies = rotated_copies(w)
+    return {"workload": w.name, "batch": w.batch, "M": w.M, "K": w.K, "N": list(w.N), "io": w.dtype,
+            "l2": f"rotating {copies} input/output copies ({copies * w.unique_bytes() / 2**20:.0f} MiB > L2)",
+            "parallelism": f"replica x{world}" if world > 1 else "single GPU"}
+
+
 class Case:
     """Device buffers (rotated copies), the fused plan and the unfused paths of one workload."""
 
@@ -232,8 +245,7 @@ class Case:
         self.plan = b2b.ChainPlan(w.dtype, w.batch, w.M, w.K, w.N)
         host = wl.make_inputs(w)
         self.host = host
-        per_copy = w.unique_bytes()
-        self.copies = max(1, min(8, -(-ROTATE_TARGET // per_copy)))
+        self.copies = rotated_copies(w)
         self.inputs = [[t.to(device) for t in host] for _ in range(self.copies)]
         _, out_dt = wl.io_dtypes(w.dtype)
         self.outs = [torch.empty(w.out_shape(), dtype=out_dt, device=device) for _ in range(self.copies)]
@@ -405,7 +417,7 @@ def run_reference(args):
         "impl": "reference", "metric": "fused B2B GEMM TFLOPS", "value": value, "unit": "TFLOP/s",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-        "data": "synthetic", "config": {"workload": w.name, "sample_rows": sw.M, "batch": sw.batch},
+        "data": "synthetic", "config": workload_config(w, world),
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": oracle.max_threads(), "kind": "oracle",
                          "sample": f"1 batch x {sw.M} rows of {w.name} per step ({sw.flops() / 1e9:.3f} GFLOP)"},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -496,10 +508,7 @@ def run_ours(args):
         "metric": "fused B2B GEMM TFLOPS", "value": value, "unit": "TFLOP/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": COMPUTE_DTYPE[w.dtype], "data": "synthetic",
-        "config": {"workload": w.name, "batch": w.batch, "M": w.M, "K": w.K, "N": list(w.N),
-                   "io": w.dtype, "l2": f"rotating {case.copies} input/output copies "
-                                         f"({case.copies * w.unique_bytes() / 2**20:.0f} MiB > L2)",
-                   "parallelism": f"replica x{world}" if world > 1 else "single GPU"},
+        "config": workload_config(w, world),
         "kernel_ms": kernel_ms,
         "eager_ms_per_call": float(np.median(per_eager)),
         "eager_ms_p10_p90": [float(np.percentile(per_eager, 10)), float(np.percentile(per_eager, 90))],

@@ -939,7 +939,6 @@ b2b_status_t run_chain_tc(b2b_plan_s* p, const void* const* W, const void* A, vo
   cudaError_t e;
   if (p->sn) {
     ChainNParams prm = p->pn;
-    prm.a_early = (p->tf0 || p->in_kind == kInTF32) ? 1 : 0;
     prm.status = p->d_status;
     prm.budget_ns = p->budget_ns;
     prm.debug = p->debug;
@@ -948,7 +947,6 @@ b2b_status_t run_chain_tc(b2b_plan_s* p, const void* const* W, const void* A, vo
                    stream, 2);
   } else {
     ChainParams prm = p->prm;
-    prm.a_early = p->in_kind == kInTF32 ? 1 : 0;
     prm.status = p->d_status;
     prm.budget_ns = p->budget_ns;
     prm.debug = p->debug;

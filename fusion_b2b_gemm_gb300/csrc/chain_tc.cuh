@@ -100,9 +100,6 @@ struct ChainParams {
   // the number of segments, then (first tile, tile count) of each, tiles
   // numbered batch-major; null = one contiguous range per CTA.
   const int* sched;
-  // A transpose kernel runs first and lets this kernel start only after the
-  // earlier kernels are complete: A may be read before this kernel's wait.
-  int a_early;
 };
 constexpr int kSchedSegs = 4;
 constexpr int kSchedStride = 1 + 2 * kSchedSegs;
@@ -404,18 +401,6 @@ __global__ void __launch_bounds__(kChainThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
-  // While the weight transpose in front of this kernel runs, pull this CTA's
-  // first A tile into L2 (only A: the weights are the transpose's output).
-  if (!RES && p.a_early && warp == 0 && lane == 0 && static_cast<int>(blockIdx.x) < p.total_tiles) {
-    const int b = static_cast<int>(blockIdx.x) / p.m_tiles;
-    const int mt = static_cast<int>(blockIdx.x) - b * p.m_tiles;
-    for (int kb = 0; kb < p.kpan0; ++kb) tma_prefetch_l2_3d(&tmA, kb * CK, mt * 128, b);
-  }
-  // The prologue above may overlap the previous kernel in the stream; no
-  // global memory is touched before that kernel has completed (except the
-  // prefetch of A above, see a_early).
-  grid_launch_dependents();
-  grid_dependency_wait();
 
   BoundedWait bw{abort_flag, p.status, p.budget_ns, kTimeoutCode};
 
@@ -454,6 +439,15 @@ __global__ void __launch_bounds__(kChainThreads, 1)
     first.init_segments(my_segs, my_nseg, p.m_tiles);
   else
     first.init(t_begin, t_step, p.m_tiles);
+  // Everything above may overlap the previous kernel in the stream: it reads
+  // only the plan's own tile schedule.  Before waiting for that kernel, pull
+  // this CTA's first A tile into L2.  A may be that kernel's output, but a
+  // prefetch touches L2 only, where its writes land too, and every load into
+  // shared memory comes after the wait, so no stale value is read.
+  if (warp == 0 && lane == 0 && t_count > 0)
+    for (int kb = 0; kb < p.kpan0; ++kb) tma_prefetch_l2_3d(&tmA, kb * CK, first.mt * 128, first.b);
+  grid_launch_dependents();
+  grid_dependency_wait();
   const int nph = NPH_FIXED + p.npass;
   const bool lookahead = p.lookahead != 0;
   // streamed weights with CTAs that run several tiles: A panels come through

@@ -92,8 +92,6 @@ struct ChainNParams {
   int w_merged;              // bit s: weight s is read as one 4-D box per half panel
   int split;                 // leftover tiles whose passes are split between two clusters
   uint32_t debug;            // test support: bit 0 = the first ring slot is never filled
-  int a_early;               // a transpose kernel runs first (see chain_tc.cuh): A may
-                             // be read before the dependency wait
   int* status;
   unsigned long long budget_ns;
 };
@@ -232,12 +230,17 @@ __global__ void __launch_bounds__(kChainNThreads, 1)
   cluster_sync();  // the peer's barriers exist before anything arrives on them
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
-  // mixed types: while the transpose of W0 runs, pull the first unit's A
-  // into L2
-  if (p.a_early && warp == 0 && lane == 0 && (blockIdx.x >> 1) < static_cast<unsigned>(p.total_tiles)) {
+  // Before waiting for the previous kernel in the stream, pull the first
+  // unit's A into L2.  A may be that kernel's output, but a prefetch touches
+  // L2 only, where its writes land too, and every load into shared memory
+  // comes after the wait, so no stale value is read.  At most four K panels
+  // (more only compete with that kernel's tail), all of them in a tf32 chain,
+  // whose weight transpose runs meanwhile.
+  if (warp == 0 && lane == 0 && (blockIdx.x >> 1) < static_cast<unsigned>(p.total_tiles)) {
     const ChainNUnit c = chainn_unit(p, static_cast<int>(blockIdx.x >> 1), static_cast<int>(gridDim.x >> 1), 0);
     const int m0 = c.mt * 256 + static_cast<int>(rank) * 128;
-    for (int q = 0; q < p.kpan[0]; ++q) tma_prefetch_l2_3d(&maps.a, q * CK0, m0, c.b);
+    const int npf = PT ? p.kpan[0] : (p.kpan[0] < 4 ? p.kpan[0] : 4);
+    for (int q = 0; q < npf; ++q) tma_prefetch_l2_3d(&maps.a, q * CK0, m0, c.b);
   }
   grid_launch_dependents();
   grid_dependency_wait();

@@ -444,8 +444,34 @@ __global__ void __launch_bounds__(kChainThreads, 1)
   // this CTA's first A tile into L2.  A may be that kernel's output, but a
   // prefetch touches L2 only, where its writes land too, and every load into
   // shared memory comes after the wait, so no stale value is read.
-  if (warp == 0 && lane == 0 && t_count > 0)
+  if (warp == 0 && lane == 0 && t_count > 0) {
     for (int kb = 0; kb < p.kpan0; ++kb) tma_prefetch_l2_3d(&tmA, kb * CK, first.mt * 128, first.b);
+    if constexpr (RES) {
+      // the weights of the first batch, and the second tile's A
+      const int b = first.b;
+      for (int kb = 0; kb < p.kpan0; ++kb) {
+        if (W_KMAJOR)
+          tma_prefetch_l2_3d(&tmW0, kb * CK, 0, b);
+        else if (p.w_merged & 1)
+          tma_prefetch_l2_4d(&tmW0, 0, kb * CK, 0, b);
+        else
+          for (int j = 0; j < N1P / WBOX_N; ++j) tma_prefetch_l2_3d(&tmW0, j * WBOX_N, kb * CK, b);
+      }
+      for (int kb = 0; kb < N1P / CK; ++kb) {
+        if (W_KMAJOR)
+          tma_prefetch_l2_3d(&tmW1, kb * CK, 0, b);
+        else if (p.w_merged & 2)
+          tma_prefetch_l2_4d(&tmW1, 0, kb * CK, 0, b);
+        else
+          for (int j = 0; j < NF / WBOX_N; ++j) tma_prefetch_l2_3d(&tmW1, j * WBOX_N, kb * CK, b);
+      }
+      if (t_count > 1) {
+        TileCursor second = first;
+        second.next();
+        for (int kb = 0; kb < p.kpan0; ++kb) tma_prefetch_l2_3d(&tmA, kb * CK, second.mt * 128, second.b);
+      }
+    }
+  }
   grid_launch_dependents();
   grid_dependency_wait();
   const int nph = NPH_FIXED + p.npass;

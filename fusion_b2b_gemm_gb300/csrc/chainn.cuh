@@ -241,6 +241,17 @@ __global__ void __launch_bounds__(kChainNThreads, 1)
     const int m0 = c.mt * 256 + static_cast<int>(rank) * 128;
     const int npf = PT ? p.kpan[0] : (p.kpan[0] < 4 ? p.kpan[0] : 4);
     for (int q = 0; q < npf; ++q) tma_prefetch_l2_3d(&maps.a, q * CK0, m0, c.b);
+    // and this CTA's half of the first GEMM's first weight panels (16-bit
+    // weights; a tf32 weight is the transpose's output, not yet written)
+    if (!TF0) {
+      const int n0 = static_cast<int>(rank) * (p.pw[0] / 2);
+      for (int q = 0; q < npf; ++q) {
+        if (p.w_merged & 1)
+          tma_prefetch_l2_4d(&maps.w[0], 0, q * CK, n0 / WBOX_N, c.b);
+        else
+          for (int j = 0; j < p.pw[0] / 2 / WBOX_N; ++j) tma_prefetch_l2_3d(&maps.w[0], n0 + j * WBOX_N, q * CK, c.b);
+      }
+    }
   }
   grid_launch_dependents();
   grid_dependency_wait();

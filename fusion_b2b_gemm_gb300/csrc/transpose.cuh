@@ -24,19 +24,24 @@ struct TransposeJob {
 
 __global__ void __launch_bounds__(256) transpose32_kernel(const __grid_constant__ TransposeJob job) {
   __shared__ uint32_t tile[32][33];
-  // Wait for the earlier kernels first, then let the chain kernel start: its
-  // start then implies that they are complete, so it may read A (which this
-  // kernel does not write) before its own wait.
-  ptx::grid_dependency_wait();
-  ptx::grid_launch_dependents();
   const int z = blockIdx.z;
-  const int mat = z / job.batch;
+  const int mat = z < job.count * job.batch ? z / job.batch : 0;
   const int b = z % job.batch;
-  if (mat >= job.count) return;
   const int R = job.rows[mat], C = job.cols[mat];
   const int r0 = blockIdx.y * 32, c0 = blockIdx.x * 32;
-  if (r0 >= R || c0 >= C) return;
+  const bool active = z < job.count * job.batch && r0 < R && c0 < C;
   const uint32_t* in = job.in[mat] + static_cast<size_t>(b) * R * C;
+  // Pull this tile's input rows into L2 before waiting for the earlier
+  // kernels (the weights may be their output, but a prefetch touches L2
+  // only, where their writes land too, and the loads below come after the
+  // wait).
+  if (active && threadIdx.x < 32 && r0 + static_cast<int>(threadIdx.x) < R)
+    ptx::prefetch_l2(in + static_cast<size_t>(r0 + threadIdx.x) * C + c0);
+  // Wait for the earlier kernels (the previous chain kernel reads the
+  // workspace written below), then let the chain kernel start.
+  ptx::grid_dependency_wait();
+  ptx::grid_launch_dependents();
+  if (!active) return;
   uint32_t* out = job.out[mat] + static_cast<size_t>(b) * R * C;
   const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;  // 32 x 8
 #pragma unroll

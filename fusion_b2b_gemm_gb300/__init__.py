@@ -112,6 +112,43 @@ def _stream_handle(stream) -> Optional[int]:
     return stream.cuda_stream or None
 
 
+def _torch_types(dtype: str):
+    """(type of A, type of each weight by stage, type of the output) of a chain type."""
+    import torch
+    f16, bf16, f32, f64 = torch.float16, torch.bfloat16, torch.float32, torch.float64
+    a, later, out = {"f16_f32out": (f16, f16, f32), "f16": (f16, f16, f16), "bf16": (bf16, bf16, bf16),
+                     "bf16_f32out": (bf16, bf16, f32), "tf32": (f32, f32, f32), "f64": (f64, f64, f64),
+                     "tf32_f16": (f32, f16, f32), "tf32_bf16": (f32, bf16, f32)}[dtype]
+    # mixed types: fp32 A and first weight (tf32 operands), 16-bit later weights
+    return a, (lambda s: a if s == 0 else later), out
+
+
+def check_operands(dtype: str, batch: int, M: int, K: int, N: Sequence[int], A, Ws: Sequence, D) -> None:
+    """Check the tensors of one run against the plan's sizes and types.
+
+    The kernels read and write exactly the plan's sizes (A [batch][M][K], W_s
+    [batch][K_s][N_s], D [batch][M][N_last], dense), so a tensor with fewer
+    elements, or of another type, would let them reach past its end: refused
+    here.  A plan without rows reads and writes nothing.
+    """
+    if batch * M == 0:
+        return
+    ta, tw, to = _torch_types(dtype)
+    kin = K
+    need = [("A", A, ta, batch * M * K)]
+    for s, (n, w) in enumerate(zip(N, Ws)):
+        need.append((f"W[{s}]", w, tw(s), batch * kin * n))
+        kin = n
+    need.append(("D", D, to, batch * M * N[-1]))
+    for name, t, want, count in need:
+        if t is None:
+            continue  # a missing operand is the C ABI's argument error
+        if t.dtype != want:
+            raise TypeError(f"{name}: {t.dtype} given, {want} expected for a {dtype} chain")
+        if t.numel() < count:
+            raise ValueError(f"{name}: {t.numel()} elements given, the plan reads or writes {count}")
+
+
 def _ptr(t) -> Optional[int]:
     if t is None:
         return None
@@ -163,6 +200,7 @@ class Plan:
         """Launch on ``stream`` (default: torch's current stream); returns D."""
         if D is None:
             D = self.empty_out(A.device)
+        check_operands(self.dtype, self.batch, self.M, self.K, self.N, A, [B, C, F][:len(self.N)], D)
         code = _lib.b2b_run(self._h, _ptr(A), _ptr(B), _ptr(C), _ptr(F), _ptr(D), _stream_handle(stream))
         _check(code, "b2b_run")
         return D
@@ -362,6 +400,7 @@ class ChainPlan(Plan):
         """Launch on ``stream`` (default: torch's current stream); returns D."""
         if D is None:
             D = self.empty_out(A.device)
+        check_operands(self.dtype, self.batch, self.M, self.K, self.N, A, list(Ws)[:len(self.N)], D)
         ptrs = (ctypes.c_void_p * max(1, len(Ws)))(*[_ptr(w) for w in Ws])
         _check(_lib.b2b_chain_run(self._h, _ptr(A), ptrs, _ptr(D), _stream_handle(stream)), "b2b_chain_run")
         return D

@@ -208,3 +208,47 @@ def test_generator_rejects_a_source_used_twice():
     with pytest.raises(b2b.B2BError) as e:
         b2b.coordination_matrix([[0, 0], [1, 1]], [[0, 0], [0, 1]])
     assert e.value.code == 1
+
+
+# ------------------------------------------- operand checks of the binding --
+
+def test_operand_checks_refuse_short_or_mistyped_tensors():
+    """The kernels read and write the plan's full sizes, so the binding refuses
+    a tensor with fewer elements or of another type before any launch."""
+    import torch
+    f16, f32 = torch.float16, torch.float32
+    N = (64, 32)
+    A = torch.zeros(2, 100, 48, dtype=f16)
+    W = [torch.zeros(2, 48, 64, dtype=f16), torch.zeros(2, 64, 32, dtype=f16)]
+    D = torch.zeros(2, 100, 32, dtype=f16)
+    b2b.check_operands("f16", 2, 100, 48, N, A, W, D)           # exact sizes
+    b2b.check_operands("f16", 2, 100, 48, N, A, W, torch.zeros(7000, dtype=f16))  # larger is fine
+    with pytest.raises(ValueError, match="A"):
+        b2b.check_operands("f16", 2, 100, 48, N, A[:, :99], W, D)
+    with pytest.raises(ValueError, match=r"W\[1\]"):
+        b2b.check_operands("f16", 2, 100, 48, N, A, [W[0], W[1][:1]], D)
+    with pytest.raises(ValueError, match="D"):
+        b2b.check_operands("f16", 2, 100, 48, N, A, W, D[:1])
+    with pytest.raises(TypeError, match="D"):
+        b2b.check_operands("f16", 2, 100, 48, N, A, W, D.float())   # f16 out expected
+    with pytest.raises(TypeError, match="A"):
+        b2b.check_operands("f16_f32out", 2, 100, 48, N, A.bfloat16(), W, D.float())
+    # a missing operand is left to the C ABI's argument error
+    b2b.check_operands("f16", 2, 100, 48, N, A, [W[0], None], D)
+    # a plan without rows reads and writes nothing
+    b2b.check_operands("f16", 2, 0, 48, N, A[:, :0], [w[:0] for w in W], D[:, :0])
+
+
+def test_operand_checks_follow_the_mixed_types():
+    """Mixed cascades: fp32 A and first weight, 16-bit later weights, fp32 out."""
+    import torch
+    N = (64, 32, 16)
+    A = torch.zeros(1, 10, 8, dtype=torch.float32)
+    W = [torch.zeros(1, 8, 64, dtype=torch.float32), torch.zeros(1, 64, 32, dtype=torch.bfloat16),
+         torch.zeros(1, 32, 16, dtype=torch.bfloat16)]
+    D = torch.zeros(1, 10, 16, dtype=torch.float32)
+    b2b.check_operands("tf32_bf16", 1, 10, 8, N, A, W, D)
+    with pytest.raises(TypeError, match=r"W\[1\]"):
+        b2b.check_operands("tf32_f16", 1, 10, 8, N, A, W, D)      # fp16 later weights expected
+    with pytest.raises(TypeError, match=r"W\[0\]"):
+        b2b.check_operands("tf32_bf16", 1, 10, 8, N, A, [W[0].bfloat16()] + W[1:], D)

@@ -295,6 +295,12 @@ def test_argument_errors_on_device():
     with pytest.raises(b2b.B2BError) as e:       # 2-byte offset: not 16-byte aligned
         plan.run(raw[1:1 + 128 * 64], B, B, None, D)
     assert e.value.code == 3
+    with pytest.raises(ValueError):              # A shorter than the plan's rows
+        plan.run(A[:, :64].contiguous(), B, B, None, D)
+    with pytest.raises(TypeError):               # output of another type
+        plan.run(A, B, B, None, D.float())
+    torch.cuda.synchronize()
+    assert plan.status() == 0                    # nothing was launched
 
 
 # ------------------------------------------ unfused reference building block --

@@ -53,7 +53,7 @@ typedef struct CUstream_st* b2b_stream_t;
 typedef enum {
   B2B_OK = 0,
   B2B_ERR_INVALID_ARG = 1, /* null plan/pointer, bad size                   */
-  B2B_ERR_UNSUPPORTED = 2, /* valid request this build has no kernel for    */
+  B2B_ERR_UNSUPPORTED = 2, /* valid request the library has no kernel for  */
   B2B_ERR_ALIGNMENT = 3,   /* pointer not 16-byte aligned                   */
   B2B_ERR_ALIAS = 4,       /* output overlaps an input                      */
   B2B_ERR_DEVICE = 5,      /* current device is not sm_103 (GB300)          */
@@ -86,7 +86,7 @@ typedef enum {
  *   K        contraction length of GEMM1, >= 1.
  *   N1, N2   output widths of GEMM1 and GEMM2.
  *   N3       output width of GEMM3, or 0 for a two-stage chain.
- * Sizes this build supports (otherwise B2B_ERR_UNSUPPORTED):
+ * Sizes the library supports (otherwise B2B_ERR_UNSUPPORTED):
  *   16-bit types: K % 8 == 0; N1, N2 (and N3) % 8 == 0; intermediate
  *                 widths (N1, and N2 of a three-stage chain) <= 512; the
  *                 last width <= 4096 (the last GEMM runs in passes of up to

@@ -195,6 +195,9 @@ EDGES = [
     wl.Workload("tf32_pairs_ktail", "tf32", 2, 10000, 68, (256, 256), "normal", 1.0 / 16, 88),
     wl.Workload("tf32_pairs_n128", "tf32", 1, 20000, 256, (128, 96), "normal", 1.0 / 16, 89),
     wl.Workload("tf32_pairs_mtail", "tf32", 3, 7000, 32, (72, 256), "normal", 1.0 / 16, 90),
+    # a tf32 chain with more tiles than SMs but a last GEMM wider than 256
+    # columns stays on the one-CTA kernel, several tiles per CTA
+    wl.Workload("tf32_wide_many_tiles", "tf32", 2, 10000, 64, (128, 384), "normal", 1.0 / 16, 92),
 ]
 
 

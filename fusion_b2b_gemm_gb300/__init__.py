@@ -123,14 +123,22 @@ def _torch_types(dtype: str):
     return a, (lambda s: a if s == 0 else later), out
 
 
-def check_operands(dtype: str, batch: int, M: int, K: int, N: Sequence[int], A, Ws: Sequence, D) -> None:
-    """Check the tensors of one run against the plan's sizes and types.
+def check_operands(dtype: str, batch: int, M: int, K: int, N: Sequence[int], A, Ws: Sequence, D,
+                   device: Optional[int] = None) -> None:
+    """Check the tensors of one run against the plan's sizes, types and device.
 
     The kernels read and write exactly the plan's sizes (A [batch][M][K], W_s
     [batch][K_s][N_s], D [batch][M][N_last], dense), so a tensor with fewer
     elements, or of another type, would let them reach past its end: refused
-    here.  A plan without rows reads and writes nothing.
+    here.  A plan is bound to the GPU that was current when it was created
+    (``device``), and its kernels run there: a tensor on another GPU would be
+    read through a peer address, so it is refused too.  A plan without rows
+    reads and writes nothing.
     """
+    if device is not None:
+        for name, t in [("A", A), ("D", D)] + [(f"W[{s}]", w) for s, w in enumerate(Ws)]:
+            if t is not None and t.is_cuda and t.device.index != device:
+                raise ValueError(f"{name} is on cuda:{t.device.index}, the plan on cuda:{device}")
     if batch * M == 0:
         return
     ta, tw, to = _torch_types(dtype)
@@ -147,6 +155,12 @@ def check_operands(dtype: str, batch: int, M: int, K: int, N: Sequence[int], A, 
             raise TypeError(f"{name}: {t.dtype} given, {want} expected for a {dtype} chain")
         if t.numel() < count:
             raise ValueError(f"{name}: {t.numel()} elements given, the plan reads or writes {count}")
+
+
+def _current_device() -> int:
+    """The CUDA device a new plan binds to (the current one)."""
+    import torch
+    return torch.cuda.current_device()
 
 
 def _ptr(t) -> Optional[int]:
@@ -177,6 +191,7 @@ class Plan:
             code = _lib.b2b_plan_create(ctypes.byref(h), DTYPES[dtype], batch, M, K, N1, N2, N3)
         _check(code, "b2b_plan_create")
         self._h = h
+        self.device_index = _current_device()
 
     # -- torch helpers ---------------------------------------------------
     def io_dtypes(self):
@@ -200,7 +215,8 @@ class Plan:
         """Launch on ``stream`` (default: torch's current stream); returns D."""
         if D is None:
             D = self.empty_out(A.device)
-        check_operands(self.dtype, self.batch, self.M, self.K, self.N, A, [B, C, F][:len(self.N)], D)
+        check_operands(self.dtype, self.batch, self.M, self.K, self.N, A, [B, C, F][:len(self.N)], D,
+                       self.device_index)
         code = _lib.b2b_run(self._h, _ptr(A), _ptr(B), _ptr(C), _ptr(F), _ptr(D), _stream_handle(stream))
         _check(code, "b2b_run")
         return D
@@ -395,12 +411,14 @@ class ChainPlan(Plan):
         _check(_lib.b2b_chain_plan_create(ctypes.byref(h), DTYPES[dtype], batch, M, K, len(widths), arr),
                "b2b_chain_plan_create")
         self._h = h
+        self.device_index = _current_device()
 
     def run(self, A, Ws: Sequence, D=None, stream=None):
         """Launch on ``stream`` (default: torch's current stream); returns D."""
         if D is None:
             D = self.empty_out(A.device)
-        check_operands(self.dtype, self.batch, self.M, self.K, self.N, A, list(Ws)[:len(self.N)], D)
+        check_operands(self.dtype, self.batch, self.M, self.K, self.N, A, list(Ws)[:len(self.N)], D,
+                       self.device_index)
         ptrs = (ctypes.c_void_p * max(1, len(Ws)))(*[_ptr(w) for w in Ws])
         _check(_lib.b2b_chain_run(self._h, _ptr(A), ptrs, _ptr(D), _stream_handle(stream)), "b2b_chain_run")
         return D

@@ -138,10 +138,12 @@ class FusedGemmChain(torch.nn.Module):
         self._plans: Dict[Tuple, object] = {}
 
     def _plan(self, key):
+        # (the plan binds to the device that is current when it is created:
+        # the caller makes it the activations' device)
         plan = self._plans.get(key)
         if plan is None:
             from . import ChainPlan
-            dt, batch, M, K, widths = key
+            dt, batch, M, K, widths, _device = key
             plan = ChainPlan(dt, batch, M, K, widths)
             self._plans[key] = plan
         return plan
@@ -183,8 +185,10 @@ class FusedGemmChain(torch.nn.Module):
             if w.shape[-2] != kin:
                 raise ValueError(f"FusedGemmChain: right operand {tuple(w.shape)} does not follow width {kin}")
             kin = w.shape[-1]
-        plan = self._plan((dt, batch, M, K, widths))
-        out = plan.run(a, ws)
+        # plans are per device: create and run this one on the activations' GPU
+        with torch.cuda.device(x.device):
+            plan = self._plan((dt, batch, M, K, widths, x.device.index))
+            out = plan.run(a, ws)
         return out.reshape(*lead, widths[-1])
 
 

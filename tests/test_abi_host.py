@@ -252,3 +252,31 @@ def test_operand_checks_follow_the_mixed_types():
         b2b.check_operands("tf32_f16", 1, 10, 8, N, A, W, D)      # fp16 later weights expected
     with pytest.raises(TypeError, match=r"W\[0\]"):
         b2b.check_operands("tf32_bf16", 1, 10, 8, N, A, [W[0].bfloat16()] + W[1:], D)
+
+
+def test_operand_checks_refuse_tensors_on_another_gpu():
+    """A plan runs on the GPU it was created on; a tensor of another GPU would
+    be read through a peer address, so the binding refuses it."""
+    import torch
+
+    class OnGpu:
+        """Stands for a CUDA tensor on device `index` (no GPU here)."""
+
+        def __init__(self, t, index):
+            self.t, self.is_cuda, self.dtype = t, True, t.dtype
+            self.device = torch.device("cuda", index)
+
+        def numel(self):
+            return self.t.numel()
+
+    f16 = torch.float16
+    N = (64, 32)
+    A = OnGpu(torch.zeros(2, 100, 48, dtype=f16), 1)
+    W = [OnGpu(torch.zeros(2, 48, 64, dtype=f16), 1), OnGpu(torch.zeros(2, 64, 32, dtype=f16), 1)]
+    D = OnGpu(torch.zeros(2, 100, 32, dtype=f16), 1)
+    b2b.check_operands("f16", 2, 100, 48, N, A, W, D, device=1)
+    for bad in ("A", "W[1]", "D"):
+        args = {"A": A, "W[0]": W[0], "W[1]": W[1], "D": D}
+        args[bad] = OnGpu(args[bad].t, 0)
+        with pytest.raises(ValueError, match=bad.replace("[", r"\[").replace("]", r"\]")):
+            b2b.check_operands("f16", 2, 100, 48, N, args["A"], [args["W[0]"], args["W[1]"]], args["D"], device=1)

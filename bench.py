@@ -522,12 +522,39 @@ def run_ours(args):
     }
     if rank == 0 and not args.quick:
         line["cpu_baseline"] = cpu_baseline(w, target_s=args.cpu_s)
-        line["per_config"] = per_config(args, peaks_all, device, stream)
+        detail = per_config(args, peaks_all, device, stream)
+        # the full record of every workload first, one line each; the
+        # headline line ends with the short form of each, so that a reader
+        # who keeps only the end of the output still sees every workload
+        for entry in detail:
+            print(json.dumps({"per_config_detail": entry}), flush=True)
+        line["per_config"] = [compact_config(e) for e in detail]
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
         torch.distributed.destroy_process_group()
     return 0
+
+
+def _sig(x, digits=3):
+    """x rounded to `digits` significant digits (None stays None)."""
+    if x is None:
+        return None
+    return float(f"{x:.{digits}g}")
+
+
+def compact_config(e: dict) -> dict:
+    """The short record of one workload for the headline line: device times
+    per call in microseconds, the speed-up over the faster unfused path, the
+    roofline side and fraction, and the CPU oracle's rate."""
+    r = e["roofline"]
+    out = {"w": e["workload"], "fused_us": _sig(e["fused_ms"] * 1e3), "torch_us": _sig(e["unfused_torch_ms"] * 1e3),
+           "own_us": _sig(e["unfused_own_ms"] * 1e3) if e["unfused_own_ms"] is not None else None,
+           "speedup": _sig(e["speedup_vs_best_unfused"]),
+           "bound": r["bound"], "frac": _sig(r["frac"])}
+    if "cpu_oracle" in e:
+        out["cpu_tflops"] = _sig(e["cpu_oracle"]["value"])
+    return out
 
 
 def per_config(args, peaks_all, device, stream):

@@ -21,7 +21,7 @@ __all__ = [
     "b2b_plan_destroy",
     "b2b_plan_device_status", "b2b_plan_set_wait_budget", "b2b_plan_set_debug", "b2b_plan_info",
     "b2b_status_string", "b2b_coordination_matrix", "b2b_probe_operand_image",
-    "b2b_probe_f64_rearrange", "b2b_run_tf32_noalloc", "coordination_matrix",
+    "b2b_probe_operand_layout", "b2b_probe_f64_rearrange", "b2b_run_tf32_noalloc", "coordination_matrix",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -68,6 +68,7 @@ def _load() -> ctypes.CDLL:
         "b2b_plan_info": [P, ip, ip, ip, ip, ip, ip, ip],
         "b2b_coordination_matrix": [i32, i32, ip, ip, ip, ip, ip],
         "b2b_probe_operand_image": [i32, i32, P, P, P],
+        "b2b_probe_operand_layout": [i32, i32, i32, i32, P, P, P],
         "b2b_probe_f64_rearrange": [i32, P, P, P],
         "b2b_run_tf32_noalloc": [i64, i64, i64, i64, i64, P, P, P, P, P],
     }
@@ -96,6 +97,7 @@ b2b_plan_info = _lib.b2b_plan_info
 b2b_status_string = _lib.b2b_status_string
 b2b_coordination_matrix = _lib.b2b_coordination_matrix
 b2b_probe_operand_image = _lib.b2b_probe_operand_image
+b2b_probe_operand_layout = _lib.b2b_probe_operand_layout
 b2b_probe_f64_rearrange = _lib.b2b_probe_f64_rearrange
 b2b_run_tf32_noalloc = _lib.b2b_run_tf32_noalloc
 
@@ -459,6 +461,20 @@ def probe_operand_image(dtype: str, acc):
         out = torch.empty((width * 256 // 4,), dtype=torch.int32, device=acc.device)
     _check(_lib.b2b_probe_operand_image(DTYPES[dtype], width, _ptr(acc.contiguous()), _ptr(out),
                                         _stream_handle(None)), "b2b_probe_operand_image")
+    return out
+
+
+PROBE_TMEM16, PROBE_PAIR_CONVERTERS = 1, 2  # B2B_PROBE_*
+
+
+def probe_operand_layout(dtype: str, form: int, acc, region: int = 0):
+    """Run another form of the 16-bit rearrangement on acc (torch fp32 [128, width] on the GPU)."""
+    import torch
+    width = acc.shape[1]
+    words = 128 * width // 2 if form == PROBE_TMEM16 else width * 256 // 4
+    out = torch.empty((words,), dtype=torch.int32, device=acc.device)
+    _check(_lib.b2b_probe_operand_layout(DTYPES[dtype], form, width, region, _ptr(acc.contiguous()), _ptr(out),
+                                         _stream_handle(None)), "b2b_probe_operand_layout")
     return out
 
 

@@ -30,6 +30,7 @@ static_assert(kMaxStages == B2B_MAX_STAGES, "stage limit of the C interface");
 namespace {
 
 constexpr uint64_t kDefaultBudgetNs = 2000000000ull;
+constexpr uint64_t kMinBudgetNs = 1000000ull;  // 1 ms
 constexpr int kSmemOptin = 232448;         // 227 KB per CTA on sm_100 / sm_103
 constexpr int kSmemBudget = kSmemOptin - 1024;  // minus the 1024-byte alignment slack
 
@@ -693,8 +694,11 @@ b2b_status_t create_common(b2b_plan_t* out, b2b_dtype_t dt, int stages, bool sin
   } else {
     p->kind = single ? kPlanGemmTC : kPlanChainTC;
     st = setup_chain_tc(p);
+    // (the limit is a property of the kernel, shared by every plan that runs
+    // it: always the largest any plan asks for, so that a plan created later
+    // never lowers it below an earlier plan's size)
     if (st == B2B_OK &&
-        cudaFuncSetAttribute(p->fn, cudaFuncAttributeMaxDynamicSharedMemorySize, p->smem_bytes) !=
+        cudaFuncSetAttribute(p->fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemOptin) !=
             cudaSuccess) {
       cudaGetLastError();
       st = B2B_ERR_CUDA;
@@ -1083,7 +1087,10 @@ b2b_status_t b2b_plan_device_status(b2b_plan_t p, b2b_stream_t stream) {
 
 b2b_status_t b2b_plan_set_wait_budget(b2b_plan_t p, uint64_t budget_ns) {
   if (!p) return B2B_ERR_INVALID_ARG;
-  p->budget_ns = budget_ns ? budget_ns : kDefaultBudgetNs;
+  // After an abort the same budget bounds the waits for copies and MMAs
+  // already in flight before tensor memory is freed: it must stay long
+  // against any one of them (microseconds), hence the floor.
+  p->budget_ns = budget_ns ? std::max<uint64_t>(budget_ns, kMinBudgetNs) : kDefaultBudgetNs;
   return B2B_OK;
 }
 
@@ -1152,6 +1159,46 @@ b2b_status_t b2b_probe_operand_image(b2b_dtype_t dtype, int width, const void* a
   return B2B_OK;
 }
 
+b2b_status_t b2b_probe_operand_layout(b2b_dtype_t dtype, int form, int width, int region, const void* acc,
+                                      void* out, b2b_stream_t stream) {
+  if (!acc || !out) return B2B_ERR_INVALID_ARG;
+  int in_kind, out_kind, esz, osz;
+  type_info(dtype, &in_kind, &out_kind, &esz, &osz);
+  if (in_kind != kInF16 && in_kind != kInBF16) return B2B_ERR_UNSUPPORTED;
+  if (form == B2B_PROBE_TMEM16) {
+    if ((width != 64 && width != 128 && width != 256) || region != 0) return B2B_ERR_INVALID_ARG;
+  } else if (form == B2B_PROBE_PAIR_CONVERTERS) {
+    if (width < 128 || width > 512 || width % 128 || (region != 0 && region != 1)) return B2B_ERR_INVALID_ARG;
+  } else {
+    return B2B_ERR_INVALID_ARG;
+  }
+  b2b_status_t st = check_device(nullptr, nullptr);
+  if (st != B2B_OK) return st;
+  const bool f16 = in_kind == kInF16;
+  const void* fn = form == B2B_PROBE_TMEM16
+                       ? (f16 ? reinterpret_cast<const void*>(&probe_layout_kernel<kInF16, 1>)
+                              : reinterpret_cast<const void*>(&probe_layout_kernel<kInBF16, 1>))
+                       : (f16 ? reinterpret_cast<const void*>(&probe_layout_kernel<kInF16, 2>)
+                              : reinterpret_cast<const void*>(&probe_layout_kernel<kInBF16, 2>));
+  const int smem = form == B2B_PROBE_TMEM16 ? 1024 : width * 256 + 1024;
+  if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess) {
+    cudaGetLastError();
+    return B2B_ERR_CUDA;
+  }
+  const uint32_t* a = static_cast<const uint32_t*>(acc);
+  uint32_t* o = static_cast<uint32_t*>(out);
+  uint32_t r0 = static_cast<uint32_t>(region);
+  uint32_t cols = form == B2B_PROBE_TMEM16 ? pow2_cols(static_cast<uint32_t>(width)) : 512u;
+  void* args[5] = {&a, &o, &width, &r0, &cols};
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (cudaLaunchKernel(fn, dim3(1), dim3(256), args, static_cast<size_t>(smem), s) != cudaSuccess ||
+      cudaStreamSynchronize(s) != cudaSuccess) {
+    cudaGetLastError();
+    return B2B_ERR_CUDA;
+  }
+  return B2B_OK;
+}
+
 b2b_status_t b2b_probe_f64_rearrange(int tiles, const double* cfrag, double* afrag,
                                      b2b_stream_t stream) {
   if (!cfrag || !afrag || tiles < 1 || tiles > 8) return B2B_ERR_INVALID_ARG;
@@ -1190,13 +1237,16 @@ b2b_status_t b2b_probe_f64_rearrange(int tiles, const double* cfrag, double* afr
 //
 // The array is `kNoAllocScratchWords` 32-bit words (4 MiB) on every GPU that
 // loads the library, held until the process exits.  Its device address is
-// looked up once per device, on the first call made while that device is
-// current; make that first call before any stream capture.  Every call shares
-// the one array and leaves the last call's transposed weights in it; calls
-// whose kernels overlap on the GPU (different streams, no ordering) race on
-// it.  Nothing in it needs to start at zero: each call writes the part it
-// reads before reading it.  A kernel that gives up a bounded wait still
-// returns, but this entry point has no status word to report it.
+// looked up once per device (and again only if that device's context has
+// been replaced, e.g. after a device reset), on the first call made while
+// that device is current; make that first call before any stream capture.
+// The same first call sets the kernel's shared-memory limit on that device.
+// Every call shares the one array and leaves the last call's transposed
+// weights in it; calls whose kernels overlap on the GPU (different streams,
+// no ordering) race on it.  Nothing in it needs to start at zero: each call
+// writes the part it reads before reading it.  A kernel that gives up a
+// bounded wait still returns, but this entry point has no status word to
+// report it.
 namespace {
 
 constexpr size_t kNoAllocScratchWords = size_t(1) << 20;
@@ -1204,20 +1254,67 @@ __device__ __align__(256) uint32_t g_noalloc_scratch[kNoAllocScratchWords];
 
 constexpr int kMaxDevices = 64;
 std::mutex g_noalloc_mu;
-void* g_noalloc_ptr[kMaxDevices];
 
-b2b_status_t noalloc_scratch(int dev, void** out) {
+// Per device: the context the entries below belong to, the scratch address
+// in it, and the kernels whose shared-memory limit is already raised there.
+struct NoAllocDevice {
+  void* ctx;
+  void* scratch;
+  std::vector<const void*> configured;
+};
+NoAllocDevice g_noalloc_dev[kMaxDevices];
+
+typedef CUresult (*CtxGetCurrentFn)(CUcontext*);
+
+CtxGetCurrentFn ctx_get_current_fn() {
+  static CtxGetCurrentFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<CtxGetCurrentFn>(f);
+  });
+  return fn;
+}
+
+// Set-up of the current device `dev` for the allocation-free call: the
+// scratch array's device address (looked up with cudaGetSymbolAddress, not
+// the host-side name of the array, which is no device address), and the
+// dynamic shared-memory limit of kernel `fn`.  Both are cached per device
+// and context, so later calls make no runtime call for them.
+b2b_status_t noalloc_setup(int dev, const void* fn, void** scratch) {
   if (dev < 0 || dev >= kMaxDevices) return B2B_ERR_DEVICE;
+  const CtxGetCurrentFn get = ctx_get_current_fn();
+  if (!get) return B2B_ERR_CUDA;
+  CUcontext ctx = nullptr;
+  if (get(&ctx) != CUDA_SUCCESS) return B2B_ERR_CUDA;
   std::lock_guard<std::mutex> lock(g_noalloc_mu);
-  if (!g_noalloc_ptr[dev]) {
+  NoAllocDevice& d = g_noalloc_dev[dev];
+  if (!ctx || d.ctx != static_cast<void*>(ctx) || !d.scratch) {
+    // (the runtime makes the device's primary context current here if no
+    // context was current yet)
     void* ptr = nullptr;
     if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || !ptr) {
       cudaGetLastError();
       return B2B_ERR_CUDA;
     }
-    g_noalloc_ptr[dev] = ptr;
+    if (!ctx && (get(&ctx) != CUDA_SUCCESS || !ctx)) return B2B_ERR_CUDA;
+    d.ctx = ctx;
+    d.scratch = ptr;
+    d.configured.clear();
   }
-  *out = g_noalloc_ptr[dev];
+  if (std::find(d.configured.begin(), d.configured.end(), fn) == d.configured.end()) {
+    // the largest dynamic shared memory any plan of this kernel asks for
+    if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemOptin) != cudaSuccess) {
+      cudaGetLastError();
+      return B2B_ERR_CUDA;
+    }
+    d.configured.push_back(fn);
+  }
+  *scratch = d.scratch;
   return B2B_OK;
 }
 
@@ -1236,10 +1333,6 @@ extern "C" b2b_status_t b2b_run_tf32_noalloc(int64_t batch, int64_t M, int64_t K
   int dev = 0, sms = 0;
   st = check_device(&dev, &sms);
   if (st != B2B_OK) return st;
-  void* scratch = nullptr;
-  st = noalloc_scratch(dev, &scratch);
-  if (st != B2B_OK) return st;
-
   // A plan on the stack: tiling only, no device memory of its own.
   b2b_plan_s pl;
   pl.kind = kPlanChainTC;
@@ -1257,7 +1350,7 @@ extern "C" b2b_status_t b2b_run_tf32_noalloc(int64_t batch, int64_t M, int64_t K
   pl.debug = 0;
   pl.tf0 = false;
   pl.d_status = nullptr;
-  pl.d_wt = scratch;
+  pl.d_wt = nullptr;
   pl.d_sched = nullptr;
   pl.wt_bytes = kNoAllocScratchWords * sizeof(uint32_t);
   pl.cache_n = 0;
@@ -1265,11 +1358,10 @@ extern "C" b2b_status_t b2b_run_tf32_noalloc(int64_t batch, int64_t M, int64_t K
   type_info(B2B_TF32, &pl.in_kind, &pl.out_kind, &pl.esz, &pl.osz);
   st = setup_chain_tc(&pl);
   if (st != B2B_OK) return st;
-  if (cudaFuncSetAttribute(pl.fn, cudaFuncAttributeMaxDynamicSharedMemorySize, pl.smem_bytes) !=
-      cudaSuccess) {
-    cudaGetLastError();
-    return B2B_ERR_CUDA;
-  }
+  void* scratch = nullptr;
+  st = noalloc_setup(dev, pl.fn, &scratch);
+  if (st != B2B_OK) return st;
+  pl.d_wt = scratch;
   if (pl.sn) {
     st = pair_grid(&pl);
     if (st != B2B_OK) return st;

@@ -159,6 +159,20 @@ __device__ __forceinline__ uint32_t tmem_col(uint32_t r0, int c) {
   return ((((static_cast<uint32_t>(c) >> 8) ^ r0) & 1u) << 8) | (static_cast<uint32_t>(c) & 255u);
 }
 
+// One converter warp's share of 128-column chunk `ch` of an intermediate
+// whose accumulator starts in region r0: the two warps that share a TMEM lane
+// quadrant take 64 columns each (h = 0: the low half, h = 1: the high half),
+// rounded into the K-major swizzled operand image `p_img` (128-byte panels
+// of 64 K elements, one per 64 columns).  `lane_off` selects the warp's lane
+// quadrant, `row` is the thread's row of the tile.
+template <int IN>
+__device__ __forceinline__ void convert_chunk_half(uint32_t tmem_base, uint32_t lane_off, uint32_t r0, int ch,
+                                                   int h, int row, uint32_t p_img) {
+  const int pcol = ch * 128 + h * 64;
+  rearrange_accumulator<IN>(tmem_base + lane_off + tmem_col(r0, pcol), 64, row,
+                            p_img + static_cast<uint32_t>(pcol / 64) * kPanelBytes);
+}
+
 // TF0: the first GEMM takes fp32 A and W0 as tf32 operands (W0 transposed to
 // [N][K], K-major, which the tf32 MMA reads), and its result is rounded to
 // the 16-bit type IN of every later GEMM: a mixed-type cascade, where the
@@ -584,14 +598,12 @@ __global__ void __launch_bounds__(kChainNThreads, 1)
         const int nch = p.wpad[s] / 128;
         const int cpp = p.pw[s] / 128;  // chunks per pass
         for (int ch = 0; ch < nch; ++ch) {
-          const int pcol = ch * 128 + h * 64;
           if (s == 0 && (cpp == 1 || !(ch & 1))) {
             if (ok) ok = warp_wait(bw, bar(knCFull0 + (cpp == 1 ? ch : ch >> 1)), static_cast<uint32_t>(it) & 1u);
             if (ok) tc_fence_after();
           }
           if (ok) {
-            rearrange_accumulator<IN>(tmem_base + lane_off + tmem_col(r0, pcol), 64, row,
-                                      p_img + static_cast<uint32_t>(pcol / 64) * kPanelBytes);
+            convert_chunk_half<IN>(tmem_base, lane_off, r0, ch, h, row, p_img);
             tc_fence_before();
           }
           named_bar_sync(2, 256);
@@ -671,6 +683,82 @@ __global__ void __launch_bounds__(kChainNThreads, 1)
     tc_fence_after();
     tmem_dealloc<CG>(tmem_base, kCols);
   }
+}
+
+// Test support: the layout probes of the rearrangement code that tensor
+// memory holds an operand for, or that two warps share per lane quadrant.
+//   FORM 1: the 16-bit intermediate kept in tensor memory (two-stage chains
+//           with resident weights): `acc` [128][width] goes into columns
+//           [0, width) in the accumulator layout, rearrange_accumulator_tmem16
+//           packs it in place, and columns [0, width / 2) are copied to `out`
+//           ([128][width / 2] 32-bit words, row-major).
+//   FORM 2: the converters of the pair kernel: `acc` goes into tensor memory
+//           as an accumulator that starts in region r0 (column c at
+//           tmem_col(r0, c)), eight warps convert it chunk by chunk with
+//           convert_chunk_half, and the operand image (width * 256 bytes) is
+//           copied to `out`.
+// One CTA of 256 threads (FORM 1 uses the first 128).
+template <int IN, int FORM>
+__global__ void __launch_bounds__(256, 1)
+    probe_layout_kernel(const uint32_t* __restrict__ acc, uint32_t* __restrict__ out, int width, uint32_t r0,
+                        uint32_t tmem_cols) {
+  using namespace ptx;
+  static_assert(IN == kInF16 || IN == kInBF16, "16-bit operands");
+  static_assert(FORM == 1 || FORM == 2, "probe form");
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ uint32_t tslot;
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t img = (raw + 1023u) & ~1023u;
+  const uint8_t* gimg = smem_raw + (img - raw);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int q = warp & 3;
+  const int row = q * 32 + lane;
+  const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
+  if (warp == 0) {
+    tmem_alloc(smem_u32(&tslot), tmem_cols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = tslot;
+  if (warp < 4) {
+    for (int c0 = 0; c0 < width; c0 += 32) {
+      uint32_t v[32];
+#pragma unroll
+      for (int i = 0; i < 32; ++i) v[i] = acc[row * width + c0 + i];
+      const uint32_t col = FORM == 2 ? tmem_col(r0, c0) : static_cast<uint32_t>(c0);
+      tmem_st32(tbase + lane_off + col, v);
+    }
+    tmem_wait_st();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if constexpr (FORM == 1) {
+    if (warp < 4) {
+      rearrange_accumulator_tmem16<IN>(tbase + lane_off, width);
+      for (int c0 = 0; c0 < width / 2; c0 += 32) {
+        uint32_t v[32];
+        tmem_ld32(tbase + lane_off + static_cast<uint32_t>(c0), v);
+        tmem_wait_ld();
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+          if (c0 + i < width / 2) out[row * (width / 2) + c0 + i] = v[i];
+      }
+    }
+  } else {
+    const int h = warp >> 2;
+    for (int ch = 0; ch < width / 128; ++ch) convert_chunk_half<IN>(tbase, lane_off, r0, ch, h, row, img);
+    __syncthreads();
+    const int words = width * 256 / 4;
+    const uint32_t* src = reinterpret_cast<const uint32_t*>(gimg);
+    for (int i = threadIdx.x; i < words; i += blockDim.x) out[i] = src[i];
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 0) tmem_dealloc(tbase, tmem_cols);
 }
 
 }  // namespace b2b

@@ -170,7 +170,10 @@ b2b_status_t b2b_plan_destroy(b2b_plan_t plan);
 b2b_status_t b2b_plan_device_status(b2b_plan_t plan, b2b_stream_t stream);
 
 /* Time budget of every bounded wait inside the kernels of this plan, in
- * nanoseconds (default 2e9).  0 restores the default. */
+ * nanoseconds (default 2e9).  0 restores the default; budgets below 1e6
+ * (1 ms) are raised to 1 ms, because after a wait runs out the same budget
+ * bounds the waits for the copies and MMAs still in flight, which must end
+ * before the kernel frees its tensor memory. */
 b2b_status_t b2b_plan_set_wait_budget(b2b_plan_t plan, uint64_t budget_ns);
 
 /*
@@ -232,6 +235,31 @@ b2b_status_t b2b_coordination_matrix(int n, int m, const int* src_thread, const 
  */
 b2b_status_t b2b_probe_operand_image(b2b_dtype_t dtype, int width, const void* acc, void* image,
                                      b2b_stream_t stream);
+
+/*
+ * Layout probes of the other forms of the 16-bit rearrangement (test
+ * support).  acc[128][width] (device, fp32 bit patterns) is put into tensor
+ * memory in the accumulator layout and rearranged by the same device code
+ * the fused kernels run; the result is copied to `out` (device):
+ *   B2B_PROBE_TMEM16: the intermediate kept in tensor memory as the A
+ *     operand of the next GEMM (two-stage 16-bit chains with resident
+ *     weights): packed in place, two K elements per 32-bit column; out is
+ *     [128][width / 2] 32-bit words, row (= TMEM lane) major.  width is 64,
+ *     128 or 256; region must be 0.
+ *   B2B_PROBE_PAIR_CONVERTERS: the converters of the CTA-pair kernel (eight
+ *     warps, two per TMEM lane quadrant, each taking 64 of every 128
+ *     columns), the accumulator starting in tensor-memory region `region`
+ *     (0 or 1, of 256 columns each; a wider one continues in the other);
+ *     out is the K-major 128-byte-swizzled shared-memory image,
+ *     width * 256 bytes.  width is 128, 256, 384 or 512.
+ * dtype is a 16-bit type (B2B_F16*, B2B_BF16*); other dtypes give
+ * B2B_ERR_UNSUPPORTED, bad forms, widths or regions B2B_ERR_INVALID_ARG.
+ * Synchronous.
+ */
+#define B2B_PROBE_TMEM16 1
+#define B2B_PROBE_PAIR_CONVERTERS 2
+b2b_status_t b2b_probe_operand_layout(b2b_dtype_t dtype, int form, int width, int region, const void* acc,
+                                      void* out, b2b_stream_t stream);
 
 /*
  * Register probe of the fp64 rearrangement (test support).  One warp loads

@@ -176,3 +176,16 @@ def sw128_inverse(rows: int, cols: int, elem_bytes: int) -> Dict[int, Coord]:
                 raise ValueError("not a bijection")
             inv[off] = (r, k)
     return inv
+
+
+def tmem_operand16(row: int, k: int) -> Tuple[int, int, int]:
+    """Where element (row, k) of a 16-bit A operand sits in tensor memory.
+
+    A tcgen05.mma of kind::f16 whose A operand (M = 128 rows, one CTA) comes
+    from tensor memory reads row m from lane m, and two consecutive K elements
+    from each 32-bit column: K elements 2c and 2c + 1 share column c, the even
+    one in the low 16 bits.  Returns (lane, column, half), half 0 = bits 0-15.
+    """
+    if not (0 <= row < 128) or k < 0:
+        raise IndexError((row, k))
+    return (row, k // 2, k % 2)

@@ -1,8 +1,18 @@
 """A model whose GEMM cascades were found and fused on its fx graph runs them
-through the fused kernels and gives the unfused model's result (needs a GB300)."""
+through the fused kernels (needs a GB300).
+
+The fused model is checked element by element against the CPU oracle applied
+to the same pieces (each fused cascade: fp32 accumulation, every intermediate
+and the output rounded to the activations' 16-bit type; the graph's other
+nodes, here a ReLU, applied exactly between them), and, as a second check,
+against the unfused model run by torch.
+"""
+import numpy as np
 import pytest
 import torch
 import torch.fx as fx
+
+import oracle
 
 pytestmark = pytest.mark.gpu
 
@@ -36,6 +46,22 @@ def rel(a, b):
     return float((a - b).abs().max() / b.abs().max())
 
 
+def rel_oracle(got, want: np.ndarray) -> float:
+    g = got.detach().double().cpu().numpy()
+    return float(np.max(np.abs(g - want)) / max(np.max(np.abs(want)), 1e-300))
+
+
+def oracle_chain(x: torch.Tensor, weights, dtype) -> np.ndarray:
+    """One fused cascade on the CPU oracle: rows of x (leading indices folded)
+    through the weights ([K_s, N_s], or [B, K_s, N_s] per batch)."""
+    mid = oracle.F16 if dtype == torch.float16 else oracle.BF16
+    a = oracle.widen(x)
+    if weights[0].dim() == 2:
+        a = a.reshape(1, -1, a.shape[-1])
+    out = oracle.chain(a, [oracle.widen(w) for w in weights], oracle.F32, mid, mid)
+    return out.reshape(*x.shape[:-1], out.shape[-1])
+
+
 @pytest.mark.parametrize("dtype", [torch.float16, torch.bfloat16])
 def test_fused_mlp_matches_the_unfused_model(dtype):
     torch.manual_seed(0)
@@ -49,6 +75,13 @@ def test_fused_mlp_matches_the_unfused_model(dtype):
     got = gm(x)
     torch.cuda.synchronize()
     assert got.shape == want.shape and got.dtype == dtype
+    # the oracle on the fused pieces: layers 0-2, ReLU (exact), layers 3-4
+    wt = [layer.weight.detach().t() for layer in model.layers]
+    h = oracle_chain(x, wt[:3], dtype)
+    h = torch.from_numpy(np.maximum(h, 0.0)).to(dtype)        # exact: h is already 16-bit
+    want_oracle = oracle_chain(h, wt[3:], dtype)
+    assert rel_oracle(got, want_oracle) <= 1e-2
+    # and the unfused model run by torch
     assert rel(got, want) <= 1e-2
     for name, mod in gm.named_modules():
         if isinstance(mod, fusion.FusedGemmChain):
@@ -72,6 +105,7 @@ def test_batched_matmul_chain():
     assert n == 1
     got = gm(x, *ws)
     torch.cuda.synchronize()
+    assert rel_oracle(got, oracle_chain(x, ws, torch.float16)) <= 1e-2
     assert rel(got, want) <= 1e-2
 
 

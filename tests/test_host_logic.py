@@ -87,3 +87,18 @@ def test_end_to_end_chunk_count_follows_the_size():
     assert len(_chunks(64, 4096, None, nbytes=138 << 20)) == 4
     assert len(_chunks(64, 4096, None, nbytes=34 << 20)) == 2
     assert len(_chunks(64, 4096, None, nbytes=1 << 20)) == 1
+
+
+def test_compact_per_config_records_stay_short():
+    """The headline line ends with one short record per workload, so that the
+    last 1.5 KB of the output hold all nine."""
+    import json
+    w = wl.ALL_WORKLOADS["three_stage_bf16"]
+    peaks = {"hbm_gbs": 6683.5, "tensor": {"bf16": 1920.8}}
+    entry = {"workload": "three_stage_bf16", "fused_ms": 0.041312345, "unfused_torch_ms": 0.0449876,
+             "unfused_own_ms": None, "speedup_vs_best_unfused": 1.08912345, "fused_tflops": 1039.9876,
+             "roofline": bench.roofline_for(w, 0.041312345, peaks), "cpu_oracle": {"value": 0.0241234567}}
+    c = bench.compact_config(entry)
+    assert c["fused_us"] == 41.3 and c["own_us"] is None and c["speedup"] == 1.09
+    assert c["bound"] == "tensor" and c["frac"] == round(c["frac"], 3)
+    assert len(json.dumps(c)) * len(wl.ALL_WORKLOADS) < 1500

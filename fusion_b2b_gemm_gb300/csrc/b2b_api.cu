@@ -175,7 +175,10 @@ struct b2b_plan_s {
   int* d_status;
   uint64_t budget_ns;
   uint32_t debug;
-  // tf32 only: the weights transposed to [N][K] before every run
+  // tf32 weights: read as stored (MN-major), or (w_kmajor, the
+  // allocation-free call only) transposed to [N][K] into d_wt before every
+  // run, which then launches two kernels
+  bool w_kmajor;
   void* d_wt;
   size_t wt_bytes;
   // resident weights: the tile schedule (host copy, then device copy)
@@ -262,10 +265,14 @@ b2b_status_t setup_chainn(b2b_plan_s* p) {
   c.off_bar = c.off_stg + static_cast<uint32_t>(c.nstg) * kPanelBytes;
   p->smem_bytes = static_cast<int>(c.off_bar + kBarBytes + 1024);
   if (p->smem_bytes > kSmemOptin) return B2B_ERR_UNSUPPORTED;
-  // a weight whose width is a multiple of 64 is read in 4-D boxes
+  // a weight whose width is a multiple of its 128-byte block (64 16-bit or
+  // 32 tf32 columns) is read in 4-D boxes (tf32 weights as stored only)
+  c.w_kmajor = p->w_kmajor ? 1 : 0;
   c.w_merged = 0;
-  for (int s = p->tf0 ? 1 : 0; s < S && !pt; ++s)
-    if (p->N[s] % 64 == 0) c.w_merged |= 1 << s;
+  for (int s = 0; s < S; ++s) {
+    const bool t32 = pt || (p->tf0 && s == 0);
+    if (t32 ? (!p->w_kmajor && p->N[s] % 32 == 0) : p->N[s] % 64 == 0) c.w_merged |= 1 << s;
+  }
   const ChainNEntry* e = find_chainn_kernel(p->in_kind, p->out_kind, p->nf, p->tf0 || pt);
   if (!e) return B2B_ERR_UNSUPPORTED;
   p->fn = e->fn;
@@ -427,10 +434,13 @@ b2b_status_t setup_chain_tc(b2b_plan_s* p) {
   p->res = L.res;
   c.dbl_p = L.dbl ? 1 : 0;
   c.p_tmem = p_tmem16 ? 1 : 0;
+  c.w_kmajor = p->w_kmajor ? 1 : 0;
   c.w_merged = 0;
-  if (p->in_kind != kInTF32)
+  // 4-D boxes for widths that are a multiple of the 128-byte block (64
+  // 16-bit or 32 tf32 columns); transposed tf32 weights are plain 3-D
+  if (!p->w_kmajor)
     for (int s = 0; s < S; ++s)
-      if (p->N[s] % 64 == 0) c.w_merged |= 1 << s;
+      if (p->N[s] % (128 / p->esz) == 0) c.w_merged |= 1 << s;
   c.p_bytes = p_bytes;
   c.nst = L.nst;
   c.nsta = L.nsta;
@@ -723,20 +733,6 @@ b2b_status_t create_common(b2b_plan_t* out, b2b_dtype_t dt, int stages, bool sin
       p->prm.sched = p->d_sched;
     }
   }
-  if (st == B2B_OK && (dt == B2B_TF32 || p->tf0) && p->kind != kPlanEmpty) {
-    // workspace for the weights transposed to [N][K] (tf32: every weight;
-    // mixed: the first)
-    int64_t words = 0, kin = K;
-    for (int s = 0; s < (p->tf0 ? 1 : stages); ++s) {
-      words += batch * kin * N[s];
-      kin = N[s];
-    }
-    p->wt_bytes = static_cast<size_t>(words) * 4;
-    if (cudaMalloc(&p->d_wt, p->wt_bytes) != cudaSuccess) {
-      cudaGetLastError();
-      st = B2B_ERR_CUDA;
-    }
-  }
   if (st != B2B_OK) {
     if (p->d_status) cudaFree(p->d_status);
     if (p->d_wt) cudaFree(p->d_wt);
@@ -750,7 +746,7 @@ b2b_status_t create_common(b2b_plan_t* out, b2b_dtype_t dt, int stages, bool sin
 
 b2b_status_t encode_3d(CUtensorMap* map, CUtensorMapDataType dt, int esz, const void* ptr,
                        int64_t inner, int64_t rows, int64_t batch, uint32_t box_inner,
-                       uint32_t box_rows) {
+                       uint32_t box_rows, CUtensorMapSwizzle swz = CU_TENSOR_MAP_SWIZZLE_128B) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return B2B_ERR_CUDA;
   const cuuint64_t dims[3] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(rows),
@@ -760,30 +756,46 @@ b2b_status_t encode_3d(CUtensorMap* map, CUtensorMapDataType dt, int esz, const 
   const cuuint32_t box[3] = {box_inner, box_rows, 1};
   const cuuint32_t estr[3] = {1, 1, 1};
   const CUresult r = fn(map, dt, 3, const_cast<void*>(ptr), dims, strides, box, estr,
-                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? B2B_OK : B2B_ERR_CUDA;
 }
 
-// Weight W[b][K][N] (N a multiple of 64) seen as a 4-D tensor
-// (64 columns, K rows, N/64 column blocks, batch): one box of
-// (64, k_rows, blocks, 1) covers k_rows rows of `blocks` adjacent 64-column
-// blocks, and lands in shared memory as `blocks` consecutive 128-byte-wide
-// swizzled panels.
+// Weight W[b][K][N] (N a multiple of the block width `blk`, whose row is
+// 128 bytes: 64 16-bit or 32 fp32 columns) seen as a 4-D tensor (blk
+// columns, K rows, N/blk column blocks, batch): one box of (blk, k_rows,
+// blocks, 1) covers k_rows rows of `blocks` adjacent column blocks, and
+// lands in shared memory as `blocks` consecutive 128-byte-wide swizzled
+// blocks of k_rows rows each.
 b2b_status_t encode_w4d(CUtensorMap* map, CUtensorMapDataType dt, int esz, const void* ptr,
-                        int64_t n, int64_t k, int64_t batch, uint32_t k_rows, uint32_t blocks) {
+                        int64_t n, int64_t k, int64_t batch, uint32_t k_rows, uint32_t blocks,
+                        CUtensorMapSwizzle swz = CU_TENSOR_MAP_SWIZZLE_128B) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return B2B_ERR_CUDA;
-  const cuuint64_t dims[4] = {64, static_cast<cuuint64_t>(k), static_cast<cuuint64_t>(n / 64),
-                              static_cast<cuuint64_t>(batch)};
-  const cuuint64_t strides[3] = {static_cast<cuuint64_t>(n * esz), static_cast<cuuint64_t>(64 * esz),
+  const int64_t blk = 128 / esz;
+  const cuuint64_t dims[4] = {static_cast<cuuint64_t>(blk), static_cast<cuuint64_t>(k),
+                              static_cast<cuuint64_t>(n / blk), static_cast<cuuint64_t>(batch)};
+  const cuuint64_t strides[3] = {static_cast<cuuint64_t>(n * esz), static_cast<cuuint64_t>(blk * esz),
                                  static_cast<cuuint64_t>(n * k * esz)};
-  const cuuint32_t box[4] = {64, k_rows, blocks, 1};
+  const cuuint32_t box[4] = {static_cast<cuuint32_t>(blk), k_rows, blocks, 1};
   const cuuint32_t estr[4] = {1, 1, 1, 1};
   const CUresult r = fn(map, dt, 4, const_cast<void*>(ptr), dims, strides, box, estr,
-                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? B2B_OK : B2B_ERR_CUDA;
+}
+
+// A tf32 weight W[b][K][N] as stored, for an MN-major B operand: blocks of
+// 32 columns (128 bytes) by k_rows rows, swizzled in 32-byte atoms (the
+// form the tf32 MMA reads MN-major); one 4-D box of `blocks` blocks when
+// `merged` (N a multiple of 32), else 3-D boxes of one block each.
+b2b_status_t encode_w_mn32(CUtensorMap* map, const void* ptr, int64_t n, int64_t k, int64_t batch,
+                           uint32_t k_rows, uint32_t blocks, bool merged) {
+  if (merged)
+    return encode_w4d(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, ptr, n, k, batch, k_rows, blocks,
+                      CU_TENSOR_MAP_SWIZZLE_128B_ATOM_32B);
+  return encode_3d(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, ptr, n, k, batch, 32, k_rows,
+                   CU_TENSOR_MAP_SWIZZLE_128B_ATOM_32B);
 }
 
 // Launch with programmatic stream serialization: the kernel may start while
@@ -830,7 +842,7 @@ b2b_status_t encode_chain_maps(b2b_plan_s* p, const void* const* W, const void* 
   b2b_status_t st = p->tf0 ? encode_3d(&maps->a, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, A, p->K, p->M, p->batch, 32, 128)
                            : encode_3d(&maps->a, in_dt, p->esz, A, p->K, p->M, p->batch, CK, 128);
   int64_t kin = p->K;
-  if (p->in_kind == kInTF32) {
+  if (p->in_kind == kInTF32 && p->w_kmajor) {
     // the weights as transposed into the workspace ([N][K] per batch)
     const uint32_t* dst = static_cast<const uint32_t*>(p->d_wt);
     for (int s = 0; s < S && st == B2B_OK; ++s) {
@@ -843,16 +855,14 @@ b2b_status_t encode_chain_maps(b2b_plan_s* p, const void* const* W, const void* 
       kin = p->N[s];
     }
   } else if (p->sn) {
-    if (p->tf0 && st == B2B_OK) {
-      // mixed: W0 as transposed into the workspace ([N1][K] per batch),
-      // boxes of this CTA's rows of a pass
-      st = encode_3d(&maps->w[0], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, p->d_wt, p->K, p->N[0], p->batch, 32,
-                     static_cast<uint32_t>(p->pn.pw[0] / 2));
-      kin = p->N[0];
-    }
-    // CTA pairs: each CTA loads half of a pass's 64-column blocks
-    for (int s = p->tf0 ? 1 : 0; s < S && st == B2B_OK; ++s) {
-      if ((p->pn.w_merged >> s) & 1) {
+    // CTA pairs: each CTA loads half of a pass's column blocks
+    for (int s = 0; s < S && st == B2B_OK; ++s) {
+      const bool merged = (p->pn.w_merged >> s) & 1;
+      if (p->in_kind == kInTF32 || (p->tf0 && s == 0)) {
+        // a tf32 weight as stored: 32 K rows of this CTA's half of a pass
+        const uint32_t wcols = static_cast<uint32_t>(p->pn.pw[s] / 2);
+        st = encode_w_mn32(&maps->w[s], W[s], p->N[s], kin, p->batch, 32, wcols / 32, merged);
+      } else if (merged) {
         // a box of this CTA's column blocks of a pass, over one K panel, or
         // two for 128-column passes after the first GEMM
         const uint32_t kps = (s > 0 && p->pn.pw[s] == 128) ? 2u : 1u;
@@ -865,10 +875,14 @@ b2b_status_t encode_chain_maps(b2b_plan_s* p, const void* const* W, const void* 
     }
   } else {
     for (int s = 0; s < S && st == B2B_OK; ++s) {
-      if ((p->prm.w_merged >> s) & 1) {
-        // 4-D view [batch][N/64][K][64]: a whole K panel of every 64-column
-        // block in one box, laid out in shared memory block after block
-        const int64_t width = s < S - 1 ? (s == 0 ? p->n1p : p->n2p) : p->nf;
+      const bool merged = (p->prm.w_merged >> s) & 1;
+      // a whole K panel of every 128-byte column block of the stage's width
+      // in one box when merged, laid out in shared memory block after block
+      const int64_t width = s < S - 1 ? (s == 0 ? p->n1p : p->n2p) : p->nf;
+      if (p->in_kind == kInTF32) {
+        st = encode_w_mn32(&maps->w[s], W[s], p->N[s], kin, p->batch, CK, static_cast<uint32_t>(width / 32),
+                           merged);
+      } else if (merged) {
         st = encode_w4d(&maps->w[s], in_dt, p->esz, W[s], p->N[s], kin, p->batch, CK,
                         static_cast<uint32_t>(width / 64));
       } else {
@@ -887,13 +901,13 @@ b2b_status_t encode_chain_maps(b2b_plan_s* p, const void* const* W, const void* 
 b2b_status_t run_chain_tc(b2b_plan_s* p, const void* const* W, const void* A, void* D,
                           cudaStream_t stream) {
   const int S = p->stages;
-  if (p->in_kind == kInTF32 || p->tf0) {
-    // The tf32 MMA reads B K-major: transpose every tf32 weight to [N][K]
-    // first (mixed cascades: W0 only).
+  if (p->w_kmajor) {
+    // K-major tf32 weights (the allocation-free call): transpose every
+    // weight to [N][K] into the workspace first.
     TransposeJob job;
     std::memset(&job, 0, sizeof(job));
     job.batch = static_cast<int>(p->batch);
-    job.count = p->tf0 ? 1 : S;
+    job.count = S;
     uint32_t* dst = static_cast<uint32_t*>(p->d_wt);
     int64_t kin = p->K;
     int max_r = 0, max_c = 0;
@@ -1105,7 +1119,7 @@ b2b_status_t b2b_plan_info(b2b_plan_t p, int* launches, int* grid, int* threads,
                            int* tmem_cols, int* ring_stages, int* passes) {
   if (!p) return B2B_ERR_INVALID_ARG;
   const bool tc = p->kind == kPlanChainTC || p->kind == kPlanGemmTC;
-  if (launches) *launches = p->kind == kPlanEmpty ? 0 : (p->d_wt ? 2 : 1);
+  if (launches) *launches = p->kind == kPlanEmpty ? 0 : (p->w_kmajor ? 2 : 1);
   if (grid) *grid = p->grid;
   if (threads) *threads = p->threads;
   if (smem) *smem = p->smem_bytes;
@@ -1231,9 +1245,10 @@ b2b_status_t b2b_probe_f64_rearrange(int tiles, const double* cfrag, double* afr
 // cudaMalloc would stall or fail (inside a memory-pool-managed framework that
 // forbids untracked allocations, or after the device memory has been handed
 // out up front), or callers that must not create the plan objects that own
-// device memory.  This entry point needs no plan: the scratch space of the
-// tf32 chain (its weights transposed to [N][K]) is a fixed array in device
-// memory that belongs to the library itself.
+// device memory.  This entry point needs no plan: it runs the tf32 chain in
+// the form that reads its weights transposed to [N][K] (a plan reads them as
+// stored), and the scratch space of that form, the transposed weights, is a
+// fixed array in device memory that belongs to the library itself.
 //
 // The array is `kNoAllocScratchWords` 32-bit words (4 MiB) on every GPU that
 // loads the library, held until the process exits.  Its device address is
@@ -1349,6 +1364,7 @@ extern "C" b2b_status_t b2b_run_tf32_noalloc(int64_t batch, int64_t M, int64_t K
   pl.budget_ns = kDefaultBudgetNs;
   pl.debug = 0;
   pl.tf0 = false;
+  pl.w_kmajor = true;  // weights transposed into the library's scratch array
   pl.d_status = nullptr;
   pl.d_wt = nullptr;
   pl.d_sched = nullptr;

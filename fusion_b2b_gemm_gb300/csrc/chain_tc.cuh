@@ -91,8 +91,10 @@ struct ChainParams {
   int dbl_p;          // two operand buffers for the intermediate (tile parity), own barriers
   uint32_t p_bytes;   // bytes of one shared-memory operand image (0: kept in tensor memory)
   int p_tmem;         // 16-bit intermediate kept in tensor memory (tf32 always is)
-  int w_merged;       // bit s: weight s is mapped 4-D (64 cols, K, col blocks, batch), so a
-                      // whole panel (all its 64-column boxes) arrives as one TMA box
+  int w_merged;       // bit s: weight s is mapped 4-D (128-byte column blocks, K, blocks,
+                      // batch), so a whole panel (all its column blocks) arrives as one TMA box
+  int w_kmajor;       // tf32 only: the weights arrive transposed ([N][K], K-major) instead of
+                      // as stored ([K][N], MN-major with 32-byte swizzle atoms)
   uint32_t debug;     // test support: bit 0 = arm the first ring stage but never fill it
   int* status;
   unsigned long long budget_ns;
@@ -339,10 +341,12 @@ __global__ void __launch_bounds__(kChainThreads, 1)
   constexpr int WBOX_BYTES = CK * 128;
   constexpr int OBOX_N = 128 / OSZ;   // output columns per TMA store box
   constexpr bool P_TMEM = TF32;
-  // tf32 weights arrive transposed ([N][K], K-major): the tf32 MMA takes its
-  // B operand K-major only.  16-bit weights are read as stored ([K][N],
-  // MN-major B operand).
-  constexpr bool W_KMAJOR = TF32;
+  // Weights are read as stored ([K][N]: an MN-major B operand), in blocks of
+  // 128 bytes of N (64 16-bit or 32 tf32 columns) by K rows.  16-bit blocks
+  // use the 128-byte swizzle; tf32 blocks the 128-byte swizzle of 32-byte
+  // atoms, the only MN-major form the tf32 MMA reads.  With w_kmajor (tf32
+  // only) the weights arrive transposed instead ([N][K], K-major).
+  const bool W_KMAJOR = TF32 && p.w_kmajor != 0;
   // With resident weights (16-bit), GEMM1 and GEMM2 are issued by two
   // threads (warps 1 and 10): the tensor pipe holds little more than the MMA
   // being executed, so every wait of a single issuing thread would leave it
@@ -553,10 +557,19 @@ __global__ void __launch_bounds__(kChainThreads, 1)
                               : (split_a ? base + p.off_aring + astage * static_cast<uint32_t>(kPanelBytes) : sbase);
       const uint32_t b_base = RES ? base + wres + static_cast<uint32_t>(kb) * 128u * width
                                   : sbase + (split_a || s != 0 ? 0u : static_cast<uint32_t>(kPanelBytes));
-      auto bdesc = [&](int kk) -> uint64_t {
-        return W_KMAJOR ? desc_sw128(b_base + kk * 32u, 16u, 1024u)
-                        : desc_sw128(b_base + kk * KSTEP * 128u, WBOX_BYTES, 1024u);
-      };
+      // B descriptor of the panel's first K step and its increment per step
+      // (the start address field counts 16-byte units; a K step moves
+      // KSTEP rows of 128 bytes, or 32 bytes along a K-major row)
+      uint64_t bd0;
+      uint32_t bstep;
+      if constexpr (TF32) {
+        bd0 = W_KMAJOR ? desc_sw128(b_base, 16u, 1024u) : desc_mn32(b_base, WBOX_BYTES, 512u);
+        bstep = W_KMAJOR ? 2u : (KSTEP * 128u) >> 4;
+      } else {
+        bd0 = desc_sw128(b_base, WBOX_BYTES, 1024u);
+        bstep = (KSTEP * 128u) >> 4;
+      }
+      auto bdesc = [&](int kk) -> uint64_t { return bd0 + static_cast<uint64_t>(kk) * bstep; };
       const uint32_t acc0 = kb != 0 ? 1u : 0u;
       // The MMAs of one panel are issued back to back, with the choice of
       // operand source made once per panel: a branch between consecutive
@@ -620,7 +633,7 @@ __global__ void __launch_bounds__(kChainThreads, 1)
             mbar_arrive_expect_tx(bar(kBarWFull), bytes);
             for (int kb = 0; kb < p.kpan0; ++kb) {
               const uint32_t dst = base + p.off_wres0 + kb * 128u * N1P;
-              if constexpr (W_KMAJOR) {
+              if (W_KMAJOR) {
                 tma_load_3d(dst, &tmW0, bar(kBarWFull), kb * CK, 0, b);
               } else if (p.w_merged & 1) {
                 tma_load_4d(dst, &tmW0, bar(kBarWFull), 0, kb * CK, 0, b);
@@ -631,7 +644,7 @@ __global__ void __launch_bounds__(kChainThreads, 1)
             }
             for (int kb = 0; kb < N1P / CK; ++kb) {
               const uint32_t dst = base + p.off_wres1 + kb * 128u * NF;
-              if constexpr (W_KMAJOR) {
+              if (W_KMAJOR) {
                 tma_load_3d(dst, &tmW1, bar(kBarWFull), kb * CK, 0, b);
               } else if (p.w_merged & 2) {
                 tma_load_4d(dst, &tmW1, bar(kBarWFull), 0, kb * CK, 0, b);
@@ -671,7 +684,7 @@ __global__ void __launch_bounds__(kChainThreads, 1)
               tma_load_3d(dst + q * kPanelBytes, &tmA, fb, kb * CK, m0, b);
             } else {
               if (a_here) tma_load_3d(dst, &tmA, fb, kb * CK, m0, b);
-              if constexpr (W_KMAJOR) {
+              if (W_KMAJOR) {
                 // one box: `width` rows of the transposed weight, 128 bytes of K
                 tma_load_3d(dst + wofs, wm, fb, kb * CK, n0, b);
               } else if ((p.w_merged >> s) & 1) {

@@ -91,6 +91,8 @@ struct ChainNParams {
   uint32_t off_ring, off_p, off_stg, off_bar;
   int w_merged;              // bit s: weight s is read as one 4-D box per half panel
   int split;                 // leftover tiles whose passes are split between two clusters
+  int w_kmajor;              // tf32 weights arrive transposed ([N][K], K-major) instead of as
+                             // stored ([K][N], MN-major with 32-byte swizzle atoms)
   uint32_t debug;            // test support: bit 0 = the first ring slot is never filled
   int* status;
   unsigned long long budget_ns;
@@ -173,18 +175,19 @@ __device__ __forceinline__ void convert_chunk_half(uint32_t tmem_base, uint32_t 
                             p_img + static_cast<uint32_t>(pcol / 64) * kPanelBytes);
 }
 
-// TF0: the first GEMM takes fp32 A and W0 as tf32 operands (W0 transposed to
-// [N][K], K-major, which the tf32 MMA reads), and its result is rounded to
+// TF0: the first GEMM takes fp32 A and W0 as tf32 operands (W0 read as
+// stored, an MN-major B operand in 128-byte rows swizzled in 32-byte atoms,
+// or, with w_kmajor, transposed to [N][K]), and its result is rounded to
 // the 16-bit type IN of every later GEMM: a mixed-type cascade, where the
 // accumulator and operand layouts of the first hand-over differ in element
 // size as well as in order.
 //
 // IN = tf32 (with TF0): a two-GEMM tf32 chain.  The intermediate (at most
 // 256 columns) is rounded to tf32 in place in tensor memory, one K element
-// per 32-bit column, and the second GEMM (one pass, its weight transposed
-// like W0) reads it from there as its A operand, so no operand image is
-// kept.  The next GEMM to write that region is the next unit's first GEMM,
-// which the tensor pipe runs after every MMA that reads it.
+// per 32-bit column, and the second GEMM (one pass, its weight read like
+// W0) reads it from there as its A operand, so no operand image is kept.
+// The next GEMM to write that region is the next unit's first GEMM, which
+// the tensor pipe runs after every MMA that reads it.
 template <int IN, int OUT, int NF, bool TF0 = false>
 __global__ void __launch_bounds__(kChainNThreads, 1)
     chainn_kernel(const __grid_constant__ ChainNMaps maps, const __grid_constant__ ChainNParams p) {
@@ -217,6 +220,7 @@ __global__ void __launch_bounds__(kChainNThreads, 1)
   const uint32_t rank = cluster_ctarank();
   const bool leader = (rank == 0);
   const int S = p.S;
+  const bool wk = p.w_kmajor != 0;  // tf32 weights transposed (K-major)
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < 16; ++i) {
@@ -248,22 +252,23 @@ __global__ void __launch_bounds__(kChainNThreads, 1)
   // unit's A into L2.  A may be that kernel's output, but a prefetch touches
   // L2 only, where its writes land too, and every load into shared memory
   // comes after the wait, so no stale value is read.  At most four K panels
-  // (more only compete with that kernel's tail), all of them in a tf32 chain,
-  // whose weight transpose runs meanwhile.
+  // (more only compete with that kernel's tail).
   if (warp == 0 && lane == 0 && (blockIdx.x >> 1) < static_cast<unsigned>(p.total_tiles)) {
     const ChainNUnit c = chainn_unit(p, static_cast<int>(blockIdx.x >> 1), static_cast<int>(gridDim.x >> 1), 0);
     const int m0 = c.mt * 256 + static_cast<int>(rank) * 128;
-    const int npf = PT ? p.kpan[0] : (p.kpan[0] < 4 ? p.kpan[0] : 4);
+    const int npf = p.kpan[0] < 4 ? p.kpan[0] : 4;
     for (int q = 0; q < npf; ++q) tma_prefetch_l2_3d(&maps.a, q * CK0, m0, c.b);
-    // and this CTA's half of the first GEMM's first weight panels (16-bit
-    // weights; a tf32 weight is the transpose's output, not yet written)
-    if (!TF0) {
+    // and this CTA's half of the first GEMM's first weight panels (as
+    // stored; a transposed tf32 weight is the transpose kernel's output, not
+    // yet written)
+    if (!p.w_kmajor) {
       const int n0 = static_cast<int>(rank) * (p.pw[0] / 2);
+      const int blk = TF0 ? 32 : WBOX_N;  // columns per 128-byte block
       for (int q = 0; q < npf; ++q) {
         if (p.w_merged & 1)
-          tma_prefetch_l2_4d(&maps.w[0], 0, q * CK, n0 / WBOX_N, c.b);
+          tma_prefetch_l2_4d(&maps.w[0], 0, q * CK0, n0 / blk, c.b);
         else
-          for (int j = 0; j < p.pw[0] / 2 / WBOX_N; ++j) tma_prefetch_l2_3d(&maps.w[0], n0 + j * WBOX_N, q * CK, c.b);
+          for (int j = 0; j < p.pw[0] / 2 / blk; ++j) tma_prefetch_l2_3d(&maps.w[0], n0 + j * blk, q * CK0, c.b);
       }
     }
   }
@@ -319,9 +324,16 @@ __global__ void __launch_bounds__(kChainNThreads, 1)
           } else {
             const CUtensorMap* wm = &maps.w[s];
             const int n0 = col0 + static_cast<int>(rank) * wcols;
-            if ((TF0 && s == 0) || PT) {
+            if (((TF0 && s == 0) || PT) && p.w_kmajor) {
               // a tf32 weight transposed: this CTA's wcols rows of 32 K elements
               tma_load_3d_pair(dst, wm, fb, kb * CK0, n0, b);
+            } else if ((TF0 && s == 0) || PT) {
+              // a tf32 weight as stored: 32 K rows of this CTA's wcols columns,
+              // in blocks of 32 columns (4 KB each)
+              if ((p.w_merged >> s) & 1)
+                tma_load_4d_pair(dst, wm, fb, 0, kb * CK0, n0 / 32, b);
+              else
+                for (int j = 0; j < wcols / 32; ++j) tma_load_3d_pair(dst + j * 4096u, wm, fb, n0 + j * 32, kb * CK0, b);
             } else if ((p.w_merged >> s) & 1) {
               // one box of npan * 64 K rows and wcols / 64 column blocks
               tma_load_4d_pair(dst, wm, fb, 0, kb * CK, n0 / WBOX_N, b);
@@ -449,19 +461,22 @@ __global__ void __launch_bounds__(kChainNThreads, 1)
         const uint32_t acc0 = kb != 0 ? 1u : 0u;
         // (straight-line MMAs: a branch between two of them costs more than
         // the tensor pipe's queue hides)
+        // a tf32 weight: 8 K elements per MMA, B as stored (MN-major, 32-column
+        // blocks of 4 KB, 32-byte swizzle atoms: a K step is 8 rows of 128
+        // bytes) or transposed (K-major: a K step is 32 bytes along a row)
+        const uint64_t tb0 = wk ? desc_sw128(wb, 16u, 1024u) : desc_mn32(wb, 4096u, 512u);
+        const uint32_t tbs = wk ? 2u : 64u;
         if constexpr (a_smem && TF0) {
-          // tf32: 8 K elements (32 bytes) per MMA, B K-major like A
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
-            mma_ss<true, CG>(d, desc_sw128(sa + kk * 32u, 16u, 1024u), desc_sw128(wb + kk * 32u, 16u, 1024u), idesc,
-                             kk ? 1u : acc0);
+            mma_ss<true, CG>(d, desc_sw128(sa + kk * 32u, 16u, 1024u), tb0 + kk * tbs, idesc, kk ? 1u : acc0);
         } else if constexpr (PT) {
           // tf32 intermediate in tensor memory: K panel kb is its columns
-          // [32 kb, 32 kb + 32), 8 per MMA; B K-major as in the first GEMM
+          // [32 kb, 32 kb + 32), 8 per MMA
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
-            mma_ts<true, CG>(d, p_tmem + static_cast<uint32_t>(kb * 32 + kk * 8), desc_sw128(wb + kk * 32u, 16u, 1024u),
-                             idesc, kk ? 1u : acc0);
+            mma_ts<true, CG>(d, p_tmem + static_cast<uint32_t>(kb * 32 + kk * 8), tb0 + kk * tbs, idesc,
+                             kk ? 1u : acc0);
         } else if constexpr (npan == 2) {
 #pragma unroll
           for (int kk = 0; kk < 2 * (CK / KSTEP); ++kk) {
@@ -508,7 +523,7 @@ __global__ void __launch_bounds__(kChainNThreads, 1)
         for (int s = 0; s < S - 1 && ok; ++s) {
           const int pw = p.pw[s];
           const uint32_t r0 = rc.take(p.wpad[s]);
-          const uint32_t idesc = ((TF0 && s == 0) || PT) ? make_idesc(2u, static_cast<uint32_t>(pw), 256u, false)
+          const uint32_t idesc = ((TF0 && s == 0) || PT) ? make_idesc(2u, static_cast<uint32_t>(pw), 256u, !wk)
                                                          : make_idesc(FMT, static_cast<uint32_t>(pw), 256u, true);
           const uint32_t cpar = ((k - 1u) >> 1) & 1u;
           int touched = 0;
@@ -539,7 +554,7 @@ __global__ void __launch_bounds__(kChainNThreads, 1)
         }
         if (!ok) break;
         // the unit's passes of the last GEMM, each in the next region
-        const uint32_t idesc = make_idesc(FMT, NF, 256u, !PT);
+        const uint32_t idesc = make_idesc(FMT, NF, 256u, !(PT && wk));
         const uint32_t cpar = ((k - 1u) >> 1) & 1u;
         for (int j = c.p0; j < c.p1 && ok; ++j) {
           const int r = static_cast<int>(rc.take(NF));

@@ -388,6 +388,20 @@ __device__ __forceinline__ uint64_t desc_sw128(uint32_t saddr, uint32_t lbo, uin
          (static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (2ull << 61);
 }
 
+// Shared-memory matrix descriptor (tcgen05) of an MN-major operand of 32-bit
+// elements (tf32) as the TMA writes it with CU_TENSOR_MAP_SWIZZLE_128B_ATOM_32B:
+// 128-byte rows (32 MN elements, one K index per row) whose 32-byte atoms are
+// permuted, the pattern repeating every four rows; layout field 1 (128-byte
+// swizzle with 32-byte atoms).  lbo = byte stride between 32-element MN
+// blocks, sbo = byte stride between groups of four K rows (512 for dense
+// rows).  Measured on the GB300: with these an MN-major tf32 B operand gives
+// exact products, while the plain 128-byte swizzle (field 2) gives zeros.
+__device__ __forceinline__ uint64_t desc_mn32(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  return static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4) |
+         (static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16) |
+         (static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (1ull << 61);
+}
+
 // Instruction descriptor for kind::f16 / kind::tf32 with an fp32 accumulator:
 // bits 4-5 D format (1 = f32), 7-9 A format, 10-12 B format (0 f16, 1 bf16,
 // 2 tf32), 15 A major (0 = K), 16 B major (1 = MN), 17-22 N>>3, 24-28 M>>4.

@@ -1,10 +1,10 @@
 // Batched 2-D transpose of 32-bit words: out[b][c][r] = in[b][r][c].
 //
-// The tf32 tensor-core MMA reads its B operand K-major only (an MN-major
-// tf32 B descriptor yields zeros on sm_103a), while the weights of a chain
-// are stored row-major [K][N].  Before a tf32 chain runs, its weights are
-// turned into [N][K] in a plan-owned workspace by this kernel.  Two matrices
-// per launch (blockIdx.z = matrix * batch + b); 32x32 tiles through shared
+// The tf32 chain kernels read their weights either as stored ([K][N], an
+// MN-major B operand; what plans do) or transposed ([N][K], K-major).  The
+// allocation-free tf32 call takes the second form: this kernel turns the
+// weights into [N][K] in the library's scratch array first.  Two matrices per
+// launch (blockIdx.z = matrix * batch + b); 32x32 tiles through shared
 // memory so that reads and writes are both coalesced.
 #pragma once
 
@@ -37,8 +37,8 @@ __global__ void __launch_bounds__(256) transpose32_kernel(const __grid_constant_
   // wait).
   if (active && threadIdx.x < 32 && r0 + static_cast<int>(threadIdx.x) < R)
     ptx::prefetch_l2(in + static_cast<size_t>(r0 + threadIdx.x) * C + c0);
-  // Wait for the earlier kernels (the previous chain kernel reads the
-  // workspace written below), then let the chain kernel start.
+  // Wait for the earlier kernels (the previous chain kernel may read the
+  // array written below), then let the chain kernel start.
   ptx::grid_dependency_wait();
   ptx::grid_launch_dependents();
   if (!active) return;

@@ -94,15 +94,13 @@ typedef enum {
  *   B2B_TF32:     two stages; K % 4 == 0; N1 <= 256; N1, N2 % 4 == 0.
  *   B2B_TF32_F16, B2B_TF32_BF16: two or more stages; K % 4 == 0; every
  *                 width % 8 == 0; intermediate widths <= 512, the last
- *                 <= 4096.  A plan allocates a workspace for W[0] transposed
- *                 (batch * K * N1 * 4 bytes); a run launches two kernels.
+ *                 <= 4096.
  *   B2B_F64:      two stages; K % 4 == 0; N1, N2 in {16, 32, 64}.
  * Binds to the current CUDA device, which must be an sm_103 GPU
  * (B2B_ERR_DEVICE otherwise).  Allocates a 4-byte device status word; a
  * two-stage 16-bit plan whose weights stay resident over several batches
- * also a tile-schedule table (36 bytes per CTA, copied once); tf32 and
- * mixed plans also the workspace of their transposed weights.  No kernel is
- * launched.
+ * also a tile-schedule table (36 bytes per CTA, copied once).  Weights of
+ * every type are read as stored.  No kernel is launched.
  */
 b2b_status_t b2b_plan_create(b2b_plan_t* out, b2b_dtype_t dtype, int64_t batch, int64_t M,
                              int64_t K, int64_t N1, int64_t N2, int64_t N3);
@@ -280,12 +278,16 @@ b2b_status_t b2b_probe_f64_rearrange(int tiles, const double* cfrag, double* afr
  * plan objects, which own device memory).
  *   Sizes, layout and arguments as for a B2B_TF32 plan with N3 = 0; A, B, C
  *   and D are the caller's device buffers (fp32, row-major, 16-byte aligned).
- *   The tf32 weights are transposed into a fixed scratch array owned by the
- *   library: 4 MiB (2^20 32-bit words) on every GPU that loads the library,
- *   kept until the process exits.  batch * (K*N1 + N1*N2) must not exceed
- *   2^20, otherwise B2B_ERR_UNSUPPORTED.
- *   The first call on a device looks up the array's device address (make it
- *   before any stream capture).  All calls share the array; calls whose
+ *   It runs the kernels of a B2B_TF32 plan in their form that reads the
+ *   weights transposed ([N][K], K-major; a plan reads them as stored), and
+ *   the weights are first transposed by a second kernel into a fixed scratch
+ *   array owned by the library: 4 MiB (2^20 32-bit words) on every GPU that
+ *   loads the library, kept until the process exits.  batch * (K*N1 + N1*N2)
+ *   must not exceed 2^20, otherwise B2B_ERR_UNSUPPORTED.
+ *   The first call on a device (and the first after that device's context
+ *   has been replaced) looks up the array's device address and raises the
+ *   kernel's shared-memory limit: make it before any stream capture.  Later
+ *   calls make neither runtime call.  All calls share the array; calls whose
  *   kernels overlap on the GPU race on it.  Nothing in it must start at zero.
  *   No cudaMalloc or cudaFree is made.  Asynchronous on `stream`; a bounded
  *   wait that runs out inside the kernel is not reported (there is no status

@@ -440,27 +440,22 @@ __global__ void __launch_bounds__(kChainNThreads, 1)
           }
         }
       };
-      // Four MMAs per 128-byte K panel.  First GEMM (npan == 0): the A
-      // panel is in this slot and the weight half panel in the next; later
-      // GEMMs read K panels kb .. kb + npan - 1 of the operand image (their
-      // weight half panels share one slot), after waiting for the chunk
-      // barrier `chunk` (if >= 0) with parity cpar.
-      auto stage_mmas = [&](auto npan_c, uint32_t d, uint32_t idesc, int kb, int chunk, uint32_t cpar) -> bool {
+      auto next_slot = [&](uint32_t x) -> uint32_t {
+        return x + 1u == static_cast<uint32_t>(p.nslot) ? 0u : x + 1u;
+      };
+      // The MMAs of one K-panel group: four per 128-byte K panel.  First
+      // GEMM (npan == 0): the A panel in slot sa_slot, the weight half panel
+      // in slot w_slot; later GEMMs read K panels kb .. kb + npan - 1 of the
+      // operand image (their weight half panels share slot w_slot).
+      // (straight-line MMAs: a branch between two of them costs more than
+      // the tensor pipe's queue hides)
+      auto group_mmas = [&](auto npan_c, uint32_t d, uint32_t idesc, int kb, uint32_t sa_slot, uint32_t w_slot,
+                            uint32_t acc0) {
         constexpr int npan = decltype(npan_c)::value;
         constexpr bool a_smem = npan == 0;
-        const uint32_t need = a_smem ? 2u : 1u;
-        if (!stage_ready(need)) return false;
-        if (chunk >= 0 && !bwm.wait(bar(chunk), cpar)) return false;
-        consumed += need;
-        tc_fence_after();
-        const uint32_t s0 = slot;
-        const uint32_t s1 = a_smem ? (slot + 1u == static_cast<uint32_t>(p.nslot) ? 0u : slot + 1u) : slot;
-        const uint32_t wb = base + p.off_ring + s1 * static_cast<uint32_t>(kPanelBytes);
-        const uint32_t sa = a_smem ? base + p.off_ring + s0 * static_cast<uint32_t>(kPanelBytes)
+        const uint32_t wb = base + p.off_ring + w_slot * static_cast<uint32_t>(kPanelBytes);
+        const uint32_t sa = a_smem ? base + p.off_ring + sa_slot * static_cast<uint32_t>(kPanelBytes)
                                    : p_img + static_cast<uint32_t>(kb) * kPanelBytes;
-        const uint32_t acc0 = kb != 0 ? 1u : 0u;
-        // (straight-line MMAs: a branch between two of them costs more than
-        // the tensor pipe's queue hides)
         // a tf32 weight: 8 K elements per MMA, B as stored (MN-major, 32-column
         // blocks of 4 KB, 32-byte swizzle atoms: a K step is 8 rows of 128
         // bytes) or transposed (K-major: a K step is 32 bytes along a row)
@@ -491,9 +486,43 @@ __global__ void __launch_bounds__(kChainNThreads, 1)
             mma_ss<false, CG>(d, desc_sw128(sa + kk * 32u, 16u, 1024u),
                               desc_sw128(wb + kk * KSTEP * 128u, WBOX_BYTES, 1024u), idesc, kk ? 1u : acc0);
         }
-        tc_commit<CG>(bar(knEmpty + s0));
-        if (a_smem) tc_commit<CG>(bar(knEmpty + s1));
-        slot = s1 + 1u == static_cast<uint32_t>(p.nslot) ? 0u : s1 + 1u;
+      };
+      // One stage: one K-panel group, or (pair) two consecutive ones, whose
+      // slots are waited for and released together, so that the per-stage
+      // work of this thread (the readiness check, a chunk wait, the fence)
+      // is paid once per eight MMAs instead of four (measured: 1-2 % on the
+      // cascades; the tensor pipe queues only about two MMAs, so that work
+      // can show up as idle pipe time).  A chunk wait (chunk >= 0, parity
+      // cpar) is for the operand image chunk holding K panel kb (a pair
+      // never spans two chunks: it starts at an even panel).
+      auto stage_mmas = [&](auto npan_c, auto pair_c, uint32_t d, uint32_t idesc, int kb, int chunk,
+                            uint32_t cpar) -> bool {
+        constexpr int npan = decltype(npan_c)::value;
+        constexpr bool pair = decltype(pair_c)::value != 0;
+        constexpr bool a_smem = npan == 0;
+        constexpr uint32_t per = a_smem ? 2u : 1u;  // slots per K-panel group
+        constexpr uint32_t need = pair ? 2u * per : per;
+        if (!stage_ready(need)) return false;
+        if (chunk >= 0 && !bwm.wait(bar(chunk), cpar)) return false;
+        consumed += need;
+        tc_fence_after();
+        const uint32_t s0 = slot;
+        const uint32_t s1 = a_smem ? next_slot(s0) : s0;
+        group_mmas(npan_c, d, idesc, kb, s0, s1, kb != 0 ? 1u : 0u);
+        uint32_t last = s1;
+        if constexpr (pair) {
+          const uint32_t s2 = next_slot(s1);
+          const uint32_t s3 = a_smem ? next_slot(s2) : s2;
+          group_mmas(npan_c, d, idesc, kb + 1, s2, s3, 1u);
+          last = s3;
+        }
+        uint32_t x = s0;
+#pragma unroll
+        for (uint32_t q = 0; q < need; ++q) {
+          tc_commit<CG>(bar(knEmpty + x));
+          x = next_slot(x);
+        }
+        slot = next_slot(last);
         return true;
       };
       // the K panels of GEMM s > 0 from kb on need chunk kb / 2 (tf32:
@@ -508,11 +537,23 @@ __global__ void __launch_bounds__(kChainNThreads, 1)
       };
       // one pass: kpan K panels, npan of them per ring slot (0: the first
       // GEMM, one K panel and two slots)
+      // (after the first GEMM, one-panel groups go in pairs while two
+      // panels are left; a chunk wait falls on an even panel, so on the
+      // first of a pair.  The first GEMM, which waits on its loads, keeps
+      // single groups: a pair would hold back its MMAs until four slots
+      // have landed.)
       auto run_pass = [&](auto npan_c, uint32_t d, uint32_t idesc, int kpan, bool first, uint32_t cpar) -> bool {
         constexpr int npan = decltype(npan_c)::value;
         constexpr int step = npan == 0 ? 1 : npan;
-        for (int kb = 0; kb < kpan; kb += step)
-          if (!stage_mmas(npan_c, d, idesc, kb, npan == 0 ? -1 : chunk_of(first, kb), cpar)) return false;
+        using Single = integral_constant_int<0>;
+        using Pair = integral_constant_int<1>;
+        int kb = 0;
+        if constexpr (npan == 1) {
+          for (; kb + 1 < kpan; kb += 2)
+            if (!stage_mmas(npan_c, Pair{}, d, idesc, kb, npan == 0 ? -1 : chunk_of(first, kb), cpar)) return false;
+        }
+        for (; kb < kpan; kb += step)
+          if (!stage_mmas(npan_c, Single{}, d, idesc, kb, npan == 0 ? -1 : chunk_of(first, kb), cpar)) return false;
         return true;
       };
       using First = integral_constant_int<0>;

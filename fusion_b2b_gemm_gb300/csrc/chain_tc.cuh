@@ -372,42 +372,6 @@ __global__ void __launch_bounds__(kChainThreads, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
-  if (threadIdx.x == 0) {
-    for (int i = 0; i < 8; ++i) {
-      mbar_init(bar(kBarFull + i), 1);
-      mbar_init(bar(kBarEmpty + i), 1);
-      mbar_init(bar(kBarAFull + i), 1);
-      mbar_init(bar(kBarAEmpty + i), 1);
-    }
-    mbar_init(bar(kBarWFull), 1);
-    mbar_init(bar(kBarWEmpty), SPLIT ? 2 : 1);
-    for (int i = 0; i < 4; ++i) {
-      mbar_init(bar(kBarRFull + i), 1);
-      mbar_init(bar(kBarREmpty + i), 128);
-    }
-    mbar_init(bar(kBarCFull), 1);
-    mbar_init(bar(kBarCFull + 1), 1);
-    mbar_init(bar(kBarPFull), 128);
-    mbar_init(bar(kBarPEmpty), 1);
-    mbar_init(bar(kBarPFull1), 128);
-    mbar_init(bar(kBarPEmpty1), 1);
-    mbar_init(bar(kBarEpiSync), 128);
-    mbar_init(bar(kBarDrain), 1);
-    mbar_init(bar(kBarDrain2), 1);
-    *abort_flag = 0;
-    fence_barrier_init();
-  }
-  if (warp == 1) {
-    tmem_alloc(smem_u32(tmem_slot), p.tmem_cols);
-    tmem_relinquish();
-  }
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem_base = *tmem_slot;
-
-  BoundedWait bw{abort_flag, p.status, p.budget_ns, kTimeoutCode};
-
   // Tiles of this CTA: a contiguous range when the weights stay resident
   // (few batch changes), otherwise strided so that concurrent CTAs share the
   // same weights in L2.
@@ -443,12 +407,22 @@ __global__ void __launch_bounds__(kChainThreads, 1)
     first.init_segments(my_segs, my_nseg, p.m_tiles);
   else
     first.init(t_begin, t_step, p.m_tiles);
-  // Everything above may overlap the previous kernel in the stream: it reads
-  // only the plan's own tile schedule.  Before waiting for that kernel, pull
-  // this CTA's first A tile into L2.  A may be that kernel's output, but a
-  // prefetch touches L2 only, where its writes land too, and every load into
-  // shared memory comes after the wait, so no stale value is read.
-  if (warp == 0 && lane == 0 && t_count > 0) {
+  // Everything up to the dependency wait may overlap the previous kernel in
+  // the stream: it reads only the plan's own tile schedule.  Before waiting
+  // for that kernel, and while the other warps set up barriers and tensor
+  // memory, one thread pulls this CTA's first A tile into L2 (measured: the
+  // TMA prefetch instructions of a tile take about half a microsecond to
+  // issue).  A may be that kernel's output, but a prefetch touches L2 only,
+  // where its writes land too, and every load into shared memory comes after
+  // the wait, so no stale value is read.
+  if (warp == 3 && lane == 0) {
+    prefetch_tmap(&tmA);
+    prefetch_tmap(&tmW0);
+    if (S >= 2) prefetch_tmap(&tmW1);
+    if (S >= 3) prefetch_tmap(&tmW2);
+    prefetch_tmap(&tmOut);
+  }
+  if (warp == 3 && lane == 0 && t_count > 0) {
     for (int kb = 0; kb < p.kpan0; ++kb) tma_prefetch_l2_3d(&tmA, kb * CK, first.mt * 128, first.b);
     if constexpr (RES) {
       // the weights of the first batch, and the second tile's A
@@ -476,6 +450,46 @@ __global__ void __launch_bounds__(kChainThreads, 1)
       }
     }
   }
+  // Barriers, set up by the lanes of warp 0 in parallel (each lane fences
+  // its own initialisations), while warp 1 allocates tensor memory.
+  if (warp == 0) {
+    if (lane < 8) {
+      mbar_init(bar(kBarFull + lane), 1);
+      mbar_init(bar(kBarEmpty + lane), 1);
+      mbar_init(bar(kBarAFull + lane), 1);
+      mbar_init(bar(kBarAEmpty + lane), 1);
+    } else if (lane < 12) {
+      mbar_init(bar(kBarRFull + lane - 8), 1);
+      mbar_init(bar(kBarREmpty + lane - 8), 128);
+    } else if (lane == 12) {
+      mbar_init(bar(kBarWFull), 1);
+      mbar_init(bar(kBarWEmpty), SPLIT ? 2 : 1);
+      mbar_init(bar(kBarCFull), 1);
+      mbar_init(bar(kBarCFull + 1), 1);
+    } else if (lane == 13) {
+      mbar_init(bar(kBarPFull), 128);
+      mbar_init(bar(kBarPEmpty), 1);
+      mbar_init(bar(kBarPFull1), 128);
+      mbar_init(bar(kBarPEmpty1), 1);
+    } else if (lane == 14) {
+      mbar_init(bar(kBarEpiSync), 128);
+      mbar_init(bar(kBarDrain), 1);
+      mbar_init(bar(kBarDrain2), 1);
+      *abort_flag = 0;
+    }
+    if (lane < 15) fence_barrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), p.tmem_cols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  BoundedWait bw{abort_flag, p.status, p.budget_ns, kTimeoutCode};
+
   grid_launch_dependents();
   grid_dependency_wait();
   const int nph = NPH_FIXED + p.npass;

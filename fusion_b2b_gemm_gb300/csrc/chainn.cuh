@@ -222,38 +222,19 @@ __global__ void __launch_bounds__(kChainNThreads, 1)
   const int S = p.S;
   const bool wk = p.w_kmajor != 0;  // tf32 weights transposed (K-major)
 
-  if (threadIdx.x == 0) {
-    for (int i = 0; i < 16; ++i) {
-      mbar_init(bar(knFull + i), 1);
-      mbar_init(bar(knEmpty + i), 1);
-    }
-    mbar_init(bar(knCFull), 1);
-    for (int i = 0; i < 4; ++i) mbar_init(bar(knCFull0 + i), 1);
-    for (int i = 0; i < 8; ++i) mbar_init(bar(knPChunk + i), 2);
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(bar(knRFull + i), 1);
-      mbar_init(bar(knREmpty + i), 2);
-    }
-    mbar_init(bar(knDrain), 1);
-    *abort_flag = 0;
-    *reinterpret_cast<volatile uint32_t*>(gbase + p.off_bar + 8 * knSlotReady) = 0u;
-    fence_barrier_init();
+  // Before waiting for the previous kernel in the stream, and while the
+  // other warps set up barriers and tensor memory, one thread pulls the first
+  // unit's A into L2 (the TMA prefetch instructions take a good part of a
+  // microsecond to issue).  A may be that kernel's output, but a prefetch
+  // touches L2 only, where its writes land too, and every load into shared
+  // memory comes after the wait, so no stale value is read.  At most four K
+  // panels (more only compete with that kernel's tail).
+  if (warp == 3 && lane == 0) {
+    prefetch_tmap(&maps.a);
+    for (int s = 0; s < S; ++s) prefetch_tmap(&maps.w[s]);
+    prefetch_tmap(&maps.out);
   }
-  if (warp == 1) {
-    tmem_alloc<CG>(smem_u32(tmem_slot), kCols);
-    tmem_relinquish<CG>();
-  }
-  tc_fence_before();
-  __syncthreads();
-  cluster_sync();  // the peer's barriers exist before anything arrives on them
-  tc_fence_after();
-  const uint32_t tmem_base = *tmem_slot;
-  // Before waiting for the previous kernel in the stream, pull the first
-  // unit's A into L2.  A may be that kernel's output, but a prefetch touches
-  // L2 only, where its writes land too, and every load into shared memory
-  // comes after the wait, so no stale value is read.  At most four K panels
-  // (more only compete with that kernel's tail).
-  if (warp == 0 && lane == 0 && (blockIdx.x >> 1) < static_cast<unsigned>(p.total_tiles)) {
+  if (warp == 3 && lane == 0 && (blockIdx.x >> 1) < static_cast<unsigned>(p.total_tiles)) {
     const ChainNUnit c = chainn_unit(p, static_cast<int>(blockIdx.x >> 1), static_cast<int>(gridDim.x >> 1), 0);
     const int m0 = c.mt * 256 + static_cast<int>(rank) * 128;
     const int npf = p.kpan[0] < 4 ? p.kpan[0] : 4;
@@ -272,6 +253,37 @@ __global__ void __launch_bounds__(kChainNThreads, 1)
       }
     }
   }
+  // Barriers, set up by the lanes of warp 0 in parallel (each lane fences
+  // its own initialisations), while warp 1 allocates tensor memory.
+  if (warp == 0) {
+    if (lane < 16) {
+      mbar_init(bar(knFull + lane), 1);
+      mbar_init(bar(knEmpty + lane), 1);
+    } else if (lane < 24) {
+      mbar_init(bar(knPChunk + lane - 16), 2);
+    } else if (lane < 28) {
+      mbar_init(bar(knCFull0 + lane - 24), 1);
+    } else if (lane < 30) {
+      mbar_init(bar(knRFull + lane - 28), 1);
+      mbar_init(bar(knREmpty + lane - 28), 2);
+    } else if (lane == 30) {
+      mbar_init(bar(knCFull), 1);
+      mbar_init(bar(knDrain), 1);
+    } else {
+      *abort_flag = 0;
+      *reinterpret_cast<volatile uint32_t*>(gbase + p.off_bar + 8 * knSlotReady) = 0u;
+    }
+    if (lane < 31) fence_barrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc<CG>(smem_u32(tmem_slot), kCols);
+    tmem_relinquish<CG>();
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();  // the peer's barriers exist before anything arrives on them
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
   grid_launch_dependents();
   grid_dependency_wait();
 

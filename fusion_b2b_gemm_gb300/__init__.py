@@ -21,7 +21,7 @@ __all__ = [
     "b2b_plan_destroy",
     "b2b_plan_device_status", "b2b_plan_set_wait_budget", "b2b_plan_set_debug", "b2b_plan_info",
     "b2b_status_string", "b2b_coordination_matrix", "b2b_probe_operand_image",
-    "b2b_probe_operand_layout", "b2b_probe_f64_rearrange", "b2b_run_tf32_noalloc", "coordination_matrix",
+    "b2b_probe_operand_layout", "b2b_schedule_table", "b2b_probe_f64_rearrange", "b2b_run_tf32_noalloc", "coordination_matrix",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -69,6 +69,7 @@ def _load() -> ctypes.CDLL:
         "b2b_coordination_matrix": [i32, i32, ip, ip, ip, ip, ip],
         "b2b_probe_operand_image": [i32, i32, P, P, P],
         "b2b_probe_operand_layout": [i32, i32, i32, i32, P, P, P],
+        "b2b_schedule_table": [i32, ctypes.POINTER(i64), i32, ctypes.POINTER(i64), i32],
         "b2b_probe_f64_rearrange": [i32, P, P, P],
         "b2b_run_tf32_noalloc": [i64, i64, i64, i64, i64, P, P, P, P, P],
     }
@@ -98,6 +99,7 @@ b2b_status_string = _lib.b2b_status_string
 b2b_coordination_matrix = _lib.b2b_coordination_matrix
 b2b_probe_operand_image = _lib.b2b_probe_operand_image
 b2b_probe_operand_layout = _lib.b2b_probe_operand_layout
+b2b_schedule_table = _lib.b2b_schedule_table
 b2b_probe_f64_rearrange = _lib.b2b_probe_f64_rearrange
 b2b_run_tf32_noalloc = _lib.b2b_run_tf32_noalloc
 
@@ -465,6 +467,15 @@ def probe_operand_image(dtype: str, acc):
 
 
 PROBE_TMEM16, PROBE_PAIR_CONVERTERS = 1, 2  # B2B_PROBE_*
+TABLE_REGION_USE, TABLE_PAIR_UNITS, TABLE_PAIR_REGIONS = 1, 2, 3  # B2B_TABLE_*
+
+
+def schedule_table(table: int, args: Sequence[int], nout: int):
+    """One of the kernels' scheduling tables, evaluated on the host (test support)."""
+    a = (ctypes.c_int64 * max(1, len(args)))(*args)
+    out = (ctypes.c_int64 * nout)()
+    _check(_lib.b2b_schedule_table(table, a, len(args), out, nout), "b2b_schedule_table")
+    return list(out)
 
 
 def probe_operand_layout(dtype: str, form: int, acc, region: int = 0):

@@ -1213,6 +1213,74 @@ b2b_status_t b2b_probe_operand_layout(b2b_dtype_t dtype, int form, int width, in
   return B2B_OK;
 }
 
+b2b_status_t b2b_schedule_table(int table, const int64_t* args, int nargs, int64_t* out, int nout) {
+  if (!args || !out || nout < 1) return B2B_ERR_INVALID_ARG;
+  switch (table) {
+    case B2B_TABLE_REGION_USE: {
+      // args: S, npass, nz, lookahead, tiles; out: (region, use) of every
+      // phase of every tile, tile-major
+      if (nargs != 5) return B2B_ERR_INVALID_ARG;
+      const int S = static_cast<int>(args[0]), tiles = static_cast<int>(args[4]);
+      ChainParams c;
+      std::memset(&c, 0, sizeof(c));
+      c.npass = static_cast<int>(args[1]);
+      c.nz = static_cast<int>(args[2]);
+      c.lookahead = static_cast<int>(args[3]);
+      if (S < 1 || S > 3 || c.npass < 1 || tiles < 0) return B2B_ERR_INVALID_ARG;
+      const int nph = S - 1 + c.npass;
+      if (static_cast<int64_t>(tiles) * nph * 2 > nout) return B2B_ERR_INVALID_ARG;
+      for (int it = 0; it < tiles; ++it)
+        for (int ph = 0; ph < nph; ++ph) {
+          int r;
+          uint32_t u;
+          region_use(c, S, it, ph, r, u);
+          out[2 * (it * nph + ph)] = r;
+          out[2 * (it * nph + ph) + 1] = u;
+        }
+      return B2B_OK;
+    }
+    case B2B_TABLE_PAIR_UNITS: {
+      // args: total_tiles, m_tiles, npass, split, ncl, cid; out[0] = the
+      // cluster's unit count, then (batch, tile, p0, p1) per unit
+      if (nargs != 6) return B2B_ERR_INVALID_ARG;
+      ChainNParams c;
+      std::memset(&c, 0, sizeof(c));
+      c.total_tiles = static_cast<int>(args[0]);
+      c.m_tiles = static_cast<int>(args[1]);
+      c.npass = static_cast<int>(args[2]);
+      c.split = static_cast<int>(args[3]);
+      const int ncl = static_cast<int>(args[4]), cid = static_cast<int>(args[5]);
+      if (c.m_tiles < 1 || ncl < 1 || cid < 0 || cid >= ncl) return B2B_ERR_INVALID_ARG;
+      const int n = chainn_units(c, cid, ncl);
+      if (1 + 4 * static_cast<int64_t>(n) > nout) return B2B_ERR_INVALID_ARG;
+      out[0] = n;
+      for (int i = 0; i < n; ++i) {
+        const ChainNUnit u = chainn_unit(c, cid, ncl, i);
+        out[1 + 4 * i] = u.b;
+        out[2 + 4 * i] = u.mt;
+        out[3 + 4 * i] = u.p0;
+        out[4 + 4 * i] = u.p1;
+      }
+      return B2B_OK;
+    }
+    case B2B_TABLE_PAIR_REGIONS: {
+      // args: accumulator widths in the order they are taken; out: the
+      // region each starts in (RegionCursor), then for each the tensor-memory
+      // column of its columns 0, 128, 256, 384 (tmem_col)
+      if (nargs < 1 || static_cast<int64_t>(nargs) * 5 > nout) return B2B_ERR_INVALID_ARG;
+      RegionCursor rc;
+      for (int i = 0; i < nargs; ++i) {
+        const uint32_t r0 = rc.take(static_cast<int>(args[i]));
+        out[5 * i] = r0;
+        for (int q = 0; q < 4; ++q) out[5 * i + 1 + q] = tmem_col(r0, 128 * q);
+      }
+      return B2B_OK;
+    }
+    default:
+      return B2B_ERR_INVALID_ARG;
+  }
+}
+
 b2b_status_t b2b_probe_f64_rearrange(int tiles, const double* cfrag, double* afrag,
                                      b2b_stream_t stream) {
   if (!cfrag || !afrag || tiles < 1 || tiles > 8) return B2B_ERR_INVALID_ARG;

@@ -113,11 +113,11 @@ struct ChainNMaps {
 struct ChainNUnit {
   int b, mt, p0, p1;  // batch, 256-row tile, passes [p0, p1) of the last GEMM
 };
-__device__ __forceinline__ int chainn_units(const ChainNParams& p, int cid, int ncl) {
+__host__ __device__ __forceinline__ int chainn_units(const ChainNParams& p, int cid, int ncl) {
   if (p.split > 0) return p.total_tiles / ncl + (cid < 2 * p.split ? 1 : 0);
   return cid < p.total_tiles ? (p.total_tiles - cid + ncl - 1) / ncl : 0;
 }
-__device__ __forceinline__ ChainNUnit chainn_unit(const ChainNParams& p, int cid, int ncl, int i) {
+__host__ __device__ __forceinline__ ChainNUnit chainn_unit(const ChainNParams& p, int cid, int ncl, int i) {
   int tile, p0 = 0, p1 = p.npass;
   if (p.split > 0 && cid < 2 * p.split) {
     if (i == 0) {
@@ -151,13 +151,13 @@ struct integral_constant_int {
 
 struct RegionCursor {
   uint32_t last = 1;
-  __device__ __forceinline__ uint32_t take(int width) {
+  __host__ __device__ __forceinline__ uint32_t take(int width) {
     const uint32_t r0 = last ^ 1u;
     last = width <= 256 ? r0 : r0 ^ 1u;
     return r0;
   }
 };
-__device__ __forceinline__ uint32_t tmem_col(uint32_t r0, int c) {
+__host__ __device__ __forceinline__ uint32_t tmem_col(uint32_t r0, int c) {
   return ((((static_cast<uint32_t>(c) >> 8) ^ r0) & 1u) << 8) | (static_cast<uint32_t>(c) & 255u);
 }
 

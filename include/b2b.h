@@ -260,6 +260,30 @@ b2b_status_t b2b_probe_operand_layout(b2b_dtype_t dtype, int form, int width, in
                                       void* out, b2b_stream_t stream);
 
 /*
+ * Scheduling tables of the kernels (test support, host only, no GPU
+ * needed): the same host-and-device functions the kernels walk, evaluated
+ * on the host, so that the CPU models of the kernels' barrier protocols can
+ * be checked against them.  args / out are host arrays of nargs / nout
+ * integers.
+ *   B2B_TABLE_REGION_USE (one-CTA kernel): args S, npass, nz, lookahead,
+ *     tiles; out receives (region, use count) for every phase of every
+ *     tile, tile-major, 2 * tiles * (S - 1 + npass) integers.
+ *   B2B_TABLE_PAIR_UNITS (CTA-pair kernel): args total_tiles, m_tiles,
+ *     npass, split, clusters, cluster; out receives the cluster's unit count
+ *     and (batch, 256-row tile, first pass, end pass) of each unit.
+ *   B2B_TABLE_PAIR_REGIONS (CTA-pair kernel): args the widths of successive
+ *     accumulators; out receives, per accumulator, the tensor-memory region
+ *     it starts in and the tensor-memory column of its columns 0, 128, 256
+ *     and 384 (5 integers each).
+ * Returns B2B_ERR_INVALID_ARG for an unknown table, bad arguments or too
+ * small an `out`.
+ */
+#define B2B_TABLE_REGION_USE 1
+#define B2B_TABLE_PAIR_UNITS 2
+#define B2B_TABLE_PAIR_REGIONS 3
+b2b_status_t b2b_schedule_table(int table, const int64_t* args, int nargs, int64_t* out, int nout);
+
+/*
  * Register probe of the fp64 rearrangement (test support).  One warp loads
  * cfrag[lane][tiles*2] (device, the m8n8k4 accumulator fragments of `tiles`
  * 8-column tiles, lane-major) into registers, performs the shuffle rounds

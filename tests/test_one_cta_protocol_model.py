@@ -18,6 +18,8 @@ its own parity formulas beside an independent count of the completion each
 wait means; random interleavings must finish without a barrier ever being
 two phases ahead of a waiter.  The ring stages (A and weight panels) are
 left out: they are plain rings between the producer and the MMA issuers.
+The region map (region_use) is checked against the kernel's own function
+(evaluated by the library on the host, b2b_schedule_table).
 """
 import random
 
@@ -319,3 +321,23 @@ def test_the_model_sees_a_missing_operand_release():
     roles = {"mma": bad_mma(p, 2, [0, 0, 0]), "epi": epilogue(p, 2, [0, 0, 0]), "conv": converters(p, 2, [0, 0, 0])}
     err = run_roles(roles, lambda k: 1, 0)
     assert err is not None and err.startswith("deadlock")
+
+
+def test_region_use_is_the_kernels_own():
+    """The model's region_use is the kernel's region_use() (evaluated by the
+    library on the host), for every mode the host selects."""
+    b2b = pytest.importorskip("fusion_b2b_gemm_gb300")
+    tiles = 7
+    for S in (1, 2, 3):
+        for npass in range(1, 5):
+            for nz in (0, 1, 2):
+                for lookahead in ((0, 1) if S == 2 else (0,)):
+                    nph = S - 1 + npass
+                    got = b2b.schedule_table(b2b.TABLE_REGION_USE, [S, npass, nz, lookahead, tiles],
+                                             2 * tiles * nph)
+                    p = {"npass": npass, "nz": nz, "lookahead": lookahead}
+                    want = []
+                    for it in range(tiles):
+                        for ph in range(nph):
+                            want += list(region_use(p, S, it, ph))
+                    assert got == want, (S, npass, nz, lookahead)

@@ -23,7 +23,10 @@ next to an independent count of which completion each wait is meant to see.
 Random interleavings of the roles must always finish, every wait must ask
 for the parity of the completion it means, and no barrier may ever be two
 phases ahead of a waiter.  Ring slots (producer, watcher) are left out: they
-form a plain ring whose only partner is the MMA thread.
+form a plain ring whose only partner is the MMA thread.  The unit list, the
+region cursor and the column map used here are checked against the kernel's
+own functions (evaluated by the library on the host, b2b_schedule_table), so
+the model cannot drift from the kernel unnoticed in those.
 """
 import random
 
@@ -325,3 +328,30 @@ def test_the_model_sees_a_planted_deadlock():
 
     err = run_model(plan, units, 0, cta=stuck_cta)
     assert err is not None and err.startswith("deadlock")
+
+
+def test_unit_list_and_region_map_are_the_kernels_own():
+    """The model's unit list, region cursor and column map are the kernel's
+    chainn_units/chainn_unit, RegionCursor and tmem_col (evaluated by the
+    library on the host)."""
+    b2b = pytest.importorskip("fusion_b2b_gemm_gb300")
+    for total, ncl, npass, split in [(256, 76, 2, 28), (256, 76, 1, 0), (7, 3, 4, 1), (5, 8, 2, 0),
+                                     (64, 64, 1, 0), (300, 76, 3, 0), (77, 76, 2, 1), (9, 4, 2, 1)]:
+        m_tiles = 4
+        units = units_of(total, ncl, npass, split)
+        for cid in range(ncl):
+            got = b2b.schedule_table(b2b.TABLE_PAIR_UNITS, [total, m_tiles, npass, split, ncl, cid],
+                                     1 + 4 * (total // ncl + 2))
+            n = got[0]
+            assert n == len(units[cid]), (total, ncl, npass, split, cid)
+            for i, (tile, p0, p1) in enumerate(units[cid]):
+                assert got[1 + 4 * i: 5 + 4 * i] == [tile // m_tiles, tile % m_tiles, p0, p1]
+    rng = random.Random(3)
+    for _ in range(50):
+        widths = [rng.choice((128, 256, 384, 512)) for _ in range(rng.randint(1, 12))]
+        got = b2b.schedule_table(b2b.TABLE_PAIR_REGIONS, widths, 5 * len(widths))
+        rc = RegionCursor()
+        for i, w in enumerate(widths):
+            r0 = rc.take(w)
+            assert got[5 * i] == r0
+            assert got[5 * i + 1: 5 * i + 5] == [tmem_col(r0, 128 * q) for q in range(4)]

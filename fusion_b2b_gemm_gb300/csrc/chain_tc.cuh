@@ -489,6 +489,9 @@ __global__ void __launch_bounds__(kChainThreads, 1)
   const uint32_t tmem_base = *tmem_slot;
 
   BoundedWait bw{abort_flag, p.status, p.budget_ns, kTimeoutCode};
+  // L2 policy of the streams read or written once (resident-weight A tiles,
+  // the output)
+  const uint64_t pol_stream = l2_policy_evict_first();
 
   grid_launch_dependents();
   grid_dependency_wait();
@@ -695,7 +698,9 @@ __global__ void __launch_bounds__(kChainThreads, 1)
           for (int q = 0; q < ppst && !drop; ++q) {
             const int kb = kb0 + q;
             if constexpr (RES) {
-              tma_load_3d(dst + q * kPanelBytes, &tmA, fb, kb * CK, m0, b);
+              // A is read once: first out of L2 (measured with the output
+              // stores likewise hinted: batched_f16 24.0 -> 23.4 us)
+              tma_load_3d_hint(dst + q * kPanelBytes, &tmA, fb, kb * CK, m0, b, pol_stream);
             } else {
               if (a_here) tma_load_3d(dst, &tmA, fb, kb * CK, m0, b);
               if (W_KMAJOR) {
@@ -1003,7 +1008,8 @@ __global__ void __launch_bounds__(kChainThreads, 1)
           }
           named_bar_sync(1, 128);
           if (elected && ok) {
-            tma_store_3d(&tmOut, stg, n0 + j * OBOX_N, m0, b);
+            // (the output is not read again here: first out of L2)
+            tma_store_3d_hint(&tmOut, stg, n0 + j * OBOX_N, m0, b, pol_stream);
             bulk_commit();
             if (p.nstg == 1 && !in_ring) bulk_wait_read<0>();
           }

@@ -107,6 +107,11 @@ EXACT = [
     # a tf32 chain with more 128-row tiles than SMs runs on CTA pairs, its
     # intermediate kept in tensor memory (ragged widths)
     wl.Workload("x_tf32_pairs", "tf32", 4, 5000, 96, (200, 136), "int", 2, 87),
+    # tf32 weights read as stored with widths that are not a multiple of 32
+    # columns (one 32-column box at a time, the last one partly past N): the
+    # one-CTA kernel and the first GEMM of a mixed-type cascade
+    wl.Workload("x_tf32_ragged", "tf32", 2, 300, 60, (200, 136), "int", 2, 93),
+    wl.Workload("x_tf32_bf16_ragged", "tf32_bf16", 1, 300, 36, (72, 40, 104), "int", 1, 94),
 ]
 
 

@@ -204,8 +204,9 @@ std::vector<int> res_schedule(int64_t batch, int64_t m_tiles, int G);
 // Cascades of 16-bit GEMMs on CTA pairs (chainn_kernel): 256-row tiles,
 // intermediates padded to a multiple of 128 columns (at most 512), every GEMM
 // in passes of at most 256 columns; shared memory holds the operand image of
-// the widest intermediate, two staging buffers per epilogue warp, and the
-// ring of 16 KB slots in what is left.
+// the widest intermediate (none when the intermediates stay in tensor
+// memory), two staging buffers per epilogue warp, and the ring of 16 KB
+// slots in what is left.
 b2b_status_t setup_chainn(b2b_plan_s* p) {
   const int S = p->stages;
   p->sn = true;
@@ -247,7 +248,11 @@ b2b_status_t setup_chainn(b2b_plan_s* p) {
   c.npass = static_cast<int>((p->N[S - 1] + p->nf - 1) / p->nf);
   p->n1p = c.wpad[0];
   p->n2p = S >= 3 ? c.wpad[1] : 0;
-  const uint32_t p_bytes = pt ? 0u : 256u * static_cast<uint32_t>(wmax);
+  // 16-bit intermediates of at most 256 columns stay in tensor memory,
+  // packed where they were accumulated, when the last GEMM runs in one pass
+  // (a second pass would take the region of the intermediate it reads)
+  c.ptm = (!pt && wmax <= 256 && c.npass == 1) ? 1 : 0;
+  const uint32_t p_bytes = (pt || c.ptm) ? 0u : 256u * static_cast<uint32_t>(wmax);
   // the rest of shared memory: ring slots of 16 KB (an A panel or a weight
   // half panel each), at most sixteen, after one or two 4 KB staging buffers
   // per epilogue warp (two, unless one buffer buys a ring slot in a ring of

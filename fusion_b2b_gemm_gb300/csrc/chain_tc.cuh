@@ -231,12 +231,12 @@ __device__ __forceinline__ void rearrange_accumulator(uint32_t tsrc, int width, 
 
 // 16-bit intermediate kept in tensor memory as the A operand of the next
 // GEMM: the accumulator row is rounded and packed in place, two K elements
-// per 32-bit column (even K in the low half), so K columns of fp32 become
-// K/2 columns of the operand starting at the region's first column.  Chunk
-// c0 is read before its packed form is written to columns [c0/2, c0/2+32),
-// which never reach an unread chunk.
+// per 32-bit column (even K in the low half), so `width` columns of fp32 at
+// tsrc become width/2 columns of the operand at tdst (tdst <= tsrc, in the
+// same lanes).  Chunk c0 is read before its packed form is written to
+// columns [tdst + c0/2, tdst + c0/2 + 32), which never reach an unread chunk.
 template <int IN>
-__device__ __forceinline__ void rearrange_accumulator_tmem16(uint32_t tsrc, int width) {
+__device__ __forceinline__ void rearrange_accumulator_tmem16(uint32_t tsrc, int width, uint32_t tdst) {
   using namespace ptx;
 #pragma unroll 1
   for (int c0 = 0; c0 < width; c0 += 64) {
@@ -250,9 +250,13 @@ __device__ __forceinline__ void rearrange_accumulator_tmem16(uint32_t tsrc, int 
       w[16 + i] =
           (IN == kInF16) ? pack_f16x2(v1[2 * i], v1[2 * i + 1]) : pack_bf16x2(v1[2 * i], v1[2 * i + 1]);
     }
-    tmem_st32(tsrc + static_cast<uint32_t>(c0 / 2), w);
+    tmem_st32(tdst + static_cast<uint32_t>(c0 / 2), w);
   }
   tmem_wait_st();
+}
+template <int IN>
+__device__ __forceinline__ void rearrange_accumulator_tmem16(uint32_t tsrc, int width) {
+  rearrange_accumulator_tmem16<IN>(tsrc, width, tsrc);
 }
 
 // Warp-uniform bounded wait: the warp goes on only if every lane saw the phase.

@@ -91,6 +91,11 @@ struct ChainNParams {
   uint32_t off_ring, off_p, off_stg, off_bar;
   int w_merged;              // bit s: weight s is read as one 4-D box per half panel
   int split;                 // leftover tiles whose passes are split between two clusters
+  int ptm;                   // 16-bit intermediates packed in tensor memory (two K per
+                             // 32-bit column, in place in their accumulator's region) and
+                             // read from there by the next GEMM; no operand image.  Plans
+                             // set it when every intermediate is at most 256 columns wide
+                             // and the last GEMM runs in one pass.
   int w_kmajor;              // tf32 weights arrive transposed ([N][K], K-major) instead of as
                              // stored ([K][N], MN-major with 32-byte swizzle atoms)
   uint32_t debug;            // test support: bit 0 = the first ring slot is never filled
@@ -221,6 +226,7 @@ __global__ void __launch_bounds__(kChainNThreads, 1)
   const bool leader = (rank == 0);
   const int S = p.S;
   const bool wk = p.w_kmajor != 0;  // tf32 weights transposed (K-major)
+  const bool ptm = !PT && p.ptm != 0;  // 16-bit intermediates packed in tensor memory
 
   // Before waiting for the previous kernel in the stream, and while the
   // other warps set up barriers and tensor memory, one thread pulls the first
@@ -485,18 +491,37 @@ __global__ void __launch_bounds__(kChainNThreads, 1)
             mma_ts<true, CG>(d, p_tmem + static_cast<uint32_t>(kb * 32 + kk * 8), tb0 + kk * tbs, idesc,
                              kk ? 1u : acc0);
         } else if constexpr (npan == 2) {
+          if (ptm) {
+            // the intermediate packed in tensor memory: K panel kb is its
+            // columns [32 kb, 32 kb + 32), 8 per MMA
 #pragma unroll
-          for (int kk = 0; kk < 2 * (CK / KSTEP); ++kk) {
-            const uint32_t pa = static_cast<uint32_t>(kk >> 2), ks = static_cast<uint32_t>(kk & 3);
-            mma_ss<false, CG>(d, desc_sw128(sa + pa * kPanelBytes + ks * 32u, 16u, 1024u),
-                              desc_sw128(wb + pa * WBOX_BYTES + ks * KSTEP * 128u, WBOX_BYTES, 1024u), idesc,
-                              kk ? 1u : acc0);
+            for (int kk = 0; kk < 2 * (CK / KSTEP); ++kk) {
+              const uint32_t pa = static_cast<uint32_t>(kk >> 2), ks = static_cast<uint32_t>(kk & 3);
+              mma_ts<false, CG>(d, p_tmem + static_cast<uint32_t>(kb * 32) + pa * 32u + ks * 8u,
+                                desc_sw128(wb + pa * WBOX_BYTES + ks * KSTEP * 128u, WBOX_BYTES, 1024u), idesc,
+                                kk ? 1u : acc0);
+            }
+          } else {
+#pragma unroll
+            for (int kk = 0; kk < 2 * (CK / KSTEP); ++kk) {
+              const uint32_t pa = static_cast<uint32_t>(kk >> 2), ks = static_cast<uint32_t>(kk & 3);
+              mma_ss<false, CG>(d, desc_sw128(sa + pa * kPanelBytes + ks * 32u, 16u, 1024u),
+                                desc_sw128(wb + pa * WBOX_BYTES + ks * KSTEP * 128u, WBOX_BYTES, 1024u), idesc,
+                                kk ? 1u : acc0);
+            }
           }
         } else {
+          if (!a_smem && ptm) {
 #pragma unroll
-          for (int kk = 0; kk < CK / KSTEP; ++kk)
-            mma_ss<false, CG>(d, desc_sw128(sa + kk * 32u, 16u, 1024u),
-                              desc_sw128(wb + kk * KSTEP * 128u, WBOX_BYTES, 1024u), idesc, kk ? 1u : acc0);
+            for (int kk = 0; kk < CK / KSTEP; ++kk)
+              mma_ts<false, CG>(d, p_tmem + static_cast<uint32_t>(kb * 32 + kk * 8),
+                                desc_sw128(wb + kk * KSTEP * 128u, WBOX_BYTES, 1024u), idesc, kk ? 1u : acc0);
+          } else {
+#pragma unroll
+            for (int kk = 0; kk < CK / KSTEP; ++kk)
+              mma_ss<false, CG>(d, desc_sw128(sa + kk * 32u, 16u, 1024u),
+                                desc_sw128(wb + kk * KSTEP * 128u, WBOX_BYTES, 1024u), idesc, kk ? 1u : acc0);
+          }
         }
       };
       // One stage: one K-panel group, or (pair) two consecutive ones, whose
@@ -630,8 +655,8 @@ __global__ void __launch_bounds__(kChainNThreads, 1)
     // Every tile: each intermediate accumulator into the operand image, in
     // 128-column chunks, by all eight warps (warp w reads TMEM lanes
     // 32 (w % 4) .. + 31; warps 2-5 take the low 64 columns of a chunk,
-    // warps 6-9 the high 64), then warps 6-9 store the passes of the last
-    // GEMM.  An intermediate's completion barrier also means that every
+    // warps 6-9 the high 64) -- or, with ptm, packed in place by warps 2-5 --
+    // then warps 6-9 store the passes of the last GEMM.  An intermediate's completion barrier also means that every
     // earlier MMA, and so every read of the image it overwrites, is done.
     const int q = warp & 3;
     const int row = q * 32 + lane;
@@ -671,7 +696,18 @@ __global__ void __launch_bounds__(kChainNThreads, 1)
             if (ok) tc_fence_after();
           }
           if (ok) {
-            convert_chunk_half<IN>(tmem_base, lane_off, r0, ch, h, row, p_img);
+            // packed in tensor memory by the four warps 2-5 (one per lane
+            // quadrant: the packing moves columns, which two warps on the
+            // same lanes could not share), or into the image by all eight
+            if (!ptm)
+              convert_chunk_half<IN>(tmem_base, lane_off, r0, ch, h, row, p_img);
+            else if (h == 0) {
+              // accumulator columns [128 ch, +128) packed into [64 ch, +64);
+              // chunks go in order, so no write reaches an unread column
+              const uint32_t treg = tmem_base + lane_off + (r0 << 8);
+              rearrange_accumulator_tmem16<IN>(treg + static_cast<uint32_t>(ch * 128), 128,
+                                               treg + static_cast<uint32_t>(ch * 64));
+            }
             tc_fence_before();
           }
           named_bar_sync(2, 256);

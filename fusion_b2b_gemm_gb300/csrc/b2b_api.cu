@@ -289,14 +289,14 @@ b2b_status_t setup_chainn(b2b_plan_s* p) {
 }
 
 // A two-GEMM tf32 chain runs on CTA pairs when both widths fit one 256-column
-// pass and the 128-row tiles outnumber the SMs: each SM then loads half of
+// pass and there are at least two 128-row tiles: each SM then loads half of
 // every weight panel (measured: 2 x 65536 rows 84.0 -> 60.6 us, 20480 rows
-// 27.3 -> 21.7 us).  With at most one tile per SM the time is the latency of
-// one tile's load -> GEMM -> round -> GEMM -> store chain, which pairs do not
-// shorten (16384 rows: 14.9 us either way), and the one-tile kernel stays.
+// 27.3 -> 21.7 us), and with at most one tile per SM the second GEMM, which
+// waits on its weight panels in the one-CTA kernel, runs at the tensor
+// pipe's rate (16384 rows: 13.5 -> 13.1 us).
 bool tf32_pairs(const b2b_plan_s* p) {
   return p->in_kind == kInTF32 && p->stages == 2 && p->N[0] <= 256 && p->N[1] <= 256 &&
-         p->batch * ((p->M + 127) / 128) > p->sms;
+         p->batch * ((p->M + 127) / 128) >= 2;
 }
 
 // Tiling of a tcgen05 chain of one or two GEMMs (chain_tc_kernel): padded

@@ -231,17 +231,30 @@ __global__ void __launch_bounds__(kChainNThreads, 1)
   // Before waiting for the previous kernel in the stream, and while the
   // other warps set up barriers and tensor memory, one thread pulls the first
   // unit's A into L2 (the TMA prefetch instructions take a good part of a
-  // microsecond to issue).  A may be that kernel's output, but a prefetch
+  // microsecond to issue).  In a tf32 chain whose cluster runs a single
+  // unit, where the set-up is on the critical path, its warp arrives on the
+  // cluster barrier first, so the barrier does not wait for the prefetches
+  // (16384 rows: set-up 1.9 -> 0.8 us, 13.5 -> 13.1 us per call; the 16-bit
+  // cascades, with several units per cluster, keep one barrier after the
+  // prefetches: the split one measured 1-3 % slower there).  A may be that
+  // kernel's output, but a prefetch
   // touches L2 only, where its writes land too, and every load into shared
   // memory comes after the wait, so no stale value is read.  At most four K
   // panels (more only compete with that kernel's tail).
+  // Work units (256-row tiles, or halves of their last GEMM) of this
+  // cluster.
+  const int cid = static_cast<int>(blockIdx.x >> 1);
+  const int ncl = static_cast<int>(gridDim.x >> 1);
+  const int t_count = chainn_units(p, cid, ncl);
+  const bool early = PT && t_count == 1;
+  if (warp == 3 && early) cluster_arrive();
   if (warp == 3 && lane == 0) {
     prefetch_tmap(&maps.a);
     for (int s = 0; s < S; ++s) prefetch_tmap(&maps.w[s]);
     prefetch_tmap(&maps.out);
   }
-  if (warp == 3 && lane == 0 && (blockIdx.x >> 1) < static_cast<unsigned>(p.total_tiles)) {
-    const ChainNUnit c = chainn_unit(p, static_cast<int>(blockIdx.x >> 1), static_cast<int>(gridDim.x >> 1), 0);
+  if (warp == 3 && lane == 0 && t_count > 0) {
+    const ChainNUnit c = chainn_unit(p, cid, ncl, 0);
     const int m0 = c.mt * 256 + static_cast<int>(rank) * 128;
     const int npf = p.kpan[0] < 4 ? p.kpan[0] : 4;
     for (int q = 0; q < npf; ++q) tma_prefetch_l2_3d(&maps.a, q * CK0, m0, c.b);
@@ -285,9 +298,17 @@ __global__ void __launch_bounds__(kChainNThreads, 1)
     tmem_alloc<CG>(smem_u32(tmem_slot), kCols);
     tmem_relinquish<CG>();
   }
+  // (every thread of both CTAs: the peer's barriers exist before anything
+  // arrives on them)
   tc_fence_before();
-  __syncthreads();
-  cluster_sync();  // the peer's barriers exist before anything arrives on them
+  if constexpr (PT) {
+    __syncwarp();
+    if (warp != 3 || !early) cluster_arrive();
+    cluster_wait();
+  } else {
+    __syncthreads();
+    cluster_sync();
+  }
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   grid_launch_dependents();
@@ -299,11 +320,7 @@ __global__ void __launch_bounds__(kChainNThreads, 1)
   BoundedWait bwm = bw;
   auto lbar = [&](int i) -> uint32_t { return mapa_shared(bar(i), 0); };
 
-  // Work units (256-row tiles, or halves of their last GEMM) of this
-  // cluster; this CTA's 128 rows of each.
-  const int cid = static_cast<int>(blockIdx.x >> 1);
-  const int ncl = static_cast<int>(gridDim.x >> 1);
-  const int t_count = chainn_units(p, cid, ncl);
+  // This CTA's 128 rows of each unit.
   auto row0 = [&](int mt) -> int { return mt * 256 + static_cast<int>(rank) * 128; };
   const uint32_t p_img = base + p.off_p;
   const int kpan_last = p.kpan[S - 1];

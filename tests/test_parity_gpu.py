@@ -87,6 +87,8 @@ EXACT = [
     wl.Workload("x_f16", "f16", 3, 257, 128, (128, 128), "int", 2, 12),
     wl.Workload("x_bf16_3", "bf16", 1, 300, 512, (256, 256, 512), "int", 1, 13),
     wl.Workload("x_tf32", "tf32", 1, 333, 256, (256, 256), "int", 2, 14),
+    # a single 128-row tile: the one-CTA kernel (two or more go to CTA pairs)
+    wl.Workload("x_tf32_one_tile", "tf32", 1, 128, 256, (256, 256), "int", 2, 95),
     wl.Workload("x_f64", "f64", 2, 77, 64, (64, 64), "int", 2, 15),
     # three-stage chains run as CTA pairs sharing each MMA (256-row tiles):
     # padded narrow widths, batches whose last pair tile is half past M, the
@@ -156,6 +158,7 @@ EDGES = [
     wl.Workload("k_tail_f16", "f16", 2, 140, 72, (128, 128), "normal_fanin", 1.0, 25),
     wl.Workload("n3_partial_bf16", "bf16", 1, 150, 512, (256, 256, 320), "normal_fanin", 1.0, 26),
     wl.Workload("ragged_tf32", "tf32", 1, 190, 256, (200, 136), "normal", 1.0 / 16, 27),
+    wl.Workload("ragged_tf32_one_tile", "tf32", 1, 77, 60, (200, 136), "normal", 1.0 / 16, 96),
     wl.Workload("m13_f64", "f64", 3, 13, 64, (64, 64), "uniform", 1.0, 28),
     wl.Workload("small_f64", "f64", 2, 40, 32, (32, 16), "uniform", 1.0, 29),
     wl.Workload("n1_192_f16", "f16", 2, 200, 64, (192, 136), "normal_fanin", 1.0, 30),
@@ -214,14 +217,16 @@ def test_edge_shapes(w):
     assert rel_err(got, want) <= TOL[w.dtype]
 
 
-def test_tf32_chains_take_pairs_only_past_one_tile_per_sm():
-    # one 128-row tile per SM or fewer: the one-CTA kernel; more: CTA pairs
-    # (384 threads, an even grid)
+def test_tf32_chains_take_pairs_from_two_tiles():
+    # a single 128-row tile, or a last GEMM wider than 256 columns: the
+    # one-CTA kernel; two tiles or more: CTA pairs (384 threads, an even grid)
     sms = torch.cuda.get_device_properties(0).multi_processor_count
-    one = b2b.Plan("tf32", 1, 128 * sms, 256, 256, 256).info()
-    many = b2b.Plan("tf32", 1, 128 * sms + 1, 256, 256, 256).info()
-    assert one["threads"] != 384
-    assert many["threads"] == 384 and many["grid"] % 2 == 0
+    one = b2b.Plan("tf32", 1, 128, 256, 256, 256).info()
+    wide = b2b.Plan("tf32", 1, 128 * sms, 256, 256, 384).info()
+    for m in (129, 128 * sms, 128 * sms + 1):
+        many = b2b.Plan("tf32", 1, m, 256, 256, 256).info()
+        assert many["threads"] == 384 and many["grid"] % 2 == 0
+    assert one["threads"] != 384 and wide["threads"] != 384
 
 
 def test_empty_chain_is_a_no_op():

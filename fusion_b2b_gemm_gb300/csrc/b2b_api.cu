@@ -204,9 +204,8 @@ std::vector<int> res_schedule(int64_t batch, int64_t m_tiles, int G);
 // Cascades of 16-bit GEMMs on CTA pairs (chainn_kernel): 256-row tiles,
 // intermediates padded to a multiple of 128 columns (at most 512), every GEMM
 // in passes of at most 256 columns; shared memory holds the operand image of
-// the widest intermediate (none when the intermediates stay in tensor
-// memory), two staging buffers per epilogue warp, and the ring of 16 KB
-// slots in what is left.
+// the widest intermediate that does not stay in tensor memory, two staging
+// buffers per epilogue warp, and the ring of 16 KB slots in what is left.
 b2b_status_t setup_chainn(b2b_plan_s* p) {
   const int S = p->stages;
   p->sn = true;
@@ -226,7 +225,6 @@ b2b_status_t setup_chainn(b2b_plan_s* p) {
   // tensor memory and the second GEMM runs in one pass
   const bool pt = p->in_kind == kInTF32;
   if (pt && (S != 2 || p->N[0] > 256 || p->N[1] > 256)) return B2B_ERR_UNSUPPORTED;
-  int wmax = 0;
   // 128-byte K panels: 64 16-bit or 32 tf32 elements
   const int ck = pt ? 32 : 64;
   c.kpan[0] = static_cast<int>(p->tf0 || pt ? (p->K + 31) / 32 : (p->K + 63) / 64);
@@ -242,17 +240,27 @@ b2b_status_t setup_chainn(b2b_plan_s* p) {
     // passes
     const int kps = (!pt && s > 0 && c.pw[s] == 128) ? 2 : 1;
     c.slots0 += (w / c.pw[s]) * (s == 0 ? 2 * c.kpan[s] : c.kpan[s] / kps);
-    wmax = std::max(wmax, w);
   }
   c.pw[S - 1] = p->nf;
   c.npass = static_cast<int>((p->N[S - 1] + p->nf - 1) / p->nf);
   p->n1p = c.wpad[0];
   p->n2p = S >= 3 ? c.wpad[1] : 0;
-  // 16-bit intermediates of at most 256 columns stay in tensor memory,
-  // packed where they were accumulated, when the last GEMM runs in one pass
-  // (a second pass would take the region of the intermediate it reads)
-  c.ptm = (!pt && wmax <= 256 && c.npass == 1) ? 1 : 0;
-  const uint32_t p_bytes = (pt || c.ptm) ? 0u : 256u * static_cast<uint32_t>(wmax);
+  // A 16-bit intermediate of at most 256 columns stays in tensor memory,
+  // packed where it was accumulated, unless the GEMM after next would
+  // overwrite its region while the next GEMM still reads it: a next
+  // intermediate wider than 256 columns takes both regions, and a second
+  // pass of the last GEMM takes the region of the last intermediate.  The
+  // operand image holds the others.
+  int wimg = 0;
+  c.ptm = 0;
+  for (int s = 0; s < S - 1; ++s) {
+    const bool next_fits = (s + 1 < S - 1) ? c.wpad[s + 1] <= 256 : c.npass == 1;
+    if (!pt && c.wpad[s] <= 256 && next_fits)
+      c.ptm |= 1 << s;
+    else
+      wimg = std::max(wimg, c.wpad[s]);
+  }
+  const uint32_t p_bytes = pt ? 0u : 256u * static_cast<uint32_t>(wimg);
   // the rest of shared memory: ring slots of 16 KB (an A panel or a weight
   // half panel each), at most sixteen, after one or two 4 KB staging buffers
   // per epilogue warp (two, unless one buffer buys a ring slot in a ring of

@@ -91,11 +91,13 @@ struct ChainNParams {
   uint32_t off_ring, off_p, off_stg, off_bar;
   int w_merged;              // bit s: weight s is read as one 4-D box per half panel
   int split;                 // leftover tiles whose passes are split between two clusters
-  int ptm;                   // 16-bit intermediates packed in tensor memory (two K per
-                             // 32-bit column, in place in their accumulator's region) and
-                             // read from there by the next GEMM; no operand image.  Plans
-                             // set it when every intermediate is at most 256 columns wide
-                             // and the last GEMM runs in one pass.
+  int ptm;                   // bit s: 16-bit intermediate s is packed in tensor memory (two
+                             // K per 32-bit column, in place in its accumulator's region)
+                             // and read from there by the next GEMM instead of from the
+                             // operand image.  Plans set it for an intermediate of at most
+                             // 256 columns whose region the GEMM after next may overwrite:
+                             // the next intermediate fits one region, or, for the last one,
+                             // the last GEMM runs in one pass.
   int w_kmajor;              // tf32 weights arrive transposed ([N][K], K-major) instead of as
                              // stored ([K][N], MN-major with 32-byte swizzle atoms)
   uint32_t debug;            // test support: bit 0 = the first ring slot is never filled
@@ -226,7 +228,6 @@ __global__ void __launch_bounds__(kChainNThreads, 1)
   const bool leader = (rank == 0);
   const int S = p.S;
   const bool wk = p.w_kmajor != 0;  // tf32 weights transposed (K-major)
-  const bool ptm = !PT && p.ptm != 0;  // 16-bit intermediates packed in tensor memory
 
   // Before waiting for the previous kernel in the stream, and while the
   // other warps set up barriers and tensor memory, one thread pulls the first
@@ -458,6 +459,9 @@ __global__ void __launch_bounds__(kChainNThreads, 1)
       // tf32 chains: the tensor-memory column of the intermediate the next
       // GEMM reads
       uint32_t p_tmem = 0;
+      // 16-bit chains: whether the intermediate the next GEMM reads is packed
+      // in tensor memory (at p_tmem) rather than in the operand image
+      bool a_tm = false;
       auto stage_ready = [&](uint32_t need) -> bool {
         if (seen >= consumed + need) return true;
         seen = ld_acquire_shared(ready);
@@ -508,7 +512,7 @@ __global__ void __launch_bounds__(kChainNThreads, 1)
             mma_ts<true, CG>(d, p_tmem + static_cast<uint32_t>(kb * 32 + kk * 8), tb0 + kk * tbs, idesc,
                              kk ? 1u : acc0);
         } else if constexpr (npan == 2) {
-          if (ptm) {
+          if (a_tm) {
             // the intermediate packed in tensor memory: K panel kb is its
             // columns [32 kb, 32 kb + 32), 8 per MMA
 #pragma unroll
@@ -528,7 +532,7 @@ __global__ void __launch_bounds__(kChainNThreads, 1)
             }
           }
         } else {
-          if (!a_smem && ptm) {
+          if (!a_smem && a_tm) {
 #pragma unroll
             for (int kk = 0; kk < CK / KSTEP; ++kk)
               mma_ts<false, CG>(d, p_tmem + static_cast<uint32_t>(kb * 32 + kk * 8),
@@ -645,6 +649,7 @@ __global__ void __launch_bounds__(kChainNThreads, 1)
           if (!ok) break;
           if (s > 0) tc_commit<CG>(bar(knCFull));
           p_tmem = tmem_base + (r0 << 8);
+          a_tm = !PT && ((p.ptm >> s) & 1);
           ++k;
         }
         if (!ok) break;
@@ -672,7 +677,7 @@ __global__ void __launch_bounds__(kChainNThreads, 1)
     // Every tile: each intermediate accumulator into the operand image, in
     // 128-column chunks, by all eight warps (warp w reads TMEM lanes
     // 32 (w % 4) .. + 31; warps 2-5 take the low 64 columns of a chunk,
-    // warps 6-9 the high 64) -- or, with ptm, packed in place by warps 2-5 --
+    // warps 6-9 the high 64) -- or, ptm bit s set, packed in place by warps 2-5 --
     // then warps 6-9 store the passes of the last GEMM.  An intermediate's completion barrier also means that every
     // earlier MMA, and so every read of the image it overwrites, is done.
     const int q = warp & 3;
@@ -716,7 +721,7 @@ __global__ void __launch_bounds__(kChainNThreads, 1)
             // packed in tensor memory by the four warps 2-5 (one per lane
             // quadrant: the packing moves columns, which two warps on the
             // same lanes could not share), or into the image by all eight
-            if (!ptm)
+            if (PT || !((p.ptm >> s) & 1))
               convert_chunk_half<IN>(tmem_base, lane_off, r0, ch, h, row, p_img);
             else if (h == 0) {
               // accumulator columns [128 ch, +128) packed into [64 ch, +64);

@@ -102,6 +102,11 @@ EXACT = [
     wl.Workload("x_f16_f32out_5", "f16_f32out", 1, 520, 16, (16, 16, 16, 16, 128), "int", 1, 20),
     wl.Workload("x_bf16_wide384", "bf16", 1, 300, 32, (384, 64), "int", 1, 41),
     wl.Workload("x_bf16_wide512_3", "bf16", 1, 260, 16, (512, 16, 256), "int", 1, 42),
+    # intermediates partly in tensor memory, partly in the operand image:
+    # the first (the next one fits a region) and the last (one final pass)
+    # are packed in tensor memory, the 256- and 384-column ones between go
+    # through shared memory
+    wl.Workload("x_bf16_5_mixed_homes", "bf16", 1, 300, 16, (128, 256, 384, 128, 256), "int", 1, 97),
     # mixed types: tf32 first GEMM (integers below 2^10 are exact in tf32),
     # then fp16 / bf16
     wl.Workload("x_tf32_f16_2", "tf32_f16", 2, 300, 64, (128, 64), "int", 2, 71),
@@ -111,8 +116,10 @@ EXACT = [
     wl.Workload("x_tf32_pairs", "tf32", 4, 5000, 96, (200, 136), "int", 2, 87),
     # tf32 weights read as stored with widths that are not a multiple of 32
     # columns (one 32-column box at a time, the last one partly past N): the
-    # one-CTA kernel and the first GEMM of a mixed-type cascade
+    # pair kernel, the one-CTA kernel (a single tile) and the first GEMM of a
+    # mixed-type cascade
     wl.Workload("x_tf32_ragged", "tf32", 2, 300, 60, (200, 136), "int", 2, 93),
+    wl.Workload("x_tf32_ragged_one_tile", "tf32", 1, 100, 60, (200, 136), "int", 2, 98),
     wl.Workload("x_tf32_bf16_ragged", "tf32_bf16", 1, 300, 36, (72, 40, 104), "int", 1, 94),
 ]
 

@@ -41,10 +41,14 @@ CASES = [
     wl.Workload("fail_mixed_bf16", "tf32_bf16", 1, 400, 64, (256, 128, 256), "normal_fanin", 1.0, 55),
     # resident weights over many batches: CTAs walk the batch-aware schedule
     wl.Workload("fail_sched_f16", "f16", 40, 2000, 128, (128, 128), "normal_fanin", 1.0, 56),
-    # one tile per CTA, output staged in the ring
+    # a tf32 chain on CTA pairs with one unit per cluster (the set-up barrier
+    # passed before the L2 prefetches are issued)
     wl.Workload("fail_one_tile_tf32", "tf32", 1, 4096, 128, (128, 256), "normal", 1.0 / 16, 57),
-    # a tf32 chain on CTA pairs (more 128-row tiles than SMs)
+    # a tf32 chain on CTA pairs, several units per cluster
     wl.Workload("fail_tf32_pairs", "tf32", 2, 10000, 64, (128, 128), "normal", 1.0 / 16, 58),
+    # the one-CTA tf32 kernel (a last GEMM wider than 256 columns), one tile
+    # per CTA, output staged in the ring
+    wl.Workload("fail_tf32_one_cta", "tf32", 1, 4096, 128, (128, 384), "normal", 1.0 / 16, 59),
 ]
 
 

@@ -467,7 +467,7 @@ def probe_operand_image(dtype: str, acc):
 
 
 PROBE_TMEM16, PROBE_PAIR_CONVERTERS = 1, 2  # B2B_PROBE_*
-TABLE_REGION_USE, TABLE_PAIR_UNITS, TABLE_PAIR_REGIONS = 1, 2, 3  # B2B_TABLE_*
+TABLE_REGION_USE, TABLE_PAIR_UNITS, TABLE_PAIR_REGIONS, TABLE_PAIR_TMEM_INTERMEDIATES = 1, 2, 3, 4  # B2B_TABLE_*
 
 
 def schedule_table(table: int, args: Sequence[int], nout: int):

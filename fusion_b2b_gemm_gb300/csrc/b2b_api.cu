@@ -201,6 +201,22 @@ namespace {
 
 std::vector<int> res_schedule(int64_t batch, int64_t m_tiles, int G);
 
+// Which intermediates of a pair-kernel cascade stay in tensor memory (bit s
+// for intermediate s, of padded width wpad[s]): a 16-bit intermediate of at
+// most 256 columns, unless the GEMM after next would overwrite its region
+// while the next GEMM still reads it (a next intermediate wider than 256
+// columns takes both regions; a second pass of the last GEMM takes the
+// region of the last intermediate).  tf32 chains keep theirs in tensor
+// memory in their own form.
+int chainn_tmem_mask(bool pt, int nint, const int* wpad, int npass) {
+  int mask = 0;
+  for (int s = 0; s < nint; ++s) {
+    const bool next_fits = (s + 1 < nint) ? wpad[s + 1] <= 256 : npass == 1;
+    if (!pt && wpad[s] <= 256 && next_fits) mask |= 1 << s;
+  }
+  return mask;
+}
+
 // Cascades of 16-bit GEMMs on CTA pairs (chainn_kernel): 256-row tiles,
 // intermediates padded to a multiple of 128 columns (at most 512), every GEMM
 // in passes of at most 256 columns; shared memory holds the operand image of
@@ -245,21 +261,12 @@ b2b_status_t setup_chainn(b2b_plan_s* p) {
   c.npass = static_cast<int>((p->N[S - 1] + p->nf - 1) / p->nf);
   p->n1p = c.wpad[0];
   p->n2p = S >= 3 ? c.wpad[1] : 0;
-  // A 16-bit intermediate of at most 256 columns stays in tensor memory,
-  // packed where it was accumulated, unless the GEMM after next would
-  // overwrite its region while the next GEMM still reads it: a next
-  // intermediate wider than 256 columns takes both regions, and a second
-  // pass of the last GEMM takes the region of the last intermediate.  The
-  // operand image holds the others.
+  // intermediates packed in tensor memory where they were accumulated; the
+  // operand image holds the others
+  c.ptm = chainn_tmem_mask(pt, S - 1, c.wpad, c.npass);
   int wimg = 0;
-  c.ptm = 0;
-  for (int s = 0; s < S - 1; ++s) {
-    const bool next_fits = (s + 1 < S - 1) ? c.wpad[s + 1] <= 256 : c.npass == 1;
-    if (!pt && c.wpad[s] <= 256 && next_fits)
-      c.ptm |= 1 << s;
-    else
-      wimg = std::max(wimg, c.wpad[s]);
-  }
+  for (int s = 0; s < S - 1; ++s)
+    if (!((c.ptm >> s) & 1)) wimg = std::max(wimg, c.wpad[s]);
   const uint32_t p_bytes = pt ? 0u : 256u * static_cast<uint32_t>(wimg);
   // the rest of shared memory: ring slots of 16 KB (an A panel or a weight
   // half panel each), at most sixteen, after one or two 4 KB staging buffers
@@ -1274,6 +1281,15 @@ b2b_status_t b2b_schedule_table(int table, const int64_t* args, int nargs, int64
         out[3 + 4 * i] = u.p0;
         out[4 + 4 * i] = u.p1;
       }
+      return B2B_OK;
+    }
+    case B2B_TABLE_PAIR_TMEM_INTERMEDIATES: {
+      // args: tf32 chain (0 / 1), last-GEMM passes, padded widths of the
+      // intermediates; out[0] = the mask of those kept in tensor memory
+      if (nargs < 3 || nargs - 2 > kMaxStages - 1) return B2B_ERR_INVALID_ARG;
+      int wpad[kMaxStages];
+      for (int s = 0; s < nargs - 2; ++s) wpad[s] = static_cast<int>(args[2 + s]);
+      out[0] = chainn_tmem_mask(args[0] != 0, nargs - 2, wpad, static_cast<int>(args[1]));
       return B2B_OK;
     }
     case B2B_TABLE_PAIR_REGIONS: {

@@ -275,12 +275,18 @@ b2b_status_t b2b_probe_operand_layout(b2b_dtype_t dtype, int form, int width, in
  *     accumulators; out receives, per accumulator, the tensor-memory region
  *     it starts in and the tensor-memory column of its columns 0, 128, 256
  *     and 384 (5 integers each).
+ *   B2B_TABLE_PAIR_TMEM_INTERMEDIATES (CTA-pair kernel): args 1 for a tf32
+ *     chain else 0, the last GEMM's pass count, then the padded widths of
+ *     the intermediates; out[0] receives the mask (bit s: intermediate s)
+ *     of the intermediates a plan keeps packed in tensor memory rather than
+ *     in the shared-memory operand image.
  * Returns B2B_ERR_INVALID_ARG for an unknown table, bad arguments or too
  * small an `out`.
  */
 #define B2B_TABLE_REGION_USE 1
 #define B2B_TABLE_PAIR_UNITS 2
 #define B2B_TABLE_PAIR_REGIONS 3
+#define B2B_TABLE_PAIR_TMEM_INTERMEDIATES 4
 b2b_status_t b2b_schedule_table(int table, const int64_t* args, int nargs, int64_t* out, int nout);
 
 /*

@@ -355,3 +355,44 @@ def test_unit_list_and_region_map_are_the_kernels_own():
             r0 = rc.take(w)
             assert got[5 * i] == r0
             assert got[5 * i + 1: 5 * i + 5] == [tmem_col(r0, 128 * q) for q in range(4)]
+
+
+def _regions(r0, width):
+    """Tensor-memory regions (0 = X, 1 = Y) an accumulator starting in r0 covers."""
+    return {tmem_col(r0, c) >> 8 for c in range(0, width, 128)}
+
+
+def test_intermediates_kept_in_tensor_memory_are_not_overwritten_while_read():
+    """The plan keeps a 16-bit intermediate packed in tensor memory exactly
+    when no accumulator written by the GEMM that reads it (the next
+    intermediate, or every pass of the last GEMM) covers its region; tf32
+    chains keep none in packed form.  The mask is the library's own
+    (chainn_tmem_mask through b2b_schedule_table); the regions come from this
+    model's region cursor."""
+    b2b = pytest.importorskip("fusion_b2b_gemm_gb300")
+    cases = [([256, 256], 2, 0b01), ([256, 256, 256], 1, 0b111), ([512], 1, 0), ([128, 256, 384, 128], 1, 0b1001),
+             ([128], 2, 0), ([128, 512, 128], 1, 0b100), ([256], 1, 0b1)]
+    rng = random.Random(11)
+    for _ in range(200):
+        ints = [rng.choice((128, 256, 384, 512)) for _ in range(rng.randint(1, 7))]
+        cases.append((ints, rng.randint(1, 4), None))
+    for ints, npass, expect in cases:
+        got = b2b.schedule_table(b2b.TABLE_PAIR_TMEM_INTERMEDIATES, [0, npass] + ints, 1)[0]
+        rc = RegionCursor()
+        starts = [rc.take(w) for w in ints]
+        passes = [rc.take(256) for _ in range(npass)]
+        want = 0
+        for s, w in enumerate(ints):
+            if w > 256:
+                continue
+            mine = _regions(starts[s], w)
+            if s + 1 < len(ints):
+                written = _regions(starts[s + 1], ints[s + 1])
+            else:
+                written = set().union(*(_regions(r, 256) for r in passes))
+            if not (mine & written):
+                want |= 1 << s
+        assert got == want, (ints, npass, got, want)
+        if expect is not None:
+            assert got == expect, (ints, npass, got)
+        assert b2b.schedule_table(b2b.TABLE_PAIR_TMEM_INTERMEDIATES, [1, npass] + ints, 1)[0] == 0

@@ -316,6 +316,14 @@ __global__ void __launch_bounds__(kChainNThreads, 1)
   grid_dependency_wait();
 
   BoundedWait bw{abort_flag, p.status, p.budget_ns, kTimeoutCode};
+  // The output is written with an L2 evict-first policy (three_stage_bf16
+  // 40.7 -> 40.4 us, mixed_tf32_bf16 35.9 -> 35.7 us); A is read with it
+  // only by a cluster with a single unit (the tf32 workload 13.1 -> 12.9
+  // us): with several units per cluster, whose next A is pulled into L2
+  // ahead, hinted A loads made every cascade slower (three_stage_bf16
+  // 40.7 -> 42.7 us).
+  const bool hint_a = t_count == 1;
+  const uint64_t pol_stream = l2_policy_evict_first();
   // Waits on barriers that threads of the peer CTA arrive on (the same
   // default-scope wait: the remote arrives are ordered by the barrier itself).
   BoundedWait bwm = bw;
@@ -356,7 +364,10 @@ __global__ void __launch_bounds__(kChainNThreads, 1)
         // test support: the very first slot is armed but never filled
         if (!((p.debug & 1u) && issued == 0)) {
           if (s < 0) {
-            tma_load_3d_pair(dst, &maps.a, fb, kb * CK0, m0, b);
+            if (hint_a)
+              tma_load_3d_pair_hint(dst, &maps.a, fb, kb * CK0, m0, b, pol_stream);
+            else
+              tma_load_3d_pair(dst, &maps.a, fb, kb * CK0, m0, b);
           } else {
             const CUtensorMap* wm = &maps.w[s];
             const int n0 = col0 + static_cast<int>(rank) * wcols;
@@ -791,7 +802,7 @@ __global__ void __launch_bounds__(kChainNThreads, 1)
           __syncwarp();
           // (the odd CTA's rows of the last tile may lie past M)
           if (lane == 0 && ok && mw < p.M) {
-            tma_store_3d(&maps.out, stg, j * NF + x * OBOX_N, mw, c.b);
+            tma_store_3d_hint(&maps.out, stg, j * NF + x * OBOX_N, mw, c.b, pol_stream);
             bulk_commit();
           }
           ++nbox;

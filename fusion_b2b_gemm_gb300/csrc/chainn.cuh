@@ -232,16 +232,17 @@ __global__ void __launch_bounds__(kChainNThreads, 1)
   // Before waiting for the previous kernel in the stream, and while the
   // other warps set up barriers and tensor memory, one thread pulls the first
   // unit's A into L2 (the TMA prefetch instructions take a good part of a
-  // microsecond to issue).  In a tf32 chain whose cluster runs a single
-  // unit, where the set-up is on the critical path, its warp arrives on the
-  // cluster barrier first, so the barrier does not wait for the prefetches
-  // (16384 rows: set-up 1.9 -> 0.8 us, 13.5 -> 13.1 us per call; the 16-bit
-  // cascades, with several units per cluster, keep one barrier after the
-  // prefetches: the split one measured 1-3 % slower there).  A may be that
-  // kernel's output, but a prefetch
+  // microsecond to issue).  A may be that kernel's output, but a prefetch
   // touches L2 only, where its writes land too, and every load into shared
   // memory comes after the wait, so no stale value is read.  At most four K
-  // panels (more only compete with that kernel's tail).
+  // panels (more only compete with that kernel's tail).  In a tf32 chain
+  // whose cluster runs a single unit, where the set-up is on the critical
+  // path, the prefetching warp arrives on the cluster barrier first, so the
+  // barrier does not wait for the prefetches (16384 rows: set-up 1.9 -> 0.8
+  // us, 13.5 -> 13.1 us per call; the 16-bit cascades, with several units
+  // per cluster, keep one barrier after the prefetches: the split one
+  // measured 1-3 % slower there).
+  //
   // Work units (256-row tiles, or halves of their last GEMM) of this
   // cluster.
   const int cid = static_cast<int>(blockIdx.x >> 1);

@@ -365,8 +365,10 @@ def test_full_size_sampled_rows(name):
 
 # ------------------------------------------------ seeded random shapes --
 
-def _random_cases(n=16, seed=2026):
-    """Cascades with random stage counts, widths, types and sizes (fixed seed)."""
+def _random_cases(n=16, seed=2026, narrow=False, first=100):
+    """Cascades with random stage counts, widths, types and sizes (fixed seed);
+    narrow: every width at most 256 columns (intermediates then mostly stay
+    in tensor memory)."""
     import random
     rng = random.Random(seed)
     cases = []
@@ -375,19 +377,20 @@ def _random_cases(n=16, seed=2026):
         S = rng.randint(2, 6)
         widths = []
         for s in range(S):
-            hi = 512 if s < S - 1 else 640
+            hi = 256 if narrow else (512 if s < S - 1 else 640)
             widths.append(8 * rng.randint(1, hi // 8))
         K = (4 if dtype.startswith("tf32") else 8) * rng.randint(1, 48)
         if not dtype.startswith("tf32"):
             K = 8 * rng.randint(1, 40)
         batch = rng.randint(1, 3)
         M = rng.randint(1, 1200)
-        cases.append(wl.Workload(f"rand{i}_{dtype}_s{S}", dtype, batch, M, K, tuple(widths),
-                                 "normal_fanin", 1.0, 100 + i))
+        cases.append(wl.Workload(f"rand{'n' if narrow else ''}{i}_{dtype}_s{S}", dtype, batch, M, K,
+                                 tuple(widths), "normal_fanin", 1.0, first + i))
     return cases
 
 
-@pytest.mark.parametrize("w", _random_cases(), ids=lambda w: w.name)
+@pytest.mark.parametrize("w", _random_cases() + _random_cases(8, 2027, narrow=True, first=120),
+                         ids=lambda w: w.name)
 def test_random_cascades(w):
     host = wl.make_inputs(w)
     dev = [t.cuda() for t in host]
